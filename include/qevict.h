@@ -1,0 +1,196 @@
+/*
+ * qevict.h — C ABI of the QEvict decode-time path on GB300 (sm_103a).
+ *
+ * QEvict ("QEvict: Recoverable Quantized KV Eviction for Attention-Drift-Robust
+ * Long-Context Decoding", arXiv 2608.05326) keeps each layer's history as
+ * contiguous windows in one of three tiers: Full (bf16), Quantized (INT2/INT4
+ * codes with fp16 scale/offset, a write-once ledger) or Evicted, under a byte
+ * budget.  Decoding attends over sink + Full + dequantised Quantized + recent
+ * tokens, accumulates a per-window attention score, and every Omega generated
+ * tokens re-ranks the windows and migrates them between tiers.
+ *
+ * Conventions for every entry point
+ *   - Pointers named d_* / the arena / every tensor argument are DEVICE
+ *     pointers unless stated otherwise; sizes are in bytes unless stated.
+ *   - The caller owns all device memory: the arena, inputs and outputs.  The
+ *     library never allocates device memory and keeps no pointer to inputs
+ *     after a call returns.  The cache handle is host memory owned by the
+ *     library (freed by qevict_destroy).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default)
+ *     and runs asynchronously; host-side argument checks are synchronous.
+ *   - Errors: QEVICT_EINVAL for bad arguments, QEVICT_EBUDGET when the budget
+ *     cannot hold the protected regions, QEVICT_ENOMEM for a too small arena,
+ *     QEVICT_ESCHEDULE for a routing call off the Omega cadence, QEVICT_ECUDA
+ *     when a launch fails, QEVICT_EDEVICE when a kernel recorded a fault in the
+ *     device status word (read by qevict_read_counters / qevict_check).  On an
+ *     error nothing is enqueued unless stated.
+ *   - Tensors are dense, row-major, bf16 (uint16 storage) unless stated.
+ *   - One cache serves `batch` sequences that decode in lockstep and all
+ *     `n_layers` layers; every (sequence, layer) pair is one independent "unit".
+ */
+#ifndef QEVICT_H
+#define QEVICT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *qevict_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  QEVICT_OK = 0,
+  QEVICT_EINVAL = 1,
+  QEVICT_EBUDGET = 2,
+  QEVICT_ENOMEM = 3,
+  QEVICT_ESCHEDULE = 4,
+  QEVICT_ECUDA = 5,
+  QEVICT_EDEVICE = 6
+} qevict_status;
+
+/* Sizes of one cache.  Semantics are per (sequence, layer); all units share them.
+ * Supported: d_head = 128; (window, bits) in {(32, 2), (64, 4)}; h_q / h_kv in
+ * {1, 2, 4, 8}; 1 <= n_sink <= 16; n_recent >= window; prompt_len > n_sink. */
+typedef struct {
+  int32_t batch, n_layers, h_q, h_kv, d_head;
+  int32_t n_sink, n_recent, window, bits, omega;
+  int32_t q_num, q_den;           /* quantised-tier fraction q = q_num / q_den (QEvict §4.3 Eq. (3)) */
+  int32_t budget_num, budget_den; /* B_total = floor(budget_num * M_FullKV / budget_den) when b_total == 0 */
+  int64_t b_total;                /* bytes per (sequence, layer); 0 = use the fraction above */
+  int32_t prompt_len, max_len;    /* max_len = prompt_len + decode steps the cache must hold */
+} qevict_config;
+
+/* Byte budget of one (sequence, layer), QEvict §4.1 (constraint), §4.3 Eq. (3), App. B.4 Eq. (7)-(8).
+ *   full_bytes = 2 * h_kv * d_head * prompt_len * 2           (bf16 K and V, Eq. (7) per layer)
+ *   b_sink = n_sink * (c_tok + 4), b_local = (n_recent + window) * (c_tok + 4), c_tok = 4 * h_kv * d_head
+ *   b_hist = b_total - b_sink - b_local
+ *   payload = 2*h_kv*window*d_head*bits/8 + h_kv*d_head*4 + h_kv*window*4   (codes, fp16 scale/offset)
+ *   m_q = payload + 4*window + 16;  m_f = window*c_tok + 4*window + 8 + payload (dormant-ledger reserve)
+ *   k_f = floor((1-q) * b_hist / m_f),  k_q = floor(q * b_hist / m_q)      (exact integers)        */
+typedef struct {
+  int64_t full_bytes, b_total, b_sink, b_local, b_hist, payload, m_f, m_q;
+  int32_t k_f, k_q;
+  int32_t n_windows;      /* window ids 0 .. n_windows-1 can ever exist: ceil((max_len - n_sink) / window) */
+  int32_t ring_windows;   /* windows of recent-region storage per unit */
+} qevict_budget_info;
+
+/* Where each part of the cache tuple lives inside the caller's arena, as byte
+ * offsets from the arena base.  Unit u = layer * batch + seq; the region of unit u
+ * starts at off_X + u * stride_X.  Layouts (all per unit):
+ *   sink   [h_kv][2 (K,V)][n_sink][d_head] bf16, row-major                     (S of Eq. (2))
+ *   ring   [h_kv][2][ring_windows][window*d_head] bf16 blocks, one block per
+ *          window j at ring slot j % ring_windows, fragment-native (below)     (L_t)
+ *   fpool  [k_f][h_kv][2][window*d_head] bf16 blocks, fragment-native          (F_t data)
+ *   ledger [k_f+k_q][h_kv][qblock] bytes: K codes | V codes | K scale[d] | K offset[d] |
+ *          V scale[window] | V offset[window] (fp16), qblock = payload / h_kv   (Q_t data, ledger Λ)
+ *   score  [h_kv][n_windows] fp32: per-KV-head partial scores; the window score S(w) of
+ *          QEvict §4.2 Eq. (1) is their sum over the KV heads (in head order), and right
+ *          after a routing event the whole sum sits in head 0
+ *   state  [n_windows] uint8: bits 0-1 tier (0 recent/unrouted, 1 Full, 2 Quantized, 3 Evicted),
+ *          bits 2-3 ledger status (0 none, 1 active, 2 dormant)                  (E_t is tier 3)
+ *   fslot, lslot [n_windows] int32: F-pool slot / ledger slot of a window, -1 if none
+ *   ftab   [k_f] int32 pairs (window id, F slot), ascending window id; f_count valid
+ *   qtab   [k_q] int32 pairs (window id, ledger slot), ascending window id; q_count valid
+ *   meta   int32[16]: [0] tokens cached T, [1] windows routed so far, [2] f_count, [3] q_count
+ *
+ * Fragment-native bf16 block of one window and KV head (W = window tokens, d = 128):
+ *   K element (tok, dim), tok < W: index (((tok/16)*8 + dim/16)*32 + lane)*8 + reg*2 + (dim%2)
+ *   V element (tok, dim):          index (((tok/16)*8 + dim/16)*32 + lane)*8 + reg*2 + (tok%2)
+ *   where for K: r = tok%16, c = dim%16; for V: r = dim%16, c = tok%16;
+ *   lane = (r%8)*4 + (c%8)/2 and reg = r/8 + 2*(c/8)  (the m16n8k16 A-operand register map).
+ * Fragment-native codes: the same (group, lane, reg, half) map; group = (tok/16)*8 + dim/16;
+ *   element e = reg*2 + half; each (group, lane) owns one field of `bits` bytes stored at lane
+ *   byte b = group*bits + e_byte, placed at (b/16)*512 + lane*16 + b%16 within the K or V codes.
+ *   INT2 bit of e inside the 16-bit field: 4e for e < 4, 4(e-4)+2 for e >= 4.  INT4: 4e.
+ */
+typedef struct {
+  int64_t off_sink, stride_sink;
+  int64_t off_ring, stride_ring;
+  int64_t off_fpool, stride_fpool;
+  int64_t off_ledger, stride_ledger;
+  int64_t off_score, stride_score;
+  int64_t off_state, stride_state;
+  int64_t off_fslot, stride_fslot;
+  int64_t off_lslot, stride_lslot;
+  int64_t off_ftab, stride_ftab;
+  int64_t off_qtab, stride_qtab;
+  int64_t off_meta, stride_meta;
+  int64_t qblock;        /* ledger bytes per (slot, KV head) */
+  int64_t arena_bytes;
+  int32_t n_split;       /* decode split-K partitions per (sequence, KV head) */
+} qevict_layout;
+
+typedef struct qevict_cache qevict_cache;
+
+/* Validates cfg and fills the budget of one (sequence, layer).  Host only. */
+qevict_status qevict_budget(const qevict_config *cfg, qevict_budget_info *out);
+
+/* Bytes of device arena a cache of this configuration needs (256-byte aligned base required). */
+qevict_status qevict_cache_bytes(const qevict_config *cfg, size_t *bytes);
+
+/* Creates a cache over the caller's arena (d_arena, at least qevict_cache_bytes bytes, 256-byte
+ * aligned) and enqueues its zero/-1 initialisation on `stream`.  *out receives a host handle. */
+qevict_status qevict_init_cache(const qevict_config *cfg, void *d_arena, size_t bytes,
+                                qevict_stream_t stream, qevict_cache **out);
+
+/* Region offsets of the cache tuple inside the arena (see qevict_layout).  Host only. */
+qevict_status qevict_get_layout(const qevict_cache *cache, qevict_layout *out);
+
+/* Prompt scoring, QEvict §4.2 (last paragraph): for every (sequence, window j starting in the
+ * prompt) S0[j] = (1/h_q) sum_h sum_{tau < P} sum_{i in w_j, i <= tau} a_tau^h(i), dense causal
+ * attention of every prompt query.  q_prompt [batch][P][h_q][d], k_prompt [batch][P][h_kv][d];
+ * s0_out [batch][ceil((P - n_sink) / window)] fp32.  Prompts are per layer: call once per layer.
+ * Scratch: a region of the arena reserved for it (no allocation); reads the inputs twice. */
+qevict_status qevict_prefill_scores(const qevict_cache *cache, const void *q_prompt, const void *k_prompt,
+                                    float *s0_out, qevict_stream_t stream);
+
+/* Prefill of one layer, QEvict §4.2 (last paragraph) and §4.3 Eq. (2)-(5): stores the sink and the
+ * recent region, sets the window scores (s0 [batch][ceil((P - n_sink)/window)] fp32, or computed
+ * from q_prompt when s0 is NULL), routes all historical prompt windows into F / Q / E and
+ * materialises F (bf16 copy) and Q (quantised once).  k_prompt, v_prompt [batch][P][h_kv][d].
+ * Must be called exactly once per layer, before any decode step of that layer. */
+qevict_status qevict_prefill_route(qevict_cache *cache, int32_t layer, const void *k_prompt,
+                                   const void *v_prompt, const float *s0, const void *q_prompt,
+                                   qevict_stream_t stream);
+
+/* One decode step of one layer for every sequence, QEvict §4.1 (attention over the accessible
+ * set) and §4.2 Eq. (1): appends k_new, v_new [batch][h_kv][d] at position T (the recent region),
+ * computes out[batch][h_q][d] = softmax(q K_acc^T / sqrt(d)) V_acc over sink + Full + dequantised
+ * Quantized + recent tokens (the new token included; query head h reads KV head h / (h_q/h_kv)),
+ * and adds (1/h_q) * sum_h (attention mass of window w) to every accessible non-sink window's
+ * score.  q [batch][h_q][d].  Fails with QEVICT_ESCHEDULE if the cache is full (T = max_len). */
+qevict_status qevict_decode_step(qevict_cache *cache, int32_t layer, const void *q, const void *k_new,
+                                 const void *v_new, void *out, qevict_stream_t stream);
+
+/* Routing event for every layer and sequence, QEvict §4.3 Eq. (4)-(6) and App. A Algorithm 1:
+ * candidates = Full + Quantized + windows aged out of the recent region; rank by score
+ * (descending, ties to the older window); first k_f -> Full, next k_q -> Quantized, rest ->
+ * Evicted.  Quantises newly demoted windows once (reusing a dormant ledger when one exists),
+ * rebuilds promoted windows in bf16 from their ledger, copies aged windows, frees evicted ones,
+ * and rebuilds the F / Q tables in window order with the lowest free slots going to new windows
+ * in window order.  Legal only when every layer has taken the same multiple of omega decode
+ * steps since its prefill (else QEVICT_ESCHEDULE). */
+qevict_status qevict_route(qevict_cache *cache, qevict_stream_t stream);
+
+/* Copies the 7 cumulative transition counters (promotions Q->F, demotions F->Q, first-time
+ * quantisations, ledger reactivations, evictions, aged->F, aged->Q), summed over all units, to
+ * host memory `host7`.  Synchronises `stream`.  Returns QEVICT_EDEVICE if a kernel recorded a
+ * fault in the device status word. */
+qevict_status qevict_read_counters(qevict_cache *cache, int64_t *host7, qevict_stream_t stream);
+
+/* Synchronises `stream`, re-reads the per-layer token counts (needed after replaying captured
+ * CUDA graphs of decode steps) and returns QEVICT_EDEVICE if the device status word is set. */
+qevict_status qevict_check(qevict_cache *cache, qevict_stream_t stream);
+
+/* Frees the host handle (the arena stays the caller's). */
+qevict_status qevict_destroy(qevict_cache *cache);
+
+const char *qevict_status_string(qevict_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QEVICT_H */

@@ -1,0 +1,183 @@
+"""Thin ctypes binding of the QEvict C ABI (include/qevict.h).
+
+Argument marshalling only: every step of the decode path runs in the CUDA library.  PyTorch
+provides the device memory (the arena and the tensors) and the stream.  If the library is
+missing this module raises; there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libqevict.so")
+
+OK, EINVAL, EBUDGET, ENOMEM, ESCHEDULE, ECUDA, EDEVICE = range(7)
+COUNTER_NAMES = ("promotions", "demotions", "first_quant", "reactivations", "evictions", "aged_full", "aged_quant")
+
+
+class QEvictError(RuntimeError):
+    def __init__(self, status: int, where: str, msg: str):
+        super().__init__(f"{where}: {msg} (status {status})")
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("batch", "n_layers", "h_q", "h_kv", "d_head", "n_sink", "n_recent",
+                                             "window", "bits", "omega", "q_num", "q_den", "budget_num",
+                                             "budget_den")] + \
+               [("b_total", ctypes.c_int64), ("prompt_len", ctypes.c_int32), ("max_len", ctypes.c_int32)]
+
+
+class BudgetInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("full_bytes", "b_total", "b_sink", "b_local", "b_hist", "payload",
+                                             "m_f", "m_q")] + \
+               [(n, ctypes.c_int32) for n in ("k_f", "k_q", "n_windows", "ring_windows")]
+
+
+_LAYOUT_REGIONS = ("sink", "ring", "fpool", "ledger", "score", "state", "fslot", "lslot", "ftab", "qtab", "meta")
+
+
+class Layout(ctypes.Structure):
+    _fields_ = [(f"{k}_{r}", ctypes.c_int64) for r in _LAYOUT_REGIONS for k in ("off", "stride")] + \
+               [("qblock", ctypes.c_int64), ("arena_bytes", ctypes.c_int64), ("n_split", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Loads libqevict.so from the package directory; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with recoverable_quantized_kv_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I32, I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+    sig = {
+        "qevict_budget": [ctypes.POINTER(Config), ctypes.POINTER(BudgetInfo)],
+        "qevict_cache_bytes": [ctypes.POINTER(Config), ctypes.POINTER(ctypes.c_size_t)],
+        "qevict_init_cache": [ctypes.POINTER(Config), P, ctypes.c_size_t, P, ctypes.POINTER(P)],
+        "qevict_get_layout": [P, ctypes.POINTER(Layout)],
+        "qevict_prefill_scores": [P, P, P, P, P],
+        "qevict_prefill_route": [P, I32, P, P, P, P, P],
+        "qevict_decode_step": [P, I32, P, P, P, P, P],
+        "qevict_route": [P, P],
+        "qevict_read_counters": [P, ctypes.POINTER(I64), P],
+        "qevict_check": [P, P],
+        "qevict_destroy": [P],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.qevict_status_string.argtypes = [ctypes.c_int]
+    lib.qevict_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def exported_symbols():
+    """Names of the C ABI entry points declared in include/qevict.h."""
+    return ["qevict_budget", "qevict_cache_bytes", "qevict_init_cache", "qevict_get_layout",
+            "qevict_prefill_scores", "qevict_prefill_route", "qevict_decode_step", "qevict_route",
+            "qevict_read_counters", "qevict_check", "qevict_destroy", "qevict_status_string"]
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise QEvictError(status, where, load().qevict_status_string(status).decode())
+
+
+def make_config(wl, **over) -> Config:
+    """C config from any object with the workload's field names (e.g. synth.Workload)."""
+    c = Config()
+    for name, _ in Config._fields_:
+        if name == "b_total":
+            c.b_total = int(over.get("b_total", getattr(wl, "b_total", 0) or 0))
+        elif name == "max_len":
+            c.max_len = int(over.get("max_len", wl.prompt_len + wl.steps))
+        else:
+            setattr(c, name, int(over.get(name, getattr(wl, name))))
+    return c
+
+
+def budget(cfg: Config) -> BudgetInfo:
+    b = BudgetInfo()
+    _check(load().qevict_budget(ctypes.byref(cfg), ctypes.byref(b)), "qevict_budget")
+    return b
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream=None) -> int:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+class Cache:
+    """A QEvict cache over a torch-allocated arena (uint8 CUDA tensor)."""
+
+    def __init__(self, cfg: Config, device="cuda", stream=None, arena=None):
+        import torch
+        lib = load()
+        self.cfg = cfg
+        self.bud = budget(cfg)
+        nbytes = ctypes.c_size_t()
+        _check(lib.qevict_cache_bytes(ctypes.byref(cfg), ctypes.byref(nbytes)), "qevict_cache_bytes")
+        self.arena = arena if arena is not None else torch.empty(nbytes.value, dtype=torch.uint8, device=device)
+        assert self.arena.numel() >= nbytes.value and self.arena.data_ptr() % 256 == 0
+        h = ctypes.c_void_p()
+        _check(lib.qevict_init_cache(ctypes.byref(cfg), self.arena.data_ptr(), self.arena.numel(), _stream(stream),
+                                     ctypes.byref(h)), "qevict_init_cache")
+        self.handle = h
+        self.layout = Layout()
+        _check(lib.qevict_get_layout(h, ctypes.byref(self.layout)), "qevict_get_layout")
+
+    def close(self):
+        if self.handle:
+            load().qevict_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # ---- the C ABI calls
+    def prefill_scores(self, q_prompt, k_prompt, s0_out, stream=None):
+        _check(load().qevict_prefill_scores(self.handle, _ptr(q_prompt), _ptr(k_prompt), _ptr(s0_out),
+                                            _stream(stream)), "qevict_prefill_scores")
+
+    def prefill_route(self, layer: int, k_prompt, v_prompt, s0=None, q_prompt=None, stream=None):
+        _check(load().qevict_prefill_route(self.handle, layer, _ptr(k_prompt), _ptr(v_prompt), _ptr(s0),
+                                           _ptr(q_prompt), _stream(stream)), "qevict_prefill_route")
+
+    def decode_step(self, layer: int, q, k_new, v_new, out, stream=None):
+        _check(load().qevict_decode_step(self.handle, layer, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out),
+                                         _stream(stream)), "qevict_decode_step")
+
+    def route(self, stream=None):
+        _check(load().qevict_route(self.handle, _stream(stream)), "qevict_route")
+
+    def counters(self, stream=None) -> dict:
+        buf = (ctypes.c_int64 * 7)()
+        _check(load().qevict_read_counters(self.handle, buf, _stream(stream)), "qevict_read_counters")
+        return dict(zip(COUNTER_NAMES, list(buf)))
+
+    def check(self, stream=None):
+        _check(load().qevict_check(self.handle, _stream(stream)), "qevict_check")
+
+    # ---- tensor views of the cache tuple inside the arena (read-only use in tests)
+    def region(self, name: str, unit: int, nbytes: int):
+        off = getattr(self.layout, f"off_{name}") + unit * getattr(self.layout, f"stride_{name}")
+        return self.arena[off:off + nbytes]
+
+    def unit(self, layer: int, seq: int) -> int:
+        return layer * self.cfg.batch + seq

@@ -1,0 +1,58 @@
+// Device view of a cache: the caller's arena plus the byte offsets of every region.
+// Built once on the host (api.cu) and passed by value to every kernel.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace qv {
+
+struct CacheDev {
+  uint8_t *arena;
+  // per-unit regions: unit u = layer * B + seq
+  int64_t off_sink, st_sink;
+  int64_t off_ring, st_ring;
+  int64_t off_fpool, st_fpool;
+  int64_t off_ledger, st_ledger;
+  int64_t off_score, st_score;
+  int64_t off_state, st_state;
+  int64_t off_fslot, st_fslot;
+  int64_t off_lslot, st_lslot;
+  int64_t off_ftab, st_ftab;
+  int64_t off_qtab, st_qtab;
+  int64_t off_meta, st_meta;
+  int64_t off_qtask, st_qtask;     // int4 quantise tasks [n_windows]
+  int64_t off_mtask, st_mtask;     // int4 promote/copy tasks [n_windows]
+  // global regions
+  int64_t off_counters;            // int64 [U][N_COUNTERS]
+  int64_t off_status;              // int32
+  int64_t off_splitctr;            // uint32 [L][B][h_kv]
+  int64_t off_headctr;             // uint32 [L][B]
+  int64_t off_part, st_part_layer; // float [L][B][h_kv][n_split][PART_FLOATS]
+  int64_t off_mu, st_mu_layer;     // float [L][B][h_kv][max_items][8]
+  int64_t off_rowstat;             // float [B][h_q][P] prefill row log2-sum-exp
+  int64_t off_colsum;              // float [B][h_q][P] prefill column sums
+  // sizes
+  int B, L, h_q, h_kv, G, n_sink, n_recent, W, bits, omega;
+  int k_f, k_q, n_windows, ring_windows, n_split, max_items, prompt_len, max_len;
+
+  template <typename T>
+  __host__ __device__ T *at(int64_t off, int64_t st, int u) const {
+    return reinterpret_cast<T *>(arena + off + st * (int64_t)u);
+  }
+  __host__ __device__ int *status() const { return reinterpret_cast<int *>(arena + off_status); }
+};
+
+constexpr int PART_FLOATS = 16 + 8 * 128;   // m[8], l[8], O[8][128] per split
+
+struct DecodeIO {
+  const __nv_bfloat16 *q;       // [B][h_q][D]
+  const __nv_bfloat16 *k_new;   // [B][h_kv][D]
+  const __nv_bfloat16 *v_new;   // [B][h_kv][D]
+  __nv_bfloat16 *out;           // [B][h_q][D]
+  int layer;
+  float scale_log2;             // log2(e) / sqrt(D)
+  float inv_hq;                 // 1 / h_q
+};
+
+}  // namespace qv

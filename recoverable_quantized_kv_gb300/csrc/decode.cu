@@ -1,0 +1,560 @@
+// Decode step of one layer: append + split-K GQA attention over sink / recent / Full (bf16) /
+// Quantized (INT2 dequantised in registers) windows + per-window attention mass + score update.
+//
+// QEvict (arXiv 2608.05326) §4.1: o = softmax(q K_acc^T / sqrt(d)) V_acc over the accessible set;
+// §4.2 Eq. (1): the window score accumulates (1/H_q) sum_h sum_{i in w} a^h(i).
+//
+// Grid (n_split, h_kv, batch).  Each CTA owns a byte-balanced contiguous range of the work list of
+// one (sequence, KV head); each warp owns a sub-range and streams its windows through a private
+// 4-stage shared-memory ring filled by 1-D bulk copies (TMA) signalled on mbarriers.  The G query
+// heads of the KV head ride on the N side of mma.m16n8k16 (tokens on M for Q K^T, dims on M for
+// P V), so both products run on tensor cores.  Softmax is online per warp; per-window masses are
+// kept as log2-sum-exp values, which the last CTA of the (sequence, KV head) to finish (counted
+// with one atomic, no waiting) normalises into the window scores while it merges the splits.
+#include "cache_dev.cuh"
+#include "common.cuh"
+
+namespace qv {
+
+constexpr int DEC_WARPS = 8;
+constexpr int DEC_STAGES = 4;
+constexpr int DEC_STAGE_BYTES = 4096;
+constexpr int DEC_SMEM = DEC_WARPS * DEC_STAGES * DEC_STAGE_BYTES + DEC_WARPS * DEC_STAGES * 8;
+
+// Work list of one (sequence, KV head): item 0 = the sink tokens, items 1..nL = recent windows
+// j0 .. j0+nL-1, then the F-table entries, then the Q-table entries.  Item costs are the bytes
+// streamed, and split / warp ranges are byte-balanced prefixes of this list.
+struct Items {
+  int nL, nF, nQ, j0;
+  long long cs, cw, cq;
+  __device__ int total() const { return 1 + nL + nF + nQ; }
+  __device__ long long total_cost() const { return cs + (long long)(nL + nF) * cw + (long long)nQ * cq; }
+  __device__ int first_at(long long target) const {   // first item whose start cost >= target
+    if (target <= 0) return 0;
+    if (target <= cs) return 1;
+    long long r = target - cs;
+    const long long nb = nL + nF;
+    if (r <= nb * cw) return 1 + (int)((r + cw - 1) / cw);
+    r -= nb * cw;
+    const int i = 1 + nL + nF + (int)((r + cq - 1) / cq);
+    return i < total() ? i : total();
+  }
+  __device__ int bound(int part, int nparts) const {
+    return part >= nparts ? total() : first_at(total_cost() * part / nparts);
+  }
+};
+
+__device__ __forceinline__ uint32_t ldg32(const void *p) { return __ldg(reinterpret_cast<const uint32_t *>(p)); }
+__device__ __forceinline__ uint32_t ldg16(const void *p) { return __ldg(reinterpret_cast<const unsigned short *>(p)); }
+
+// One online-softmax step over NMT 16-token groups of S^T fragments (rows tokens, cols heads).
+// s is in log2 units; rows flagged invalid are excluded.  On return s holds the probabilities
+// (relative to the new running max), tsum the per-head sum over this item, mnew the new max.
+template <int NMT>
+__device__ __forceinline__ void online_step(float (&s)[NMT][4], const bool (&valid)[NMT][2], float (&m_run)[2],
+                                            float (&l_run)[2], float (&o)[8][4], float (&tsum)[2],
+                                            float (&mnew)[2]) {
+  float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int mt = 0; mt < NMT; ++mt)
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+      if (valid[mt][r]) {
+        mx[0] = fmaxf(mx[0], s[mt][2 * r]);
+        mx[1] = fmaxf(mx[1], s[mt][2 * r + 1]);
+      }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    mx[h] = warp_max_xor_g(mx[h]);
+    mnew[h] = fmaxf(m_run[h], mx[h]);
+  }
+  float base[2], corr[2], ps[2] = {0.f, 0.f};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    base[h] = (mnew[h] == -INFINITY) ? 0.f : mnew[h];
+    corr[h] = exp2f(m_run[h] - base[h]);
+  }
+#pragma unroll
+  for (int mt = 0; mt < NMT; ++mt)
+#pragma unroll
+    for (int r = 0; r < 2; ++r)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const float p = valid[mt][r] ? exp2f(s[mt][2 * r + h] - base[h]) : 0.f;
+        s[mt][2 * r + h] = p;
+        ps[h] += p;
+      }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    tsum[h] = warp_sum_xor_g(ps[h]);
+    l_run[h] = l_run[h] * corr[h] + tsum[h];
+    m_run[h] = mnew[h];
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    o[i][0] *= corr[0];
+    o[i][2] *= corr[0];
+    o[i][1] *= corr[1];
+    o[i][3] *= corr[1];
+  }
+}
+
+// B fragments of P^T for k-step kk from the S^T accumulator layout (8x8 transposes).
+template <int NMT>
+__device__ __forceinline__ void p_to_b(const float (&p)[NMT][4], uint32_t (&pb)[NMT][2]) {
+#pragma unroll
+  for (int kk = 0; kk < NMT; ++kk) {
+    pb[kk][0] = movmatrix_trans(pack_bf16(p[kk][0], p[kk][1]));
+    pb[kk][1] = movmatrix_trans(pack_bf16(p[kk][2], p[kk][3]));
+  }
+}
+
+__device__ __forceinline__ float h2f_lo(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFF))); }
+__device__ __forceinline__ float h2f_hi(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v >> 16))); }
+
+// x_hat = bf16(fp32(code * s + m)) for the two halves of an INT2 field element pair.
+__device__ __forceinline__ uint32_t dq_pair(uint32_t field, int sh_lo, int sh_hi, float s_lo, float m_lo, float s_hi,
+                                            float m_hi) {
+  const float lo = __fmaf_rn(code_f((field >> sh_lo) & 3u), s_lo, m_lo);
+  const float hi = __fmaf_rn(code_f((field >> sh_hi) & 3u), s_hi, m_hi);
+  return pack_bf16(lo, hi);
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int k) {
+  return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
+}
+
+template <int W, int BITS>
+__global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDev C, const DecodeIO io) {
+  static_assert(W == 32 && BITS == 2, "decode kernel instantiated for W=32, INT2");
+  using Gm = Geo<W, BITS>;
+  constexpr int NMT = W / 16;
+  extern __shared__ __align__(128) uint8_t smem[];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gl = lane >> 2, tl = lane & 3;
+  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int unit = io.layer * C.B + b;
+  const int G = C.G;
+  int *status = C.status();
+  int *meta = C.at<int>(C.off_meta, C.st_meta, unit);
+  const int T = meta[M_T], n_route = meta[M_NROUTE], nF = meta[M_FCOUNT], nQ = meta[M_QCOUNT];
+  const int2 *ftab = C.at<const int2>(C.off_ftab, C.st_ftab, unit);
+  const int2 *qtab = C.at<const int2>(C.off_qtab, C.st_qtab, unit);
+  const __nv_bfloat16 *sink = C.at<const __nv_bfloat16>(C.off_sink, C.st_sink, unit) + (size_t)g * 2 * C.n_sink * D;
+  __nv_bfloat16 *ring = C.at<__nv_bfloat16>(C.off_ring, C.st_ring, unit) + (size_t)g * 2 * C.ring_windows * Gm::BLK;
+  const uint8_t *fpool = C.at<const uint8_t>(C.off_fpool, C.st_fpool, unit);
+  const uint8_t *ledger = C.at<const uint8_t>(C.off_ledger, C.st_ledger, unit);
+  const int bg = b * C.h_kv + g;
+  float *mu = reinterpret_cast<float *>(C.arena + C.off_mu + C.st_mu_layer * io.layer) + (size_t)bg * C.max_items * 8;
+  float *part = reinterpret_cast<float *>(C.arena + C.off_part + C.st_part_layer * io.layer) +
+                (size_t)bg * C.n_split * PART_FLOATS;
+
+  Items I;
+  const int jn = (T - C.n_sink) / W;   // window of the new token at position T
+  I.j0 = n_route;
+  I.nL = jn - n_route + 1;
+  I.nF = nF;
+  I.nQ = nQ;
+  I.cs = (long long)C.n_sink * 2 * D * 2;
+  I.cw = 2LL * W * D * 2;
+  I.cq = Gm::QB;
+  const int nparts = C.n_split * DEC_WARPS;
+  const int i0 = I.bound(split * DEC_WARPS + warp, nparts);
+  const int i1 = I.bound(split * DEC_WARPS + warp + 1, nparts);
+
+  uint8_t *stage = smem + warp * DEC_STAGES * DEC_STAGE_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + DEC_WARPS * DEC_STAGES * DEC_STAGE_BYTES) + warp * DEC_STAGES;
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < DEC_STAGES; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  // q as the B operand of S^T = K q^T: b0 = q[head gl][16j+2tl .. +1], b1 = the same at +8.
+  uint32_t qb[8][2];
+  {
+    const __nv_bfloat16 *qh = io.q + ((size_t)b * C.h_q + (size_t)g * G + gl) * D;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      qb[j][0] = gl < G ? ldg32(qh + 16 * j + 2 * tl) : 0u;
+      qb[j][1] = gl < G ? ldg32(qh + 16 * j + 2 * tl + 8) : 0u;
+    }
+  }
+
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+  float o[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+  // ---- chunk stream: bf16 windows = NMT K chunks then NMT V chunks (4 KB each); Q window = 1 chunk
+  auto n_chunks = [&](int it) -> int { return it == 0 ? 0 : (it <= I.nL + I.nF ? 2 * NMT : 1); };
+  auto chunk_src = [&](int it, int sub, const void *&src, uint32_t &bytes) {
+    if (it <= I.nL) {                                   // recent window in the ring
+      const int rs = (I.j0 + it - 1) % C.ring_windows;
+      const __nv_bfloat16 *kb = ring + (size_t)rs * Gm::BLK;
+      const __nv_bfloat16 *vb = ring + (size_t)(C.ring_windows + rs) * Gm::BLK;
+      src = sub < NMT ? (const void *)(kb + sub * 2048) : (const void *)(vb + (sub - NMT) * 2048);
+      bytes = DEC_STAGE_BYTES;
+    } else if (it <= I.nL + I.nF) {                     // Full window
+      const int slot = __ldg(&ftab[it - 1 - I.nL].y);
+      const uint8_t *base = fpool + ((size_t)slot * C.h_kv + g) * 2 * Gm::BLK * 2;
+      src = base + (size_t)sub * DEC_STAGE_BYTES;
+      bytes = DEC_STAGE_BYTES;
+    } else {                                            // Quantized window: one ledger block
+      const int slot = __ldg(&qtab[it - 1 - I.nL - I.nF].y);
+      src = ledger + ((size_t)slot * C.h_kv + g) * Gm::QB;
+      bytes = Gm::QB;
+    }
+  };
+  int issued = 0, consumed = 0;
+  int p_it = i0, p_sub = 0;
+  bool ok = true;
+  auto issue = [&]() {
+    while (issued - consumed < DEC_STAGES && p_it < i1) {
+      const int nc = n_chunks(p_it);
+      if (nc == 0) {
+        ++p_it;
+        p_sub = 0;
+        continue;
+      }
+      if (lane == 0) {
+        const void *src;
+        uint32_t bytes;
+        chunk_src(p_it, p_sub, src, bytes);
+        const int st = issued % DEC_STAGES;
+        fence_proxy_async();
+        mbar_arrive_expect_tx(&bars[st], bytes);
+        bulk_g2s(stage + st * DEC_STAGE_BYTES, src, bytes, &bars[st]);
+      }
+      ++issued;
+      if (++p_sub == nc) {
+        ++p_it;
+        p_sub = 0;
+      }
+    }
+  };
+  auto wait_chunk = [&](int c) -> const uint8_t * {
+    const int st = c % DEC_STAGES;
+    if (!mbar_wait(&bars[st], (uint32_t)((c / DEC_STAGES) & 1), status)) ok = false;
+    return stage + st * DEC_STAGE_BYTES;
+  };
+
+  issue();
+  for (int it = i0; it < i1 && ok; ++it) {
+    float tsum[2], mnew[2];
+    if (it == 0) {
+      // ---------------- sink tokens (no mass): fragments straight from the compact sink rows
+      float s[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+      const __nv_bfloat16 *sk = sink, *sv = sink + (size_t)C.n_sink * D;
+      const bool r0 = gl < C.n_sink, r1 = gl + 8 < C.n_sink;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t a0 = r0 ? ldg32(sk + gl * D + 16 * j + 2 * tl) : 0u;
+        const uint32_t a1 = r1 ? ldg32(sk + (gl + 8) * D + 16 * j + 2 * tl) : 0u;
+        const uint32_t a2 = r0 ? ldg32(sk + gl * D + 16 * j + 2 * tl + 8) : 0u;
+        const uint32_t a3 = r1 ? ldg32(sk + (gl + 8) * D + 16 * j + 2 * tl + 8) : 0u;
+        mma_bf16(s[0], a0, a1, a2, a3, qb[j][0], qb[j][1]);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) s[0][k] *= io.scale_log2;
+      const bool valid[1][2] = {{r0, r1}};
+      online_step<1>(s, valid, m_run, l_run, o, tsum, mnew);
+      uint32_t pb[1][2];
+      p_to_b<1>(s, pb);
+      const int t0 = 2 * tl, t1 = 2 * tl + 8;   // token rows of this lane's B/A columns
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int d0 = 16 * i + gl, d1 = d0 + 8;
+        auto vv = [&](int t, int d) -> uint32_t { return t < C.n_sink ? ldg16(sv + t * D + d) : 0u; };
+        const uint32_t a0 = vv(t0, d0) | (vv(t0 + 1, d0) << 16);
+        const uint32_t a1 = vv(t0, d1) | (vv(t0 + 1, d1) << 16);
+        const uint32_t a2 = vv(t1, d0) | (vv(t1 + 1, d0) << 16);
+        const uint32_t a3 = vv(t1, d1) | (vv(t1 + 1, d1) << 16);
+        mma_bf16(o[i], a0, a1, a2, a3, pb[0][0], pb[0][1]);
+      }
+      continue;
+    }
+
+    int wid;
+    bool valid[NMT][2];
+    float s[NMT][4];
+#pragma unroll
+    for (int mt = 0; mt < NMT; ++mt) s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
+
+    if (it <= I.nL + I.nF) {
+      // ---------------- bf16 window (recent or Full)
+      const bool is_local = it <= I.nL;
+      wid = is_local ? I.j0 + it - 1 : __ldg(&ftab[it - 1 - I.nL].x);
+      const int newtok = (is_local && wid == jn) ? T - (C.n_sink + jn * W) : -1;
+      const uint8_t *kc[NMT];
+#pragma unroll
+      for (int mt = 0; mt < NMT; ++mt) kc[mt] = wait_chunk(consumed + mt);
+      if (newtok >= 0 && ok) {
+        // append: the new token enters the recent ring (global) and this warp's staged copy
+        const int rs = jn % C.ring_windows;
+        __nv_bfloat16 *kb = ring + (size_t)rs * Gm::BLK;
+        const __nv_bfloat16 *kn = io.k_new + ((size_t)b * C.h_kv + g) * D;
+        uint8_t *kst = const_cast<uint8_t *>(kc[newtok >> 4]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int d = 4 * lane + 2 * h;
+          const uint32_t pair = ldg32(kn + d);
+          const int idx = fnk_index(newtok, d);
+          *reinterpret_cast<uint32_t *>(kb + idx) = pair;
+          *reinterpret_cast<uint32_t *>(kst + (idx - (newtok >> 4) * 2048) * 2) = pair;
+        }
+        __syncwarp();
+      }
+#pragma unroll
+      for (int mt = 0; mt < NMT; ++mt) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint4 a = lds128(kc[mt] + (j * 32 + lane) * 16);
+          mma_bf16(s[mt], a.x, a.y, a.z, a.w, qb[j][0], qb[j][1]);
+        }
+      }
+      __syncwarp();
+      consumed += NMT;
+      issue();
+#pragma unroll
+      for (int mt = 0; mt < NMT; ++mt) {
+        const int tok0 = 16 * mt + gl;
+        if (is_local) {
+          const int p0 = C.n_sink + wid * W + tok0;
+          valid[mt][0] = p0 <= T;
+          valid[mt][1] = p0 + 8 <= T;
+        } else {
+          valid[mt][0] = valid[mt][1] = true;
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) s[mt][k] *= io.scale_log2;
+      }
+      online_step<NMT>(s, valid, m_run, l_run, o, tsum, mnew);
+      uint32_t pb[NMT][2];
+      p_to_b<NMT>(s, pb);
+      const uint8_t *vc[NMT];
+#pragma unroll
+      for (int kk = 0; kk < NMT; ++kk) vc[kk] = wait_chunk(consumed + kk);
+      if (newtok >= 0 && ok) {
+        const int rs = jn % C.ring_windows;
+        __nv_bfloat16 *vb = ring + (size_t)(C.ring_windows + rs) * Gm::BLK;
+        const __nv_bfloat16 *vn = io.v_new + ((size_t)b * C.h_kv + g) * D;
+        uint8_t *vst = const_cast<uint8_t *>(vc[newtok >> 4]);
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          const int d = 4 * lane + h;
+          const unsigned short x = (unsigned short)ldg16(vn + d);
+          const int idx = fnv_index(newtok, d);
+          reinterpret_cast<unsigned short *>(vb)[idx] = x;
+          reinterpret_cast<unsigned short *>(vst)[idx - (newtok >> 4) * 2048] = x;
+        }
+        __syncwarp();
+      }
+#pragma unroll
+      for (int kk = 0; kk < NMT; ++kk) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 a = lds128(vc[kk] + (i * 32 + lane) * 16);
+          mma_bf16(o[i], a.x, a.y, a.z, a.w, pb[kk][0], pb[kk][1]);
+        }
+      }
+      __syncwarp();
+      consumed += NMT;
+      issue();
+    } else {
+      // ---------------- Quantized window: INT2 codes + fp16 params, dequantised in registers
+      wid = __ldg(&qtab[it - 1 - I.nL - I.nF].x);
+      const uint8_t *ch = wait_chunk(consumed);
+      const uint4 kcw[NMT] = {lds128(ch + lane * 16), lds128(ch + 512 + lane * 16)};
+      const uint4 vcw[NMT] = {lds128(ch + Gm::OFF_VCODE + lane * 16), lds128(ch + Gm::OFF_VCODE + 512 + lane * 16)};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t spA = lds32(ch + Gm::OFF_KS + 2 * (16 * j + 2 * tl));
+        const uint32_t spB = lds32(ch + Gm::OFF_KS + 2 * (16 * j + 2 * tl + 8));
+        const uint32_t mpA = lds32(ch + Gm::OFF_KM + 2 * (16 * j + 2 * tl));
+        const uint32_t mpB = lds32(ch + Gm::OFF_KM + 2 * (16 * j + 2 * tl + 8));
+        const float sA0 = h2f_lo(spA), sA1 = h2f_hi(spA), sB0 = h2f_lo(spB), sB1 = h2f_hi(spB);
+        const float mA0 = h2f_lo(mpA), mA1 = h2f_hi(mpA), mB0 = h2f_lo(mpB), mB1 = h2f_hi(mpB);
+#pragma unroll
+        for (int mt = 0; mt < NMT; ++mt) {
+          const uint32_t f = word_of(kcw[mt], j >> 1) >> (16 * (j & 1));
+          const uint32_t a0 = dq_pair(f, 0, 4, sA0, mA0, sA1, mA1);
+          const uint32_t a1 = dq_pair(f, 8, 12, sA0, mA0, sA1, mA1);
+          const uint32_t a2 = dq_pair(f, 2, 6, sB0, mB0, sB1, mB1);
+          const uint32_t a3 = dq_pair(f, 10, 14, sB0, mB0, sB1, mB1);
+          mma_bf16(s[mt], a0, a1, a2, a3, qb[j][0], qb[j][1]);
+        }
+      }
+#pragma unroll
+      for (int mt = 0; mt < NMT; ++mt) {
+        valid[mt][0] = valid[mt][1] = true;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) s[mt][k] *= io.scale_log2;
+      }
+      online_step<NMT>(s, valid, m_run, l_run, o, tsum, mnew);
+      uint32_t pb[NMT][2];
+      p_to_b<NMT>(s, pb);
+#pragma unroll
+      for (int kk = 0; kk < NMT; ++kk) {
+        const int t0 = 16 * kk + 2 * tl;
+        const uint32_t spA = lds32(ch + Gm::OFF_VS + 2 * t0), spB = lds32(ch + Gm::OFF_VS + 2 * (t0 + 8));
+        const uint32_t mpA = lds32(ch + Gm::OFF_VM + 2 * t0), mpB = lds32(ch + Gm::OFF_VM + 2 * (t0 + 8));
+        const float sA0 = h2f_lo(spA), sA1 = h2f_hi(spA), sB0 = h2f_lo(spB), sB1 = h2f_hi(spB);
+        const float mA0 = h2f_lo(mpA), mA1 = h2f_hi(mpA), mB0 = h2f_lo(mpB), mB1 = h2f_hi(mpB);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t f = word_of(vcw[kk], i >> 1) >> (16 * (i & 1));
+          const uint32_t a0 = dq_pair(f, 0, 4, sA0, mA0, sA1, mA1);
+          const uint32_t a1 = dq_pair(f, 8, 12, sA0, mA0, sA1, mA1);
+          const uint32_t a2 = dq_pair(f, 2, 6, sB0, mB0, sB1, mB1);
+          const uint32_t a3 = dq_pair(f, 10, 14, sB0, mB0, sB1, mB1);
+          mma_bf16(o[i], a0, a1, a2, a3, pb[kk][0], pb[kk][1]);
+        }
+      }
+      __syncwarp();
+      consumed += 1;
+      issue();
+    }
+    // log2-sum-exp of this window's logits per head: the mass is 2^(mu - M) / L after the merge
+    if (gl == 0) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int head = 2 * tl + h;
+        if (head < G) mu[(size_t)it * 8 + head] = tsum[h] > 0.f ? mnew[h] + __log2f(tsum[h]) : -INFINITY;
+      }
+    }
+  }
+  // drain: never leave a bulk copy in flight into shared memory
+  while (consumed < issued) {
+    wait_chunk(consumed);
+    ++consumed;
+  }
+
+  // ---------------- merge the warps of this CTA into one split partial
+  __syncthreads();
+  float *cm = reinterpret_cast<float *>(smem);            // [warp][8]
+  float *cl = cm + DEC_WARPS * 8;                           // [warp][8]
+  float *cO = cl + DEC_WARPS * 8;                           // [warp][8][D]
+  if (gl == 0) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      cm[warp * 8 + 2 * tl + h] = m_run[h];
+      cl[warp * 8 + 2 * tl + h] = l_run[h];
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float *w0 = cO + (warp * 8 + 2 * tl) * D, *w1 = w0 + D;
+    w0[16 * i + gl] = o[i][0];
+    w1[16 * i + gl] = o[i][1];
+    w0[16 * i + gl + 8] = o[i][2];
+    w1[16 * i + gl + 8] = o[i][3];
+  }
+  __syncthreads();
+  float *mypart = part + (size_t)split * PART_FLOATS;
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int h = idx / D, d = idx % D;
+    float M = -INFINITY;
+    for (int w = 0; w < DEC_WARPS; ++w) M = fmaxf(M, cm[w * 8 + h]);
+    float acc = 0.f, l = 0.f;
+    if (M != -INFINITY) {
+      for (int w = 0; w < DEC_WARPS; ++w) {
+        const float f = exp2f(cm[w * 8 + h] - M);
+        acc += cO[(w * 8 + h) * D + d] * f;
+        l += cl[w * 8 + h] * f;
+      }
+    }
+    mypart[16 + h * D + d] = acc;
+    if (d == 0) {
+      mypart[h] = M;
+      mypart[8 + h] = l;
+    }
+  }
+
+  // ---------------- the last CTA of this (sequence, KV head) merges the splits
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  unsigned *splitctr = reinterpret_cast<unsigned *>(C.arena + C.off_splitctr) + ((size_t)io.layer * C.B + b) * C.h_kv + g;
+  if (threadIdx.x == 0) s_last = (atomicAdd(splitctr, 1u) == (unsigned)(C.n_split - 1));
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  float *Mh = cm, *Lh = cm + 8;
+  if (warp < G) {
+    const int h = warp;
+    float M = -INFINITY;
+    for (int s = lane; s < C.n_split; s += 32) {
+      const float *ps = part + (size_t)s * PART_FLOATS;
+      if (__ldcg(ps + 8 + h) > 0.f) M = fmaxf(M, __ldcg(ps + h));
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float L = 0.f;
+    for (int s = lane; s < C.n_split; s += 32) {
+      const float *ps = part + (size_t)s * PART_FLOATS;
+      const float l = __ldcg(ps + 8 + h);
+      if (l > 0.f) L += l * exp2f(__ldcg(ps + h) - M);
+    }
+#pragma unroll
+    for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    if (lane == 0) {
+      Mh[h] = M;
+      Lh[h] = L;
+    }
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int h = idx / D, d = idx % D;
+    float acc = 0.f;
+    for (int s = 0; s < C.n_split; ++s) {
+      const float *ps = part + (size_t)s * PART_FLOATS;
+      const float l = __ldcg(ps + 8 + h);
+      if (l > 0.f) acc += __ldcg(ps + 16 + h * D + d) * exp2f(__ldcg(ps + h) - Mh[h]);
+    }
+    io.out[((size_t)b * C.h_q + (size_t)g * G + h) * D + d] = __float2bfloat16_rn(acc / Lh[h]);
+  }
+  // window scores: S_g[w] += (1/H_q) * sum_{h in group} 2^(mu - M_h) / L_h
+  float *score = C.at<float>(C.off_score, C.st_score, unit) + (size_t)g * C.n_windows;
+  const int total = I.total();
+  for (int it = 1 + threadIdx.x; it < total; it += blockDim.x) {
+    int w;
+    if (it <= I.nL) w = I.j0 + it - 1;
+    else if (it <= I.nL + I.nF) w = ftab[it - 1 - I.nL].x;
+    else w = qtab[it - 1 - I.nL - I.nF].x;
+    float mass = 0.f;
+    for (int h = 0; h < G; ++h) mass += exp2f(__ldcg(mu + (size_t)it * 8 + h) - Mh[h]) / Lh[h];
+    score[w] += mass * io.inv_hq;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    *splitctr = 0u;
+    __threadfence();
+    unsigned *headctr = reinterpret_cast<unsigned *>(C.arena + C.off_headctr) + (size_t)io.layer * C.B + b;
+    if (atomicAdd(headctr, 1u) == (unsigned)(C.h_kv - 1)) {
+      *headctr = 0u;
+      meta[M_T] = T + 1;     // every CTA of this unit has read T by now
+    }
+  }
+}
+
+int decode_smem_bytes() { return DEC_SMEM; }
+int decode_warps() { return DEC_WARPS; }
+
+cudaError_t launch_decode(const CacheDev &C, const DecodeIO &io, cudaStream_t stream) {
+  static bool attr_set = false;
+  auto kern = decode_kernel<32, 2>;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DEC_SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(C.n_split, C.h_kv, C.B);
+  kern<<<grid, DEC_WARPS * 32, DEC_SMEM, stream>>>(C, io);
+  return cudaGetLastError();
+}
+
+}  // namespace qv

@@ -1,0 +1,67 @@
+"""CPU checks of the C-ABI library: it builds, loads, exports every declared entry point, and its
+host-side budget arithmetic agrees with the oracle (no compute call needs a GPU here)."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import layout as LY
+from oracle import qevict_oracle as O
+from recoverable_quantized_kv_gb300 import binding, build, synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def cpu_lib():
+    build.build()
+    return binding.load()
+
+
+def test_exports_every_declared_symbol(cpu_lib):
+    header = open(os.path.join(ROOT, "include", "qevict.h")).read()
+    declared = set(re.findall(r"\b(qevict_\w+)\s*\(", header))
+    assert declared == set(binding.exported_symbols())
+    for name in declared:
+        assert hasattr(cpu_lib, name), name
+
+
+@pytest.mark.parametrize("name", list(synth.WORKLOADS))
+def test_budget_matches_oracle(cpu_lib, name):
+    wl = synth.workload(name)
+    b = binding.budget(binding.make_config(wl))
+    ob = O.budget(O.Config.from_obj(wl))
+    assert (b.full_bytes, b.b_total, b.b_sink, b.b_local, b.b_hist, b.payload, b.m_f, b.m_q, b.k_f, b.k_q) == \
+        (ob.full_bytes, ob.b_total, ob.b_sink, ob.b_local, ob.b_hist, ob.payload, ob.m_f, ob.m_q, ob.k_f, ob.k_q)
+
+
+def test_budget_sweep_matches_oracle(cpu_lib):
+    base = synth.workload("long_131k")
+    for bn in (10, 20, 40):
+        for qn in (50, 70, 90):
+            wl = base.replace(budget_num=bn, q_num=qn)
+            b = binding.budget(binding.make_config(wl))
+            ob = O.budget(O.Config.from_obj(wl))
+            assert (b.k_f, b.k_q) == (ob.k_f, ob.k_q)
+
+
+def test_rejections(cpu_lib):
+    wl = synth.workload("tiny_4k")
+    for over, status in [(dict(budget_num=1, budget_den=1000), binding.EBUDGET), (dict(d_head=64), binding.EINVAL),
+                         (dict(h_q=6, h_kv=4), binding.EINVAL), (dict(n_sink=17), binding.EINVAL),
+                         (dict(prompt_len=4), binding.EINVAL), (dict(q_num=101), binding.EINVAL)]:
+        with pytest.raises(binding.QEvictError) as e:
+            binding.budget(binding.make_config(wl, **over))
+        assert e.value.status == status, over
+
+
+def test_documented_layouts_are_bijections():
+    for W, bits in ((32, 2), (64, 4)):
+        for is_v in (False, True):
+            idx = LY.fn_index(W, is_v)
+            assert np.array_equal(np.sort(idx.ravel()), np.arange(W * 128))
+            byte, shift = LY.code_position(W, bits, is_v)
+            key = byte * 8 + shift
+            assert len(np.unique(key)) == W * 128 and byte.max() < W * 128 * bits // 8
+            assert np.all(shift % bits == 0)

@@ -1,0 +1,124 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle (QEvict §4.1-§4.3, App. A).
+
+Every test here is marked gpu and runs in lockstep (tests/gpu_lockstep.py): outputs within
+2e-2 max-abs, window masses and scores within 1e-3 relative, tier states / slots / tables /
+INT2 codes / fp16 parameters / bf16 window data bit-exact given identical scores.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gpu_lockstep import Lockstep, OUT_TOL
+from oracle import qevict_oracle as O
+from recoverable_quantized_kv_gb300 import binding, synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(wl, steps, **kw):
+    ls = Lockstep(wl, **kw)
+    ls.prefill()
+    ls.decode(steps)
+    got, want = ls.counters()
+    assert got == want, (got, want)
+    return ls
+
+
+def test_tiny_workload_full_run(lib):
+    """The tiny workload end to end: 4096-token prefill, 64 decode steps, 8 routing events."""
+    ls = _run(synth.workload("tiny_4k"), 64)
+    c = ls.cache.counters()
+    assert c["evictions"] > 0 and c["first_quant"] > 0
+
+
+@pytest.mark.parametrize("shape", [
+    dict(h_q=8, h_kv=2, prompt_len=1000, n_sink=5, batch=2),        # ragged prompt, odd sink, batch 2
+    dict(h_q=8, h_kv=8, prompt_len=777, n_sink=1),                  # G = 1
+    dict(h_q=16, h_kv=2, prompt_len=1500, n_sink=16, n_recent=64),  # G = 8, 16 sinks
+    dict(h_q=4, h_kv=2, prompt_len=600, n_sink=3, omega=4, budget_num=40),
+])
+def test_edge_shapes(lib, shape):
+    base = synth.workload("tiny_4k", steps=24, n_plant=4, kappa=6.0)
+    _run(base.replace(**shape), 24)
+
+
+def test_two_tier_and_quantized_only(lib):
+    """q = 0: Full/Evicted only (two-tier window eviction); q = 1: K_f = 0 (quantised retention)."""
+    base = synth.workload("tiny_4k", prompt_len=1200, steps=16, n_plant=4)
+    ls = _run(base.replace(q_num=0), 16)
+    assert ls.bud.k_q == 0
+    ls = _run(base.replace(q_num=100), 16)
+    assert ls.bud.k_f == 0
+
+
+def test_budget_above_full_is_dense_attention(lib):
+    """B_total >= the full cache with K_f >= every window: the step is dense softmax attention (torch SDPA)."""
+    wl = synth.workload("tiny_4k", prompt_len=700, steps=16, q_num=0, budget_num=400, n_plant=2)
+    ls = Lockstep(wl)
+    ls.prefill()
+    pk = synth.prompt_inputs(wl, 0, 0)
+    K = [pk["k"].float()]
+    V = [pk["v"].float()]
+    dec = synth.decode_inputs(wl, 0, 0)
+    for s in range(16):
+        K.append(dec["k"][s:s + 1].float())
+        V.append(dec["v"][s:s + 1].float())
+        q = dec["q"][s:s + 1].cuda()
+        out = torch.empty(1, wl.h_q, 128, dtype=torch.bfloat16, device="cuda")
+        ls.cache.decode_step(0, q, dec["k"][s:s + 1].cuda(), dec["v"][s:s + 1].cuda(), out)
+        Kt = torch.cat(K).cuda().permute(1, 0, 2).repeat_interleave(wl.h_q // wl.h_kv, 0)
+        Vt = torch.cat(V).cuda().permute(1, 0, 2).repeat_interleave(wl.h_q // wl.h_kv, 0)
+        ref = torch.nn.functional.scaled_dot_product_attention(q[0].float()[:, None, :], Kt, Vt)[:, 0, :]
+        assert (out[0].float() - ref).abs().max().item() <= OUT_TOL
+        if (s + 1) % wl.omega == 0:
+            ls.cache.route()
+    torch.cuda.synchronize()
+    st = ls.cache.region("state", 0, ls.N).cpu().numpy() & 3
+    assert not np.any(st == O.EVICTED) and not np.any(st == O.QUANT)
+
+
+def test_full_size_llama_shape(lib):
+    """The 32K Llama-3-8B-shaped workload in the bench's launch configuration (batch 1, 8 KV heads),
+    two layers, 16 steps and 2 routing events, every output and window compared."""
+    wl = synth.workload("llama8b_32k", n_layers=2, steps=16)
+    ls = _run(wl, 16, oracle_prefill_scores=False)
+    assert ls.max_out_err <= OUT_TOL
+
+
+def test_status_codes(lib):
+    wl = synth.workload("tiny_4k", prompt_len=600, steps=16, n_plant=2, budget_num=60)
+    cfg = binding.make_config(wl)
+    small = binding.make_config(wl, budget_num=1, budget_den=1000)
+    with pytest.raises(binding.QEvictError) as e:
+        binding.budget(small)
+    assert e.value.status == binding.EBUDGET
+    with pytest.raises(binding.QEvictError) as e:
+        binding.Cache(cfg, arena=torch.empty(1024, dtype=torch.uint8, device="cuda"))
+    assert e.value.status == binding.ENOMEM
+    with pytest.raises(binding.QEvictError) as e:
+        binding.budget(binding.make_config(wl, d_head=64))
+    assert e.value.status == binding.EINVAL
+    c = binding.Cache(cfg)
+    q = torch.zeros(1, wl.h_q, 128, dtype=torch.bfloat16, device="cuda")
+    kv = torch.zeros(1, wl.h_kv, 128, dtype=torch.bfloat16, device="cuda")
+    out = torch.empty_like(q)
+    with pytest.raises(binding.QEvictError) as e:     # decode before prefill
+        c.decode_step(0, q, kv, kv, out)
+    assert e.value.status == binding.ESCHEDULE
+    p = synth.prompt_inputs(wl, 0, 0)
+    s0 = torch.rand(1, O.prompt_windows(O.Config.from_obj(wl)), device="cuda")
+    c.prefill_route(0, p["k"][None].cuda(), p["v"][None].cuda(), s0=s0)
+    with pytest.raises(binding.QEvictError) as e:     # prefill twice
+        c.prefill_route(0, p["k"][None].cuda(), p["v"][None].cuda(), s0=s0)
+    assert e.value.status == binding.ESCHEDULE
+    with pytest.raises(binding.QEvictError) as e:     # route off the Omega cadence
+        c.route()
+    assert e.value.status == binding.ESCHEDULE
+    for _ in range(wl.omega):
+        c.decode_step(0, q, kv, kv, out)
+    with pytest.raises(binding.QEvictError) as e:     # a routing event is due
+        c.decode_step(0, q, kv, kv, out)
+    assert e.value.status == binding.ESCHEDULE
+    c.route()
+    c.decode_step(0, q, kv, kv, out)
+    c.check()
