@@ -1,0 +1,516 @@
+"""Benchmark of the QEvict decode step on GB300: decode steps/s and achieved HBM GB/s at 32K context.
+
+One step = for every layer: append + split-K attention over sink / Full / Quantized / recent
+windows + window-score update (one qevict_decode_step launch per layer), plus a routing event
+(route + quantise + promote/copy launches) after every Omega-th step, for all sequences.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload llama8b_32k] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  `value` is whole-job decode steps/s with the inputs resident in HBM
+(CUDA-graph replay of exactly K steps, CUDA events on the launching stream); `e2e` is the same
+metric with every step's inputs copied from pinned host memory and its outputs copied back inside
+the timed region; `roofline` is the decode kernel's algorithmic bytes per launch over its average
+launch duration (CUDA events around each launch of an event-bracketed pass over the same
+workload), against the measured HBM copy bandwidth.  `--impl reference` times the CPU oracle.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode steps/sec and achieved HBM GB/s (% of GB300 peak) at 32K ctx, 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+D = 128
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--workload", default="llama8b_32k")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-sample-steps", type=int, default=8)
+    ap.add_argument("--oracle-child", default=None, help=argparse.SUPPRESS)
+    return ap.parse_args()
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", FALLBACK_HBM_GBS)), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# --------------------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML (the driver's library, read only)
+    every ~2 ms while active; falls back to nvidia-smi polling when NVML cannot be loaded."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting", 0x1: "gpu_idle"}
+
+    def __init__(self, bus_id: str):
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self._stop = threading.Event()
+        self._on = threading.Event()
+        self._nvml = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            assert nv.nvmlInit_v2() == 0
+            h = ctypes.c_void_p()
+            assert nv.nvmlDeviceGetHandleByPciBusId_v2(bus_id.encode(), ctypes.byref(h)) == 0
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = mx.value
+            self._nvml, self._h = nv, h
+            self._getr = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        except Exception:
+            self._nvml = None
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+
+    def _run(self):
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self._on.is_set() and self._nvml is not None:
+                if self._nvml.nvmlDeviceGetClockInfo(self._h, 1, ctypes.byref(clk)) == 0:
+                    self.samples.append(clk.value)
+                if self._getr(self._h, ctypes.byref(rs)) == 0:
+                    for bit, name in self.REASONS.items():
+                        if rs.value & bit and name != "gpu_idle":
+                            self.reasons.add(name)
+            time.sleep(0.002)
+
+    def start(self):
+        self._on.set()
+
+    def pause(self):
+        self._on.clear()
+
+    def close(self):
+        self._stop.set()
+        self._t.join(timeout=2)
+
+    def smi_snapshot(self):
+        try:
+            out = subprocess.run(["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm", "--format=csv,noheader,nounits",
+                                  "-i", "0"], capture_output=True, text=True, timeout=20).stdout.strip().splitlines()
+            a, b = out[0].split(",")
+            return int(a), int(b)
+        except Exception:
+            return None, None
+
+    def summary(self):
+        med = statistics.median(self.samples) if self.samples else None
+        if med is None:
+            med, mx = self.smi_snapshot()
+            self.max_mhz = self.max_mhz or mx
+        return {"sm_mhz": med, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                "samples": len(self.samples), "source": "nvml" if self._nvml is not None else "nvidia-smi"}
+
+
+# --------------------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample(wl_name: str, steps: int, layers: int = 1) -> dict:
+    """Times the CPU oracle on a bounded sample of the workload: one (sequence, layer) unit, its
+    prefill routing (untimed), `steps` decode steps and one routing event; scaled to whole steps
+    (every layer and sequence, routing amortised over Omega)."""
+    import numpy as np
+    from oracle import qevict_oracle as O
+    from recoverable_quantized_kv_gb300 import synth
+    wl = synth.workload(wl_name)
+    cfg = O.Config.from_obj(wl)
+    rng = np.random.default_rng(12345)
+    t_dec, t_route = [], []
+    for layer in range(layers):
+        u = O.Unit(cfg)
+        p = synth.prompt_inputs(wl, 0, layer, with_queries=False)
+        s0 = rng.random(O.prompt_windows(cfg))          # scores are inputs here: timing does not depend on them
+        u.prefill_route(p["k"].float().numpy(), p["v"].float().numpy(), s0)
+        dec = synth.decode_inputs(wl, 0, layer, steps=max(steps, wl.omega))
+        for s in range(steps):
+            t0 = time.perf_counter()
+            u.decode_step(dec["q"][s].float().numpy(), dec["k"][s].float().numpy(), dec["v"][s].float().numpy())
+            t_dec.append(time.perf_counter() - t0)
+        for s in range(steps, wl.omega):
+            u.decode_step(dec["q"][s].float().numpy(), dec["k"][s].float().numpy(), dec["v"][s].float().numpy())
+        t0 = time.perf_counter()
+        u.route()
+        t_route.append(time.perf_counter() - t0)
+    td, tr = statistics.mean(t_dec), statistics.mean(t_route)
+    per_step = wl.n_layers * wl.batch * (td + tr / wl.omega)
+    return {"value": 1.0 / per_step, "unit": "steps/s", "layer_step_s": td, "route_s": tr,
+            "sample": f"oracle on {layers} (sequence, layer) unit(s) of {wl_name}: {steps} decode steps + 1 routing "
+                      f"event timed, scaled x{wl.n_layers * wl.batch} units with routing amortised over Omega="
+                      f"{wl.omega}"}
+
+
+def run_oracle_child(args):
+    """Runs in a subprocess with one BLAS/OpenMP thread so `cores` is exact."""
+    r = oracle_sample(args.workload, args.cpu_sample_steps)
+    print(json.dumps(r))
+
+
+def cpu_baseline(args, steps):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    t0 = time.time()
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--workload", args.workload,
+                        "--cpu-sample-steps", str(steps), "--oracle-child", "1"], capture_output=True, text=True,
+                       env=env, timeout=1800)
+    if r.returncode != 0:
+        return {"value": None, "unit": "steps/s", "cores": 1, "kind": "oracle", "error": r.stderr[-400:]}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    d.update({"cores": 1, "kind": "oracle", "cpu": _cpu_model(), "host_cores": len(os.sched_getaffinity(0)),
+              "wall_s": round(time.time() - t0, 1)})
+    return d
+
+
+def _cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part", "hardware")):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return os.uname().machine
+
+
+# --------------------------------------------------------------------------------------- GPU bench
+
+def algorithmic_bytes(wl, f_count, q_count, local_tokens, payload):
+    """Bytes a decode launch must move for one (sequence, layer): Full windows bf16 K+V, Quantized
+    windows' codes + parameters, sink + recent tokens, table entries, one score read+write per
+    accessible window, and the step's q / out / k_new / v_new / ring write."""
+    c_tok = 4 * wl.h_kv * D
+    W = wl.window
+    n_local_windows = math.ceil(local_tokens / W)
+    return (f_count * W * c_tok + q_count * payload + (wl.n_sink + local_tokens) * c_tok
+            + (f_count + q_count) * 8 + 8 * (f_count + q_count + n_local_windows)
+            + 2 * wl.h_q * D * 2 + 2 * wl.h_kv * D * 2 + c_tok)
+
+
+def route_bytes(wl, n_cand, firstq, promo, aged, payload):
+    c_tok = 4 * wl.h_kv * D
+    W = wl.window
+    return 8 * n_cand + firstq * (W * c_tok + payload) + promo * (payload + W * c_tok) + aged * (W * c_tok + W * c_tok)
+
+
+def traffic_from_profile(kernel_sha):
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    return d.get("dram_bytes_per_launch") if d.get("kernel_source_sha") == kernel_sha else None
+
+
+def kernel_sha():
+    h = hashlib.sha256()
+    for f in ("decode.cu", "common.cuh", "cache_dev.cuh"):
+        with open(os.path.join(ROOT, "recoverable_quantized_kv_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def run_gpu(args, rank, world):
+    import numpy as np
+    import torch
+    from recoverable_quantized_kv_gb300 import binding, build, synth
+    build.build()
+    binding.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    wl = synth.workload(args.workload)
+    K, Wm = args.steps, args.warmup
+    Om = wl.omega
+    K_kern = 2 * Om
+    K_e2e = 0 if args.no_e2e else K
+    total = Wm + K_kern + K + K_e2e
+    steps_cap = max(wl.steps, int(math.ceil(total / Om) * Om) + Om)
+    cfg = binding.make_config(wl, max_len=wl.prompt_len + steps_cap)
+    cache = binding.Cache(cfg, device=dev)
+    bud = cache.bud
+    L, B = wl.n_layers, wl.batch
+    stream = torch.cuda.Stream(device=dev)      # graphs cannot be captured on the legacy default stream
+    torch.cuda.set_stream(stream)
+
+    # ---- prefill every layer (inputs generated on the device; scores from prompt attention)
+    t_pre = time.time()
+    for layer in range(L):
+        ins = [synth.prompt_inputs(wl, b, layer, device=dev) for b in range(B)]
+        q = torch.stack([x["q"] for x in ins])
+        k = torch.stack([x["k"] for x in ins])
+        v = torch.stack([x["v"] for x in ins])
+        cache.prefill_route(layer, k, v, s0=None, q_prompt=q)
+        del ins, q, k, v
+    torch.cuda.synchronize()
+    t_pre = time.time() - t_pre
+
+    # ---- decode inputs for every step resident in HBM: [step][layer][B][...]
+    qs = torch.empty(total, L, B, wl.h_q, D, dtype=torch.bfloat16, device=dev)
+    ks = torch.empty(total, L, B, wl.h_kv, D, dtype=torch.bfloat16, device=dev)
+    vs = torch.empty_like(ks)
+    for layer in range(L):
+        for b in range(B):
+            d = synth.decode_inputs(wl, b, layer, steps=total, device=dev)
+            qs[:, layer, b] = d["q"]
+            ks[:, layer, b] = d["k"]
+            vs[:, layer, b] = d["v"]
+    outs = torch.empty(L, B, wl.h_q, D, dtype=torch.bfloat16, device=dev)
+    state = {"step": 0, "launches": 0}
+
+    def one_step(i, q_src=None, k_src=None, v_src=None, out_dst=None, events=None):
+        for layer in range(L):
+            if events is not None:
+                events[layer][0].record(stream)
+            cache.decode_step(layer, (q_src if q_src is not None else qs[i])[layer],
+                              (k_src if k_src is not None else ks[i])[layer],
+                              (v_src if v_src is not None else vs[i])[layer],
+                              (out_dst if out_dst is not None else outs)[layer], stream)
+            if events is not None:
+                events[layer][1].record(stream)
+            state["launches"] += 1
+        state["step"] += 1
+        if state["step"] % Om == 0:
+            cache.route(stream)
+            state["launches"] += 3
+
+    def read_meta():
+        lay = cache.layout
+        ms = []
+        for u in range(L * B):
+            off = lay.off_meta + u * lay.stride_meta
+            ms.append(cache.arena[off:off + 64].view(torch.int32).cpu().numpy().copy())
+        return ms
+
+    # ---- warm-up (untimed)
+    for _ in range(Wm):
+        one_step(state["step"])
+    torch.cuda.synchronize()
+
+    # ---- event-bracketed pass: decode kernel duration and the algorithmic bytes of each launch
+    kern_ms, kern_bytes, step_bytes = [], [], []
+    c0 = cache.counters()
+    for _ in range(K_kern):
+        metas = read_meta()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
+        i = state["step"]
+        one_step(i, events=ev)
+        torch.cuda.synchronize()
+        sb = 0
+        for layer in range(L):
+            by = 0
+            for b in range(B):
+                m = metas[layer * B + b]
+                T, n_route, nf, nq = int(m[0]), int(m[1]), int(m[2]), int(m[3])
+                local = T - wl.n_sink - n_route * wl.window + 1
+                by += algorithmic_bytes(wl, nf, nq, local, bud.payload)
+            kern_ms.append(ev[layer][0].elapsed_time(ev[layer][1]))
+            kern_bytes.append(by)
+            sb += by
+        step_bytes.append(sb)
+    c1 = cache.counters()
+    n_events = K_kern // Om
+    rb = route_bytes(wl, (bud.k_f + bud.k_q) * L * B * n_events, c1["first_quant"] - c0["first_quant"],
+                     c1["promotions"] - c0["promotions"], (c1["aged_full"] - c0["aged_full"]), bud.payload)
+    bytes_per_step = statistics.mean(step_bytes) + rb / K_kern
+
+    # ---- timed region: exactly K steps, captured once in a CUDA graph and replayed once
+    launches_before = state["launches"]
+    g = torch.cuda.CUDAGraph()
+    first = state["step"]
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(K):
+            one_step(first + i)
+    timed_launches = state["launches"] - launches_before
+    torch.cuda.synchronize()
+    sampler = ClockSampler(_bus_id(torch, dev))
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.start()
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.pause()
+    if world > 1:
+        torch.distributed.barrier()
+    ms_total = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    cache.check(stream)
+
+    # ---- e2e: inputs from pinned host memory, outputs back to pinned host memory, every step
+    e2e = None
+    if K_e2e:
+        hq = torch.empty(K_e2e, L, B, wl.h_q, D, dtype=torch.bfloat16, pin_memory=True)
+        hk = torch.empty(K_e2e, L, B, wl.h_kv, D, dtype=torch.bfloat16, pin_memory=True)
+        hv = torch.empty_like(hk, pin_memory=True)
+        s_e = state["step"]
+        hq.copy_(qs[s_e:s_e + K_e2e].cpu())
+        hk.copy_(ks[s_e:s_e + K_e2e].cpu())
+        hv.copy_(vs[s_e:s_e + K_e2e].cpu())
+        ho = torch.empty(K_e2e, L, B, wl.h_q, D, dtype=torch.bfloat16, pin_memory=True)
+        dq = torch.empty(L, B, wl.h_q, D, dtype=torch.bfloat16, device=dev)
+        dk = torch.empty(L, B, wl.h_kv, D, dtype=torch.bfloat16, device=dev)
+        dv = torch.empty_like(dk)
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2, stream=stream):
+            for i in range(K_e2e):
+                dq.copy_(hq[i], non_blocking=True)
+                dk.copy_(hk[i], non_blocking=True)
+                dv.copy_(hv[i], non_blocking=True)
+                one_step(s_e + i, dq, dk, dv, outs)
+                ho[i].copy_(outs, non_blocking=True)
+        torch.cuda.synchronize()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        g2.replay()
+        f1.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = f0.elapsed_time(f1)
+        if world > 1:
+            t = torch.tensor([ms_e2e], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms_e2e = float(t.item())
+        in_bytes = (hq[0].numel() + hk[0].numel() + hv[0].numel()) * 2
+        e2e = {"value": world * K_e2e / (ms_e2e / 1e3), "unit": "steps/s", "h2d_bytes_per_step": in_bytes,
+               "d2h_bytes_per_step": ho[0].numel() * 2, "ms_per_step": ms_e2e / K_e2e,
+               "timing": "CUDA graph of the C-ABI calls with pinned-host copies, CUDA events"}
+        cache.check(stream)
+    clocks = sampler.summary()
+    sampler.close()
+
+    peak, peak_kind = measured_peaks()
+    avg_kern_ms = statistics.mean(kern_ms)
+    bytes_per_launch = statistics.mean(kern_bytes)
+    achieved = bytes_per_launch / (avg_kern_ms / 1e3) / 1e9
+    sha = kernel_sha()
+    ms_step = ms_total / K
+    result = {
+        "metric": METRIC, "value": world * K / (ms_total / 1e3), "unit": "steps/s", "n_gpus": world, "steps": K,
+        "warmup": Wm, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": B, "layers": L, "h_q": wl.h_q, "h_kv": wl.h_kv, "d_head": D,
+                   "prompt_len": wl.prompt_len, "decode_steps_cached": steps_cap, "window": wl.window,
+                   "bits": wl.bits, "omega": Om, "budget": f"{wl.budget_num}/{wl.budget_den}",
+                   "q": f"{wl.q_num}/{wl.q_den}", "k_f": bud.k_f, "k_q": bud.k_q,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: each step streams every layer's cache (%.0f MB)" %
+                         (bytes_per_step / 1e6)},
+        "hbm_gbs_step": bytes_per_step / (ms_step / 1e3) / 1e9,
+        "hbm_frac_step": bytes_per_step / (ms_step / 1e3) / 1e9 / peak,
+        "bytes_per_step": bytes_per_step,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic_from_profile(sha), "peak_kind": f"{peak_kind} copy bandwidth",
+                     "kernel": "decode_kernel", "bytes_per_launch": bytes_per_launch, "avg_launch_us": avg_kern_ms * 1e3,
+                     "launches_timed": len(kern_ms), "kernel_source_sha": sha,
+                     "vs_8tbs": achieved / 8000.0},
+        "gpu_launches": timed_launches,
+        "clocks": clocks,
+        "prefill_s": round(t_pre, 2),
+    }
+    if e2e:
+        result["e2e"] = e2e
+    return result
+
+
+def _bus_id(torch, dev):
+    p = torch.cuda.get_device_properties(dev)
+    return "%08x:%02x:%02x.0" % (getattr(p, "pci_domain_id", 0), p.pci_bus_id, p.pci_device_id)
+
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: K decode steps of one (sequence, layer) unit after W
+    warm-up steps, routing every Omega steps, each step scaled to every layer and sequence."""
+    if rank != 0:
+        return None
+    import numpy as np
+    from oracle import qevict_oracle as O
+    from recoverable_quantized_kv_gb300 import synth
+    wl = synth.workload(args.workload)
+    cfg = O.Config.from_obj(wl, max_len=wl.prompt_len + args.warmup + args.steps + wl.omega)
+    u = O.Unit(cfg)
+    p = synth.prompt_inputs(wl, 0, 0, with_queries=False)
+    u.prefill_route(p["k"].float().numpy(), p["v"].float().numpy(),
+                    np.random.default_rng(12345).random(O.prompt_windows(cfg)))
+    dec = synth.decode_inputs(wl, 0, 0, steps=args.warmup + args.steps)
+    t = 0.0
+    for s in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        u.decode_step(dec["q"][s].float().numpy(), dec["k"][s].float().numpy(), dec["v"][s].float().numpy())
+        if (s + 1) % wl.omega == 0:
+            u.route()
+        if s >= args.warmup:
+            t += time.perf_counter() - t0
+    per_step = t / args.steps * wl.n_layers * wl.batch
+    value = 1.0 / per_step
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "batch": wl.batch, "layers": wl.n_layers, "prompt_len": wl.prompt_len},
+            "cpu_baseline": {"value": value, "unit": "steps/s", "kind": "oracle",
+                             "cores": _threads_hint(), "cpu": _cpu_model(),
+                             "sample": f"oracle, one (sequence, layer) unit per step of {wl.name}, routing every "
+                                       f"{wl.omega} steps, scaled x{wl.n_layers * wl.batch} units"},
+            "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def _threads_hint():
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS"):
+        if os.environ.get(k):
+            return int(os.environ[k])
+    return len(os.sched_getaffinity(0))
+
+
+def main():
+    args = parse_args()
+    if args.oracle_child:
+        run_oracle_child(args)
+        return
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        r = run_reference(args, rank, world)
+        if r is not None:
+            print(json.dumps(r))
+        return
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    res = run_gpu(args, rank, world)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline(args, args.cpu_sample_steps)
+        print(json.dumps(res))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -100,10 +100,14 @@ typedef struct {
  *   V element (tok, dim):          index (((tok/16)*8 + dim/16)*32 + lane)*8 + reg*2 + (tok%2)
  *   where for K: r = tok%16, c = dim%16; for V: r = dim%16, c = tok%16;
  *   lane = (r%8)*4 + (c%8)/2 and reg = r/8 + 2*(c/8)  (the m16n8k16 A-operand register map).
- * Fragment-native codes: the same (group, lane, reg, half) map; group = (tok/16)*8 + dim/16;
- *   element e = reg*2 + half; each (group, lane) owns one field of `bits` bytes stored at lane
- *   byte b = group*bits + e_byte, placed at (b/16)*512 + lane*16 + b%16 within the K or V codes.
- *   INT2 bit of e inside the 16-bit field: 4e for e < 4, 4(e-4)+2 for e >= 4.  INT4: 4e.
+ * Fragment-native INT2 codes (W = 32; 1 KB per K or V block): each of the 32 lanes owns 32 bytes,
+ * stored as two 16-byte pieces at piece*512 + lane*16 + (byte%16), lane byte b -> piece b/16.
+ *   K element (tok, dim): with r, c, lane, reg as above, group = (tok/16)*8 + dim/16,
+ *     e = reg*2 + dim%2, bit = 4e (e < 4) or 4(e-4)+2 (e >= 4) inside the 16-bit field of
+ *     (group, lane), which is lane bytes 2*group, 2*group+1 (little-endian).
+ *   V element (tok, dim): with r = dim%16, c = tok%16, lane and reg as above, i = dim/16,
+ *     rr = (i%2)*4 + reg, word w = (tok/16)*4 + i/2 (lane bytes 4w .. 4w+3, little-endian),
+ *     bit = (rr < 5 ? 2*rr : 10 + 2*(rr-5)) + 16*(tok%2) inside that word.
  */
 typedef struct {
   int64_t off_sink, stride_sink;

@@ -131,7 +131,8 @@ class Cache:
         nbytes = ctypes.c_size_t()
         _check(lib.qevict_cache_bytes(ctypes.byref(cfg), ctypes.byref(nbytes)), "qevict_cache_bytes")
         self.arena = arena if arena is not None else torch.empty(nbytes.value, dtype=torch.uint8, device=device)
-        assert self.arena.numel() >= nbytes.value and self.arena.data_ptr() % 256 == 0
+        if self.arena.data_ptr() % 256:
+            raise QEvictError(EINVAL, "Cache", "arena must be 256-byte aligned")
         h = ctypes.c_void_p()
         _check(lib.qevict_init_cache(ctypes.byref(cfg), self.arena.data_ptr(), self.arena.numel(), _stream(stream),
                                      ctypes.byref(h)), "qevict_init_cache")

@@ -40,18 +40,33 @@ __host__ __device__ __forceinline__ int fnv_index(int tok, int dim) {
   return ((grp * 32 + frag_lane(r, c)) << 3) | (frag_reg(r, c) << 1) | (c & 1);
 }
 
-// Code field of element (tok, dim) in a K (is_v = false) or V code block:
-// returns the byte offset inside the block and the bit shift inside that byte.
-template <int BITS>
-__host__ __device__ __forceinline__ void code_pos(bool is_v, int tok, int dim, int &byte, int &shift) {
-  int r, c;
-  if (!is_v) { r = tok & 15; c = dim & 15; } else { r = dim & 15; c = tok & 15; }
-  const int grp = (tok >> 4) * 8 + (dim >> 4);
-  const int lane = frag_lane(r, c);
-  const int e = (frag_reg(r, c) << 1) | (c & 1);
-  const int bit = (BITS == 2) ? (e < 4 ? 4 * e : 4 * (e - 4) + 2) : 4 * e;
-  const int lb = grp * BITS + (bit >> 3);           // byte inside the lane's stream
-  byte = (lb >> 4) * 512 + lane * 16 + (lb & 15);
+// Position of the INT2 code of element (tok, dim) inside a window's K or V code block (1 KB for
+// W = 32): returns the byte offset and the bit shift inside that byte.  Each lane of the decode warp
+// owns 32 bytes, stored as two 16-byte pieces at piece*512 + lane*16 (conflict-free 128-bit loads).
+//  K: the codes of one m16n8k16 A-register group (16 tokens x 16 channels) form a 16-bit field per
+//     lane; element e = reg*2 + half sits at bit 4e (e < 4) or 4(e-4)+2 (e >= 4), so masking with
+//     0x3333 yields byte-permute selectors directly.
+//  V: one 32-bit word per (16-token group kk, pair of 16-dim tiles); register r = (tile%2)*4 + reg
+//     keeps its two codes (even, odd token) at bits b and b+16 with b = 2r (r < 5) or 10 + 2(r-5),
+//     so one mask (after at most one shift by 10) lands them in fp16 mantissas.
+__host__ __device__ __forceinline__ void code_pos2(bool is_v, int tok, int dim, int &byte, int &shift) {
+  int lb, bit;
+  if (!is_v) {
+    const int r = tok & 15, c = dim & 15, grp = (tok >> 4) * 8 + (dim >> 4);
+    const int lane = frag_lane(r, c);
+    const int e = (frag_reg(r, c) << 1) | (c & 1);
+    bit = e < 4 ? 4 * e : 4 * (e - 4) + 2;
+    lb = grp * 2 + (bit >> 3);
+    byte = (lb >> 4) * 512 + lane * 16 + (lb & 15);
+  } else {
+    const int rr = dim & 15, c = tok & 15, i = dim >> 4;
+    const int lane = frag_lane(rr, c);
+    const int r = ((i & 1) << 2) | frag_reg(rr, c);
+    const int w = (tok >> 4) * 4 + (i >> 1);
+    bit = (r < 5 ? 2 * r : 10 + 2 * (r - 5)) + 16 * (c & 1);
+    lb = 4 * w + (bit >> 3);
+    byte = (lb >> 4) * 512 + lane * 16 + (lb & 15);
+  }
   shift = bit & 7;
 }
 

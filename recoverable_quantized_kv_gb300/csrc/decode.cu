@@ -16,10 +16,12 @@
 
 namespace qv {
 
-constexpr int DEC_WARPS = 8;
-constexpr int DEC_STAGES = 4;
+constexpr int DEC_WARPS = 16;
+constexpr int DEC_STAGES = 3;
 constexpr int DEC_STAGE_BYTES = 4096;
-constexpr int DEC_SMEM = DEC_WARPS * DEC_STAGES * DEC_STAGE_BYTES + DEC_WARPS * DEC_STAGES * 8;
+constexpr int DEC_TBL_BYTES = 1024;   // per-warp key lookup tables: 8 k-steps x 4 lane classes x 32 B
+constexpr int DEC_SMEM = DEC_WARPS * (DEC_STAGES * DEC_STAGE_BYTES + DEC_TBL_BYTES) + DEC_WARPS * DEC_STAGES * 8 +
+                         DEC_WARPS * 8 * 4;
 
 // Work list of one (sequence, KV head): item 0 = the sink tokens, items 1..nL = recent windows
 // j0 .. j0+nL-1, then the F-table entries, then the Q-table entries.  Item costs are the bytes
@@ -124,6 +126,45 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int k) {
   return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
 }
 
+// Exact bf16(fp32(code * s + m)) for keys via per-channel byte tables: lo/hi bytes of the 4
+// dequantised values of channel pair A (2t, 2t+1) and B (2t+8, 2t+9) of k-step j.
+__device__ __forceinline__ void lut_k_regs(uint32_t f, const uint4 &TA, const uint4 &TB, uint32_t &a0, uint32_t &a1,
+                                           uint32_t &a2, uint32_t &a3) {
+  const uint32_t sel01 = (f & 0x3333u) | 0x4040u;
+  const uint32_t sel23 = ((f >> 2) & 0x3333u) | 0x4040u;
+  uint32_t lo = __byte_perm(TA.x, TA.y, sel01), hi = __byte_perm(TA.z, TA.w, sel01);
+  a0 = __byte_perm(lo, hi, 0x5140);
+  a1 = __byte_perm(lo, hi, 0x7362);
+  lo = __byte_perm(TB.x, TB.y, sel23);
+  hi = __byte_perm(TB.z, TB.w, sel23);
+  a2 = __byte_perm(lo, hi, 0x5140);
+  a3 = __byte_perm(lo, hi, 0x7362);
+}
+
+// Value codes as exact fp16 integers: mask two codes into fp16 mantissas under exponent 2^10
+// (value 1024 + 4^p c), then one packed fma (x - 1024) * 4^-p recovers c exactly.
+__device__ __forceinline__ uint32_t dq_v(uint32_t w, int p) {
+  static constexpr uint32_t SCL[5] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u, 0x1C001C00u};
+  static constexpr uint32_t OFF[5] = {0xE400E400u, 0xDC00DC00u, 0xD400D400u, 0xCC00CC00u, 0xC400C400u};
+  const uint32_t x = (w & (0x00030003u << (2 * p))) | 0x64006400u;
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(SCL[p]), "r"(OFF[p]));
+  return r;
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_half(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&v);
+}
+
 template <int W, int BITS>
 __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDev C, const DecodeIO io) {
   static_assert(W == 32 && BITS == 2, "decode kernel instantiated for W=32, INT2");
@@ -150,27 +191,42 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   float *part = reinterpret_cast<float *>(C.arena + C.off_part + C.st_part_layer * io.layer) +
                 (size_t)bg * C.n_split * PART_FLOATS;
 
-  Items I;
   const int jn = (T - C.n_sink) / W;   // window of the new token at position T
-  I.j0 = n_route;
-  I.nL = jn - n_route + 1;
-  I.nF = nF;
-  I.nQ = nQ;
-  I.cs = (long long)C.n_sink * 2 * D * 2;
-  I.cw = 2LL * W * D * 2;
-  I.cq = Gm::QB;
-  const int nparts = C.n_split * DEC_WARPS;
-  const int i0 = I.bound(split * DEC_WARPS + warp, nparts);
-  const int i1 = I.bound(split * DEC_WARPS + warp + 1, nparts);
+  const int j0 = n_route;
+  const int nL = jn - n_route + 1;
+  // this CTA's proportional slice of every class; item ids: 0 sink, 1..nL recent, then F, then Q
+  const int ns = C.n_split;
+  const int L0 = split * nL / ns, L1 = (split + 1) * nL / ns;
+  const int F0 = split * nF / ns, F1 = (split + 1) * nF / ns;
+  const int Q0 = split * nQ / ns, Q1 = (split + 1) * nQ / ns;
+  const int has_sink = split == 0 ? 1 : 0;
+  const int cta_items = has_sink + (L1 - L0) + (F1 - F0) + (Q1 - Q0);
+  auto item_of = [&](int k) -> int {
+    if (has_sink) {
+      if (k == 0) return 0;
+      k -= 1;
+    }
+    if (k < L1 - L0) return 1 + L0 + k;
+    k -= L1 - L0;
+    if (k < F1 - F0) return 1 + nL + F0 + k;
+    k -= F1 - F0;
+    return 1 + nL + nF + Q0 + k;
+  };
 
   uint8_t *stage = smem + warp * DEC_STAGES * DEC_STAGE_BYTES;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + DEC_WARPS * DEC_STAGES * DEC_STAGE_BYTES) + warp * DEC_STAGES;
+  uint8_t *tbl = smem + DEC_WARPS * DEC_STAGES * DEC_STAGE_BYTES + warp * DEC_TBL_BYTES;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + DEC_WARPS * (DEC_STAGES * DEC_STAGE_BYTES + DEC_TBL_BYTES)) +
+                   warp * DEC_STAGES;
+  int *gring = reinterpret_cast<int *>(smem + DEC_WARPS * (DEC_STAGES * DEC_STAGE_BYTES + DEC_TBL_BYTES) +
+                                       DEC_WARPS * DEC_STAGES * 8) + warp * 8;
+  __shared__ int q_next;
+  if (threadIdx.x == 0) q_next = 0;
   if (lane == 0) {
 #pragma unroll
-    for (int s = 0; s < DEC_STAGES; ++s) mbar_init(&bars[s], 1);
+    for (int st = 0; st < DEC_STAGES; ++st) mbar_init(&bars[st], 1);
     fence_mbar_init();
   }
-  __syncwarp();
+  __syncthreads();
 
   // q as the B operand of S^T = K q^T: b0 = q[head gl][16j+2tl .. +1], b1 = the same at +8.
   uint32_t qb[8][2];
@@ -183,46 +239,63 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
     }
   }
 
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f}, macc[2] = {0.f, 0.f};
   float o[8][4];
 #pragma unroll
   for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
 
-  // ---- chunk stream: bf16 windows = NMT K chunks then NMT V chunks (4 KB each); Q window = 1 chunk
-  auto n_chunks = [&](int it) -> int { return it == 0 ? 0 : (it <= I.nL + I.nF ? 2 * NMT : 1); };
+  // ---- chunk stream.  bf16 window: NMT K chunks then NMT V chunks (4 KB each).  Q window: 1 chunk.
+  auto n_chunks = [&](int it) -> int { return it == 0 ? 0 : (it <= nL + nF ? 2 * NMT : 1); };
   auto chunk_src = [&](int it, int sub, const void *&src, uint32_t &bytes) {
-    if (it <= I.nL) {                                   // recent window in the ring
-      const int rs = (I.j0 + it - 1) % C.ring_windows;
+    if (it <= nL) {
+      const int rs = (j0 + it - 1) % C.ring_windows;
       const __nv_bfloat16 *kb = ring + (size_t)rs * Gm::BLK;
       const __nv_bfloat16 *vb = ring + (size_t)(C.ring_windows + rs) * Gm::BLK;
       src = sub < NMT ? (const void *)(kb + sub * 2048) : (const void *)(vb + (sub - NMT) * 2048);
       bytes = DEC_STAGE_BYTES;
-    } else if (it <= I.nL + I.nF) {                     // Full window
-      const int slot = __ldg(&ftab[it - 1 - I.nL].y);
-      const uint8_t *base = fpool + ((size_t)slot * C.h_kv + g) * 2 * Gm::BLK * 2;
-      src = base + (size_t)sub * DEC_STAGE_BYTES;
+    } else if (it <= nL + nF) {
+      const int slot = __ldg(&ftab[it - 1 - nL].y);
+      src = fpool + ((size_t)slot * C.h_kv + g) * 2 * Gm::BLK * 2 + (size_t)sub * DEC_STAGE_BYTES;
       bytes = DEC_STAGE_BYTES;
-    } else {                                            // Quantized window: one ledger block
-      const int slot = __ldg(&qtab[it - 1 - I.nL - I.nF].y);
+    } else {
+      const int slot = __ldg(&qtab[it - 1 - nL - nF].y);
       src = ledger + ((size_t)slot * C.h_kv + g) * Gm::QB;
       bytes = Gm::QB;
     }
   };
-  int issued = 0, consumed = 0;
-  int p_it = i0, p_sub = 0;
-  bool ok = true;
+  int issued = 0, consumed = 0;      // chunks
+  int ngrab = 0, p_idx = 0, p_sub = 0, c_idx = 0;
+  bool exhausted = false, ok = true;
+  auto grab = [&]() {
+    int k = 0;
+    if (lane == 0) k = atomicAdd(&q_next, 1);
+    k = __shfl_sync(0xffffffffu, k, 0);
+    if (k >= cta_items) {
+      exhausted = true;
+      return;
+    }
+    gring[ngrab & 7] = item_of(k);
+    __syncwarp();
+    ++ngrab;
+  };
   auto issue = [&]() {
-    while (issued - consumed < DEC_STAGES && p_it < i1) {
-      const int nc = n_chunks(p_it);
+    while (issued - consumed < DEC_STAGES) {
+      if (p_idx == ngrab) {
+        if (exhausted || ngrab - c_idx >= 7) break;
+        grab();
+        if (exhausted) break;
+      }
+      const int it = gring[p_idx & 7];
+      const int nc = n_chunks(it);
       if (nc == 0) {
-        ++p_it;
+        ++p_idx;
         p_sub = 0;
         continue;
       }
       if (lane == 0) {
         const void *src;
         uint32_t bytes;
-        chunk_src(p_it, p_sub, src, bytes);
+        chunk_src(it, p_sub, src, bytes);
         const int st = issued % DEC_STAGES;
         fence_proxy_async();
         mbar_arrive_expect_tx(&bars[st], bytes);
@@ -230,7 +303,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
       }
       ++issued;
       if (++p_sub == nc) {
-        ++p_it;
+        ++p_idx;
         p_sub = 0;
       }
     }
@@ -242,11 +315,20 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   };
 
   issue();
-  for (int it = i0; it < i1 && ok; ++it) {
+  while (ok) {
+    if (c_idx == ngrab) {
+      issue();
+      if (c_idx == ngrab) {
+        if (exhausted) break;
+        grab();
+        if (exhausted) break;
+      }
+    }
+    const int it = gring[c_idx & 7];
     float tsum[2], mnew[2];
     if (it == 0) {
       // ---------------- sink tokens (no mass): fragments straight from the compact sink rows
-      float s[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+      float sacc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
       const __nv_bfloat16 *sk = sink, *sv = sink + (size_t)C.n_sink * D;
       const bool r0 = gl < C.n_sink, r1 = gl + 8 < C.n_sink;
 #pragma unroll
@@ -255,15 +337,18 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
         const uint32_t a1 = r1 ? ldg32(sk + (gl + 8) * D + 16 * j + 2 * tl) : 0u;
         const uint32_t a2 = r0 ? ldg32(sk + gl * D + 16 * j + 2 * tl + 8) : 0u;
         const uint32_t a3 = r1 ? ldg32(sk + (gl + 8) * D + 16 * j + 2 * tl + 8) : 0u;
-        mma_bf16(s[0], a0, a1, a2, a3, qb[j][0], qb[j][1]);
+        mma_bf16(sacc[0], a0, a1, a2, a3, qb[j][0], qb[j][1]);
       }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) s[0][k] *= io.scale_log2;
+      for (int k = 0; k < 4; ++k) sacc[0][k] *= io.scale_log2;
       const bool valid[1][2] = {{r0, r1}};
-      online_step<1>(s, valid, m_run, l_run, o, tsum, mnew);
+      const float mold0 = m_run[0], mold1 = m_run[1];
+      online_step<1>(sacc, valid, m_run, l_run, o, tsum, mnew);
+      macc[0] *= exp2f(mold0 - (m_run[0] == -INFINITY ? 0.f : m_run[0]));
+      macc[1] *= exp2f(mold1 - (m_run[1] == -INFINITY ? 0.f : m_run[1]));
       uint32_t pb[1][2];
-      p_to_b<1>(s, pb);
-      const int t0 = 2 * tl, t1 = 2 * tl + 8;   // token rows of this lane's B/A columns
+      p_to_b<1>(sacc, pb);
+      const int t0 = 2 * tl, t1 = 2 * tl + 8;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int d0 = 16 * i + gl, d1 = d0 + 8;
@@ -274,19 +359,19 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
         const uint32_t a3 = vv(t1, d1) | (vv(t1 + 1, d1) << 16);
         mma_bf16(o[i], a0, a1, a2, a3, pb[0][0], pb[0][1]);
       }
+      ++c_idx;
       continue;
     }
 
-    int wid;
     bool valid[NMT][2];
     float s[NMT][4];
 #pragma unroll
     for (int mt = 0; mt < NMT; ++mt) s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
 
-    if (it <= I.nL + I.nF) {
+    if (it <= nL + nF) {
       // ---------------- bf16 window (recent or Full)
-      const bool is_local = it <= I.nL;
-      wid = is_local ? I.j0 + it - 1 : __ldg(&ftab[it - 1 - I.nL].x);
+      const bool is_local = it <= nL;
+      const int wid = is_local ? j0 + it - 1 : __ldg(&ftab[it - 1 - nL].x);
       const int newtok = (is_local && wid == jn) ? T - (C.n_sink + jn * W) : -1;
       const uint8_t *kc[NMT];
 #pragma unroll
@@ -331,7 +416,10 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
 #pragma unroll
         for (int k = 0; k < 4; ++k) s[mt][k] *= io.scale_log2;
       }
+      const float mold0 = m_run[0], mold1 = m_run[1];
       online_step<NMT>(s, valid, m_run, l_run, o, tsum, mnew);
+      macc[0] *= exp2f(mold0 - (m_run[0] == -INFINITY ? 0.f : m_run[0]));
+      macc[1] *= exp2f(mold1 - (m_run[1] == -INFINITY ? 0.f : m_run[1]));
       uint32_t pb[NMT][2];
       p_to_b<NMT>(s, pb);
       const uint8_t *vc[NMT];
@@ -364,26 +452,39 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
       consumed += NMT;
       issue();
     } else {
-      // ---------------- Quantized window: INT2 codes + fp16 params, dequantised in registers
-      wid = __ldg(&qtab[it - 1 - I.nL - I.nF].x);
+      // ---------------- Quantized window: INT2 codes + fp16 scale/offset
       const uint8_t *ch = wait_chunk(consumed);
-      const uint4 kcw[NMT] = {lds128(ch + lane * 16), lds128(ch + 512 + lane * 16)};
-      const uint4 vcw[NMT] = {lds128(ch + Gm::OFF_VCODE + lane * 16), lds128(ch + Gm::OFF_VCODE + 512 + lane * 16)};
+      // key tables: channel d = 4*lane + k, values bf16(fp32(c*s + m)), c = 0..3, split in lo / hi bytes
+      {
+        const uint2 sp = *reinterpret_cast<const uint2 *>(ch + Gm::OFF_KS + 8 * lane);
+        const uint2 mp = *reinterpret_cast<const uint2 *>(ch + Gm::OFF_KM + 8 * lane);
+        uint32_t *tw = reinterpret_cast<uint32_t *>(tbl);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t sw = k < 2 ? sp.x : sp.y, mw = k < 2 ? mp.x : mp.y;
+          const float sc = (k & 1) ? h2f_hi(sw) : h2f_lo(sw);
+          const float mn = (k & 1) ? h2f_hi(mw) : h2f_lo(mw);
+          const uint32_t p01 = pack_bf16(mn, __fadd_rn(sc, mn));
+          const uint32_t p23 = pack_bf16(__fmaf_rn(2.f, sc, mn), __fmaf_rn(3.f, sc, mn));
+          const int d = 4 * lane + k, j = d >> 4, c16 = d & 15;
+          const int t = (c16 & 7) >> 1, which = c16 >> 3, half = c16 & 1;
+          const int base = (j * 4 + t) * 8 + which * 4 + half;
+          tw[base] = __byte_perm(p01, p23, 0x6420);
+          tw[base + 2] = __byte_perm(p01, p23, 0x7531);
+        }
+      }
+      __syncwarp();
+      const uint4 kcw0 = lds128(ch + lane * 16), kcw1 = lds128(ch + 512 + lane * 16);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const uint32_t spA = lds32(ch + Gm::OFF_KS + 2 * (16 * j + 2 * tl));
-        const uint32_t spB = lds32(ch + Gm::OFF_KS + 2 * (16 * j + 2 * tl + 8));
-        const uint32_t mpA = lds32(ch + Gm::OFF_KM + 2 * (16 * j + 2 * tl));
-        const uint32_t mpB = lds32(ch + Gm::OFF_KM + 2 * (16 * j + 2 * tl + 8));
-        const float sA0 = h2f_lo(spA), sA1 = h2f_hi(spA), sB0 = h2f_lo(spB), sB1 = h2f_hi(spB);
-        const float mA0 = h2f_lo(mpA), mA1 = h2f_hi(mpA), mB0 = h2f_lo(mpB), mB1 = h2f_hi(mpB);
+        const uint4 TA = lds128(tbl + (j * 4 + tl) * 32);
+        const uint4 TB = lds128(tbl + (j * 4 + tl) * 32 + 16);
 #pragma unroll
         for (int mt = 0; mt < NMT; ++mt) {
-          const uint32_t f = word_of(kcw[mt], j >> 1) >> (16 * (j & 1));
-          const uint32_t a0 = dq_pair(f, 0, 4, sA0, mA0, sA1, mA1);
-          const uint32_t a1 = dq_pair(f, 8, 12, sA0, mA0, sA1, mA1);
-          const uint32_t a2 = dq_pair(f, 2, 6, sB0, mB0, sB1, mB1);
-          const uint32_t a3 = dq_pair(f, 10, 14, sB0, mB0, sB1, mB1);
+          const uint32_t wd = word_of(mt == 0 ? kcw0 : kcw1, j >> 1);
+          const uint32_t f = (j & 1) ? (wd >> 16) : wd;
+          uint32_t a0, a1, a2, a3;
+          lut_k_regs(f, TA, TB, a0, a1, a2, a3);
           mma_bf16(s[mt], a0, a1, a2, a3, qb[j][0], qb[j][1]);
         }
       }
@@ -393,31 +494,43 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
 #pragma unroll
         for (int k = 0; k < 4; ++k) s[mt][k] *= io.scale_log2;
       }
+      const float mold0 = m_run[0], mold1 = m_run[1];
       online_step<NMT>(s, valid, m_run, l_run, o, tsum, mnew);
-      uint32_t pb[NMT][2];
-      p_to_b<NMT>(s, pb);
+      macc[0] *= exp2f(mold0 - m_run[0]);
+      macc[1] *= exp2f(mold1 - m_run[1]);
+      // values: o += sum_tok (p * s_tok) * code + (sum_tok p * m_tok) in every dim
+      uint32_t pbh[NMT][2];
+      float pm0 = 0.f, pm1 = 0.f;
+      const __half *vsp = reinterpret_cast<const __half *>(ch + Gm::OFF_VS);
+      const __half *vmp = reinterpret_cast<const __half *>(ch + Gm::OFF_VM);
 #pragma unroll
       for (int kk = 0; kk < NMT; ++kk) {
-        const int t0 = 16 * kk + 2 * tl;
-        const uint32_t spA = lds32(ch + Gm::OFF_VS + 2 * t0), spB = lds32(ch + Gm::OFF_VS + 2 * (t0 + 8));
-        const uint32_t mpA = lds32(ch + Gm::OFF_VM + 2 * t0), mpB = lds32(ch + Gm::OFF_VM + 2 * (t0 + 8));
-        const float sA0 = h2f_lo(spA), sA1 = h2f_hi(spA), sB0 = h2f_lo(spB), sB1 = h2f_hi(spB);
-        const float mA0 = h2f_lo(mpA), mA1 = h2f_hi(mpA), mB0 = h2f_lo(mpB), mB1 = h2f_hi(mpB);
+        const int t0 = 16 * kk + gl, t1 = t0 + 8;
+        const float s0v = __half2float(vsp[t0]), s1v = __half2float(vsp[t1]);
+        const float m0v = __half2float(vmp[t0]), m1v = __half2float(vmp[t1]);
+        pm0 = fmaf(s[kk][0], m0v, fmaf(s[kk][2], m1v, pm0));
+        pm1 = fmaf(s[kk][1], m0v, fmaf(s[kk][3], m1v, pm1));
+        pbh[kk][0] = movmatrix_trans(pack_half(s[kk][0] * s0v, s[kk][1] * s0v));
+        pbh[kk][1] = movmatrix_trans(pack_half(s[kk][2] * s1v, s[kk][3] * s1v));
+      }
+      macc[0] += warp_sum_xor_g(pm0);
+      macc[1] += warp_sum_xor_g(pm1);
+      const uint4 vw0 = lds128(ch + Gm::OFF_VCODE + lane * 16), vw1 = lds128(ch + Gm::OFF_VCODE + 512 + lane * 16);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t f = word_of(vcw[kk], i >> 1) >> (16 * (i & 1));
-          const uint32_t a0 = dq_pair(f, 0, 4, sA0, mA0, sA1, mA1);
-          const uint32_t a1 = dq_pair(f, 8, 12, sA0, mA0, sA1, mA1);
-          const uint32_t a2 = dq_pair(f, 2, 6, sB0, mB0, sB1, mB1);
-          const uint32_t a3 = dq_pair(f, 10, 14, sB0, mB0, sB1, mB1);
-          mma_bf16(o[i], a0, a1, a2, a3, pb[kk][0], pb[kk][1]);
+      for (int kk = 0; kk < NMT; ++kk) {
+#pragma unroll
+        for (int ip = 0; ip < 4; ++ip) {
+          const uint32_t w = word_of(kk == 0 ? vw0 : vw1, ip);
+          const uint32_t w10 = w >> 10;
+          mma_f16(o[2 * ip], dq_v(w, 0), dq_v(w, 1), dq_v(w, 2), dq_v(w, 3), pbh[kk][0], pbh[kk][1]);
+          mma_f16(o[2 * ip + 1], dq_v(w, 4), dq_v(w10, 0), dq_v(w10, 1), dq_v(w10, 2), pbh[kk][0], pbh[kk][1]);
         }
       }
       __syncwarp();
       consumed += 1;
       issue();
     }
-    // log2-sum-exp of this window's logits per head: the mass is 2^(mu - M) / L after the merge
+    // log2-sum-exp of this window's logits per head: its mass is 2^(mu - M) / L after the merge
     if (gl == 0) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -425,6 +538,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
         if (head < G) mu[(size_t)it * 8 + head] = tsum[h] > 0.f ? mnew[h] + __log2f(tsum[h]) : -INFINITY;
       }
     }
+    ++c_idx;
   }
   // drain: never leave a bulk copy in flight into shared memory
   while (consumed < issued) {
@@ -447,10 +561,10 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     float *w0 = cO + (warp * 8 + 2 * tl) * D, *w1 = w0 + D;
-    w0[16 * i + gl] = o[i][0];
-    w1[16 * i + gl] = o[i][1];
-    w0[16 * i + gl + 8] = o[i][2];
-    w1[16 * i + gl + 8] = o[i][3];
+    w0[16 * i + gl] = o[i][0] + macc[0];
+    w1[16 * i + gl] = o[i][1] + macc[1];
+    w0[16 * i + gl + 8] = o[i][2] + macc[0];
+    w1[16 * i + gl + 8] = o[i][3] + macc[1];
   }
   __syncthreads();
   float *mypart = part + (size_t)split * PART_FLOATS;
@@ -519,12 +633,12 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   }
   // window scores: S_g[w] += (1/H_q) * sum_{h in group} 2^(mu - M_h) / L_h
   float *score = C.at<float>(C.off_score, C.st_score, unit) + (size_t)g * C.n_windows;
-  const int total = I.total();
+  const int total = 1 + nL + nF + nQ;
   for (int it = 1 + threadIdx.x; it < total; it += blockDim.x) {
     int w;
-    if (it <= I.nL) w = I.j0 + it - 1;
-    else if (it <= I.nL + I.nF) w = ftab[it - 1 - I.nL].x;
-    else w = qtab[it - 1 - I.nL - I.nF].x;
+    if (it <= nL) w = j0 + it - 1;
+    else if (it <= nL + nF) w = ftab[it - 1 - nL].x;
+    else w = qtab[it - 1 - nL - nF].x;
     float mass = 0.f;
     for (int h = 0; h < G; ++h) mass += exp2f(__ldcg(mu + (size_t)it * 8 + h) - Mh[h]) / Lh[h];
     score[w] += mass * io.inv_hq;

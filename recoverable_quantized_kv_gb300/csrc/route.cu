@@ -315,22 +315,6 @@ __global__ void __launch_bounds__(RT_THREADS, 1) route_kernel(const CacheDev C, 
 
 // ----------------------------------------------------------------------------- quantise once
 
-// Element of code field (grp, lane, e) of a K (is_v = false) or V block -> (tok, dim).
-__device__ __forceinline__ void code_elem(bool is_v, int grp, int lane, int e, int &tok, int &dim) {
-  const int reg = e >> 1, half = e & 1;
-  const int r = (lane >> 2) + 8 * (reg & 1);
-  const int c = 2 * (lane & 3) + half + 8 * (reg >> 1);
-  if (!is_v) {
-    tok = 16 * (grp >> 3) + r;
-    dim = 16 * (grp & 7) + c;
-  } else {
-    tok = 16 * (grp >> 3) + c;
-    dim = 16 * (grp & 7) + r;
-  }
-}
-
-__device__ __forceinline__ int int2_bit(int e) { return e < 4 ? 4 * e : 4 * (e - 4) + 2; }
-
 template <int W>
 __device__ void load_window(const CacheDev &C, const PromptIO &pio, int unit, int b, int g, int kind, int src,
                             float (*xk)[D + 1], float (*xv)[D + 1]) {
@@ -376,6 +360,7 @@ __global__ void __launch_bounds__(MIG_THREADS) quant_kernel(const CacheDev C, co
   using Gm = Geo<W, 2>;
   __shared__ float xk[W][D + 1], xv[W][D + 1];
   __shared__ unsigned char ck[W][D], cv[W][D];
+  __shared__ uint32_t cw[2 * Gm::CODE_BYTES / 4];
   const int unit = unit0 + blockIdx.y;
   const int b = unit % C.B;
   const int *meta = C.at<const int>(C.off_meta, C.st_meta, unit);
@@ -427,28 +412,20 @@ __global__ void __launch_bounds__(MIG_THREADS) quant_kernel(const CacheDev C, co
       for (int d = lane; d < D; d += 32) cv[t][d] = (unsigned char)quant_code(xv[t][d], s, m);
     }
     __syncthreads();
-    // pack the fragment-native code fields (two 16-bit fields per 32-bit word)
-    for (int wi = tid; wi < 2 * Gm::CODE_BYTES / 4; wi += blockDim.x) {
-      const bool is_v = wi >= Gm::CODE_BYTES / 4;
-      const int o = (wi * 4) % Gm::CODE_BYTES;
-      const int chunk = o / 512, ln = (o % 512) / 16;
-      const int lb = chunk * 16 + (o % 16);
-      uint32_t word = 0;
-#pragma unroll
-      for (int fh = 0; fh < 2; ++fh) {
-        const int grp = lb / 2 + fh;
-        uint32_t field = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          int tok, dim;
-          code_elem(is_v, grp, ln, e, tok, dim);
-          const uint32_t c = is_v ? cv[tok][dim] : ck[tok][dim];
-          field |= c << int2_bit(e);
-        }
-        word |= field << (16 * fh);
-      }
-      reinterpret_cast<uint32_t *>(blk + (is_v ? Gm::OFF_VCODE : 0))[o / 4] = word;
+    // scatter the codes into their fragment-native positions (shared-memory words, then copy out)
+    for (int i = tid; i < 2 * Gm::CODE_BYTES / 4; i += blockDim.x) cw[i] = 0u;
+    __syncthreads();
+    for (int idx = tid; idx < 2 * W * D; idx += blockDim.x) {
+      const bool is_v = idx >= W * D;
+      const int e = is_v ? idx - W * D : idx, tok = e / D, dim = e % D;
+      int byte, shift;
+      code_pos2(is_v, tok, dim, byte, shift);
+      const unsigned c = is_v ? cv[tok][dim] : ck[tok][dim];
+      const int gb = byte + (is_v ? Gm::CODE_BYTES : 0);
+      atomicOr(&cw[gb >> 2], c << (8 * (gb & 3) + shift));
     }
+    __syncthreads();
+    for (int i = tid; i < 2 * Gm::CODE_BYTES / 4; i += blockDim.x) reinterpret_cast<uint32_t *>(blk)[i] = cw[i];
   }
 }
 
@@ -484,25 +461,17 @@ __global__ void __launch_bounds__(MIG_THREADS) move_kernel(const CacheDev C, con
       const __half *km = reinterpret_cast<const __half *>(led + Gm::OFF_KM);
       const __half *vsp = reinterpret_cast<const __half *>(led + Gm::OFF_VS);
       const __half *vmp = reinterpret_cast<const __half *>(led + Gm::OFF_VM);
-      for (int wi = tid; wi < 2 * Gm::BLK / 2; wi += blockDim.x) {   // output 32-bit words of K then V
-        const bool is_v = wi >= Gm::BLK / 2;
-        const int e2 = (wi % (Gm::BLK / 2)) * 2;                      // element index in the FN block
-        const int grp = e2 >> 8, ln = (e2 >> 3) & 31, reg = (e2 & 7) >> 1;
-        const int lb = grp * 2;                                       // INT2: 2 bytes per field
-        const int off = (lb >> 4) * 512 + ln * 16 + (lb & 15);
-        const uint32_t field = led[(is_v ? Gm::OFF_VCODE : 0) + off] | (led[(is_v ? Gm::OFF_VCODE : 0) + off + 1] << 8);
-        float x[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int e = reg * 2 + h;
-          int tok, dim;
-          code_elem(is_v, grp, ln, e, tok, dim);
-          const float c = (float)((field >> int2_bit(e)) & 3u);
-          const float s = __half2float(is_v ? vsp[tok] : ks[dim]);
-          const float m = __half2float(is_v ? vmp[tok] : km[dim]);
-          x[h] = __fmaf_rn(c, s, m);
-        }
-        reinterpret_cast<uint32_t *>(is_v ? dv : dk)[wi % (Gm::BLK / 2)] = pack_bf16(x[0], x[1]);
+      for (int idx = tid; idx < 2 * W * D; idx += blockDim.x) {
+        const bool is_v = idx >= W * D;
+        const int e = is_v ? idx - W * D : idx, tok = e / D, dim = e % D;
+        int byte, shift;
+        code_pos2(is_v, tok, dim, byte, shift);
+        const float c = (float)((led[byte + (is_v ? Gm::OFF_VCODE : 0)] >> shift) & 3u);
+        const float s = __half2float(is_v ? vsp[tok] : ks[dim]);
+        const float m = __half2float(is_v ? vmp[tok] : km[dim]);
+        const __nv_bfloat16 x = __float2bfloat16_rn(__fmaf_rn(c, s, m));
+        if (is_v) dv[fnv_index(tok, dim)] = x;
+        else dk[fnk_index(tok, dim)] = x;
       }
     } else if (src_kind == SRC_RING) {
       const int rs = tk.z % C.ring_windows;

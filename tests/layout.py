@@ -30,14 +30,24 @@ def fn_index(W, is_v):
 
 
 def code_position(W, bits, is_v):
-    """(byte offset, bit shift) of every (tok, dim) code inside a K or V code block."""
+    """(byte offset, bit shift) of every (tok, dim) INT2 code inside a K or V code block."""
+    assert bits == 2
     tok, dim = _maps(W)
-    r, c = (dim % 16, tok % 16) if is_v else (tok % 16, dim % 16)
-    lane, reg = _frag(r, c)
-    grp = (tok // 16) * 8 + dim // 16
-    e = reg * 2 + c % 2
-    bit = np.where(e < 4, 4 * e, 4 * (e - 4) + 2) if bits == 2 else 4 * e
-    lb = grp * bits + bit // 8
+    if not is_v:
+        r, c = tok % 16, dim % 16
+        lane, reg = _frag(r, c)
+        grp = (tok // 16) * 8 + dim // 16
+        e = reg * 2 + c % 2
+        bit = np.where(e < 4, 4 * e, 4 * (e - 4) + 2)
+        lb = grp * 2 + bit // 8
+    else:
+        r, c = dim % 16, tok % 16
+        lane, reg = _frag(r, c)
+        i = dim // 16
+        rr = (i % 2) * 4 + reg
+        w = (tok // 16) * 4 + i // 2
+        bit = np.where(rr < 5, 2 * rr, 10 + 2 * (rr - 5)) + 16 * (c % 2)
+        lb = 4 * w + bit // 8
     byte = (lb // 16) * 512 + lane * 16 + lb % 16
     return byte.reshape(W, D), (bit % 8).reshape(W, D)
 
