@@ -34,6 +34,7 @@ struct qevict_cache {
   std::vector<int> t_host;      // tokens cached per layer (host mirror)
   std::vector<int> prefilled;
   int routes_done;
+  int last_decode_layer;        // layer of the last decode enqueued, -1 after any other call
 };
 
 namespace {
@@ -228,6 +229,7 @@ qevict_status qevict_init_cache(const qevict_config *cfg, void *d_arena, size_t 
   c->t_host.assign(cfg->n_layers, 0);
   c->prefilled.assign(cfg->n_layers, 0);
   c->routes_done = 0;
+  c->last_decode_layer = -1;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(d_arena, 0, (size_t)p.lay.arena_bytes, s);
   if (e == cudaSuccess) e = qv::launch_init(c->dev, s);
@@ -272,6 +274,7 @@ qevict_status qevict_prefill_route(qevict_cache *cache, int32_t layer, const voi
   if (e != cudaSuccess) return QEVICT_ECUDA;
   cache->prefilled[layer] = 1;
   cache->t_host[layer] = cache->cfg.prompt_len;
+  cache->last_decode_layer = -1;
   return QEVICT_OK;
 }
 
@@ -291,8 +294,10 @@ qevict_status qevict_decode_step(qevict_cache *cache, int32_t layer, const void 
   io.layer = layer;
   io.scale_log2 = 1.4426950408889634f / std::sqrt((float)D);
   io.inv_hq = 1.0f / (float)cache->cfg.h_q;
+  io.wait_first = (cache->last_decode_layer == layer) ? 1 : 0;
   cudaError_t e = qv::launch_decode(cache->dev, io, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return QEVICT_ECUDA;
+  cache->last_decode_layer = layer;
   cache->t_host[layer] = T + 1;
   return QEVICT_OK;
 }
@@ -306,6 +311,7 @@ qevict_status qevict_route(qevict_cache *cache, qevict_stream_t stream) {
                                    reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return QEVICT_ECUDA;
   cache->routes_done += 1;
+  cache->last_decode_layer = -1;
   return QEVICT_OK;
 }
 

@@ -53,6 +53,7 @@ struct DecodeIO {
   int layer;
   float scale_log2;             // log2(e) / sqrt(D)
   float inv_hq;                 // 1 / h_q
+  int wait_first;               // 1: the previous kernel in the stream may be this layer's decode
 };
 
 }  // namespace qv

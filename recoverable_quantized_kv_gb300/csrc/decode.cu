@@ -20,8 +20,10 @@ constexpr int DEC_WARPS = 16;
 constexpr int DEC_STAGES = 3;
 constexpr int DEC_STAGE_BYTES = 4096;
 constexpr int DEC_TBL_BYTES = 1024;   // per-warp key lookup tables: 8 k-steps x 4 lane classes x 32 B
-constexpr int DEC_SMEM = DEC_WARPS * (DEC_STAGES * DEC_STAGE_BYTES + DEC_TBL_BYTES) + DEC_WARPS * DEC_STAGES * 8 +
-                         DEC_WARPS * 8 * 4;
+constexpr int DEC_SLICE_CAP = 2048;   // table entries of one CTA's slices kept in shared memory
+constexpr int DEC_SLICE_OFF = DEC_WARPS * (DEC_STAGES * DEC_STAGE_BYTES + DEC_TBL_BYTES) + DEC_WARPS * DEC_STAGES * 8 +
+                              DEC_WARPS * 8 * 4;
+constexpr int DEC_SMEM = DEC_SLICE_OFF + DEC_SLICE_CAP * 8;
 
 // Work list of one (sequence, KV head): item 0 = the sink tokens, items 1..nL = recent windows
 // j0 .. j0+nL-1, then the F-table entries, then the Q-table entries.  Item costs are the bytes
@@ -177,6 +179,13 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int unit = io.layer * C.B + b;
   const int G = C.G;
+  // Programmatic dependent launch.  This kernel may start while the previous kernel in the stream
+  // (the decode of another layer) finishes; that kernel writes only its own layer's state, and every
+  // kernel before it has completed (each decode kernel lets its successor start only after its own
+  // wait below).  So this layer's tables and windows can be read and prefetched right away, and
+  // only the step's inputs (q, k_new, v_new) wait.  When the previous decode was the same layer,
+  // wait first.
+  if (io.wait_first) asm volatile("griddepcontrol.wait;" ::: "memory");
   int *status = C.status();
   int *meta = C.at<int>(C.off_meta, C.st_meta, unit);
   const int T = meta[M_T], n_route = meta[M_NROUTE], nF = meta[M_FCOUNT], nQ = meta[M_QCOUNT];
@@ -221,23 +230,26 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
                                        DEC_WARPS * DEC_STAGES * 8) + warp * 8;
   __shared__ int q_next;
   if (threadIdx.x == 0) q_next = 0;
+  // this CTA's table slices, staged once in shared memory (one coalesced round trip)
+  int2 *sft = reinterpret_cast<int2 *>(smem + DEC_SLICE_OFF);
+  int2 *sqt = sft + (F1 - F0);
+  const bool slices_in_smem = (F1 - F0) + (Q1 - Q0) <= DEC_SLICE_CAP;
+  if (slices_in_smem) {
+    for (int i = threadIdx.x; i < F1 - F0; i += blockDim.x) sft[i] = ftab[F0 + i];
+    for (int i = threadIdx.x; i < Q1 - Q0; i += blockDim.x) sqt[i] = qtab[Q0 + i];
+  }
+  auto f_entry = [&](int idx) -> int2 {
+    return (slices_in_smem && idx >= F0 && idx < F1) ? sft[idx - F0] : ftab[idx];
+  };
+  auto q_entry = [&](int idx) -> int2 {
+    return (slices_in_smem && idx >= Q0 && idx < Q1) ? sqt[idx - Q0] : qtab[idx];
+  };
   if (lane == 0) {
 #pragma unroll
     for (int st = 0; st < DEC_STAGES; ++st) mbar_init(&bars[st], 1);
     fence_mbar_init();
   }
   __syncthreads();
-
-  // q as the B operand of S^T = K q^T: b0 = q[head gl][16j+2tl .. +1], b1 = the same at +8.
-  uint32_t qb[8][2];
-  {
-    const __nv_bfloat16 *qh = io.q + ((size_t)b * C.h_q + (size_t)g * G + gl) * D;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      qb[j][0] = gl < G ? ldg32(qh + 16 * j + 2 * tl) : 0u;
-      qb[j][1] = gl < G ? ldg32(qh + 16 * j + 2 * tl + 8) : 0u;
-    }
-  }
 
   float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f}, macc[2] = {0.f, 0.f};
   float o[8][4];
@@ -254,11 +266,11 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
       src = sub < NMT ? (const void *)(kb + sub * 2048) : (const void *)(vb + (sub - NMT) * 2048);
       bytes = DEC_STAGE_BYTES;
     } else if (it <= nL + nF) {
-      const int slot = __ldg(&ftab[it - 1 - nL].y);
+      const int slot = f_entry(it - 1 - nL).y;
       src = fpool + ((size_t)slot * C.h_kv + g) * 2 * Gm::BLK * 2 + (size_t)sub * DEC_STAGE_BYTES;
       bytes = DEC_STAGE_BYTES;
     } else {
-      const int slot = __ldg(&qtab[it - 1 - nL - nF].y);
+      const int slot = q_entry(it - 1 - nL - nF).y;
       src = ledger + ((size_t)slot * C.h_kv + g) * Gm::QB;
       bytes = Gm::QB;
     }
@@ -315,6 +327,20 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   };
 
   issue();
+  // the step's inputs come from the previous kernel in a model: wait for it, then let the next start
+  if (!io.wait_first) asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // q as the B operand of S^T = K q^T: b0 = q[head gl][16j+2tl .. +1], b1 = the same at +8
+  // (loaded while the first bulk copies are in flight)
+  uint32_t qb[8][2];
+  {
+    const __nv_bfloat16 *qh = io.q + ((size_t)b * C.h_q + (size_t)g * G + gl) * D;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      qb[j][0] = gl < G ? ldg32(qh + 16 * j + 2 * tl) : 0u;
+      qb[j][1] = gl < G ? ldg32(qh + 16 * j + 2 * tl + 8) : 0u;
+    }
+  }
   while (ok) {
     if (c_idx == ngrab) {
       issue();
@@ -371,7 +397,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
     if (it <= nL + nF) {
       // ---------------- bf16 window (recent or Full)
       const bool is_local = it <= nL;
-      const int wid = is_local ? j0 + it - 1 : __ldg(&ftab[it - 1 - nL].x);
+      const int wid = is_local ? j0 + it - 1 : f_entry(it - 1 - nL).x;
       const int newtok = (is_local && wid == jn) ? T - (C.n_sink + jn * W) : -1;
       const uint8_t *kc[NMT];
 #pragma unroll
@@ -548,9 +574,11 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
 
   // ---------------- merge the warps of this CTA into one split partial
   __syncthreads();
-  float *cm = reinterpret_cast<float *>(smem);            // [warp][8]
-  float *cl = cm + DEC_WARPS * 8;                           // [warp][8]
-  float *cO = cl + DEC_WARPS * 8;                           // [warp][8][D]
+  float *cm = reinterpret_cast<float *>(smem);            // [warp][8] running max
+  float *cl = cm + DEC_WARPS * 8;                           // [warp][8] running sum
+  float *cf = cl + DEC_WARPS * 8;                           // [warp][8] rescale factor
+  float *sM = cf + DEC_WARPS * 8;                           // [8] CTA max per head
+  float *cO = sM + 16;                                      // [warp][8][D]
   if (gl == 0) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -567,88 +595,115 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
     w1[16 * i + gl + 8] = o[i][3] + macc[1];
   }
   __syncthreads();
+  if (threadIdx.x < 8) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < DEC_WARPS; ++w) M = fmaxf(M, cm[w * 8 + threadIdx.x]);
+    sM[threadIdx.x] = M;
+  }
+  __syncthreads();
+  if (threadIdx.x < DEC_WARPS * 8) {
+    const float M = sM[threadIdx.x & 7];
+    cf[threadIdx.x] = M == -INFINITY ? 0.f : exp2f(cm[threadIdx.x] - M);
+  }
+  __syncthreads();
   float *mypart = part + (size_t)split * PART_FLOATS;
   for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
     const int h = idx / D, d = idx % D;
-    float M = -INFINITY;
-    for (int w = 0; w < DEC_WARPS; ++w) M = fmaxf(M, cm[w * 8 + h]);
-    float acc = 0.f, l = 0.f;
-    if (M != -INFINITY) {
-      for (int w = 0; w < DEC_WARPS; ++w) {
-        const float f = exp2f(cm[w * 8 + h] - M);
-        acc += cO[(w * 8 + h) * D + d] * f;
-        l += cl[w * 8 + h] * f;
-      }
-    }
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < DEC_WARPS; ++w) acc = fmaf(cO[(w * 8 + h) * D + d], cf[w * 8 + h], acc);
     mypart[16 + h * D + d] = acc;
-    if (d == 0) {
-      mypart[h] = M;
-      mypart[8 + h] = l;
-    }
+  }
+  if (threadIdx.x < G) {
+    float l = 0.f;
+#pragma unroll
+    for (int w = 0; w < DEC_WARPS; ++w) l = fmaf(cl[w * 8 + threadIdx.x], cf[w * 8 + threadIdx.x], l);
+    mypart[threadIdx.x] = sM[threadIdx.x];
+    mypart[8 + threadIdx.x] = l;
   }
 
   // ---------------- the last CTA of this (sequence, KV head) merges the splits
   __shared__ int s_last;
-  __threadfence();
-  __syncthreads();
+  __syncthreads();   // every partial write of this CTA happens before thread 0's release below
   unsigned *splitctr = reinterpret_cast<unsigned *>(C.arena + C.off_splitctr) + ((size_t)io.layer * C.B + b) * C.h_kv + g;
-  if (threadIdx.x == 0) s_last = (atomicAdd(splitctr, 1u) == (unsigned)(C.n_split - 1));
+  if (threadIdx.x == 0) {
+    unsigned prev;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(prev) : "l"(splitctr) : "memory");
+    s_last = prev == (unsigned)(C.n_split - 1);
+  }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
 
-  float *Mh = cm, *Lh = cm + 8;
-  if (warp < G) {
-    const int h = warp;
+  const int nsp = C.n_split;
+  float *sml = cO;                         // [nsp][16]: m[8], l[8] of every split
+  float *sf = sml + nsp * 16;              // [nsp][8]: 2^(m - M) / L
+  float *Mh = sM, *iL = sM + 8;
+  for (int i = threadIdx.x; i < nsp * 16; i += blockDim.x) sml[i] = __ldcg(part + (size_t)(i >> 4) * PART_FLOATS + (i & 15));
+  __syncthreads();
+  if (threadIdx.x < G) {
+    const int h = threadIdx.x;
     float M = -INFINITY;
-    for (int s = lane; s < C.n_split; s += 32) {
-      const float *ps = part + (size_t)s * PART_FLOATS;
-      if (__ldcg(ps + 8 + h) > 0.f) M = fmaxf(M, __ldcg(ps + h));
-    }
-#pragma unroll
-    for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    for (int sp = 0; sp < nsp; ++sp)
+      if (sml[sp * 16 + 8 + h] > 0.f) M = fmaxf(M, sml[sp * 16 + h]);
     float L = 0.f;
-    for (int s = lane; s < C.n_split; s += 32) {
-      const float *ps = part + (size_t)s * PART_FLOATS;
-      const float l = __ldcg(ps + 8 + h);
-      if (l > 0.f) L += l * exp2f(__ldcg(ps + h) - M);
+    for (int sp = 0; sp < nsp; ++sp) {
+      const float l = sml[sp * 16 + 8 + h];
+      if (l > 0.f) L = fmaf(l, exp2f(sml[sp * 16 + h] - M), L);
     }
-#pragma unroll
-    for (int off = 16; off; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-    if (lane == 0) {
-      Mh[h] = M;
-      Lh[h] = L;
-    }
+    Mh[h] = M;
+    iL[h] = 1.f / L;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < nsp * 8; i += blockDim.x) {
+    const int sp = i >> 3, h = i & 7;
+    const float l = sml[sp * 16 + 8 + h];
+    sf[i] = (h < G && l > 0.f) ? exp2f(sml[sp * 16 + h] - Mh[h]) * iL[h] : 0.f;
   }
   __syncthreads();
   for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
     const int h = idx / D, d = idx % D;
-    float acc = 0.f;
-    for (int s = 0; s < C.n_split; ++s) {
-      const float *ps = part + (size_t)s * PART_FLOATS;
-      const float l = __ldcg(ps + 8 + h);
-      if (l > 0.f) acc += __ldcg(ps + 16 + h * D + d) * exp2f(__ldcg(ps + h) - Mh[h]);
+    const float *po = part + 16 + h * D + d;
+    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+    int sp = 0;
+    for (; sp + 4 <= nsp; sp += 4) {
+      const float o0 = __ldcg(po + (size_t)sp * PART_FLOATS), o1 = __ldcg(po + (size_t)(sp + 1) * PART_FLOATS);
+      const float o2 = __ldcg(po + (size_t)(sp + 2) * PART_FLOATS), o3 = __ldcg(po + (size_t)(sp + 3) * PART_FLOATS);
+      acc0 = fmaf(o0, sf[sp * 8 + h], acc0);
+      acc1 = fmaf(o1, sf[(sp + 1) * 8 + h], acc1);
+      acc2 = fmaf(o2, sf[(sp + 2) * 8 + h], acc2);
+      acc3 = fmaf(o3, sf[(sp + 3) * 8 + h], acc3);
     }
-    io.out[((size_t)b * C.h_q + (size_t)g * G + h) * D + d] = __float2bfloat16_rn(acc / Lh[h]);
+    for (; sp < nsp; ++sp) acc0 = fmaf(__ldcg(po + (size_t)sp * PART_FLOATS), sf[sp * 8 + h], acc0);
+    io.out[((size_t)b * C.h_q + (size_t)g * G + h) * D + d] = __float2bfloat16_rn((acc0 + acc1) + (acc2 + acc3));
   }
-  // window scores: S_g[w] += (1/H_q) * sum_{h in group} 2^(mu - M_h) / L_h
+  // window scores: S_g[w] += (1/H_q) * sum_{h in group} 2^(mu - M_h) / L_h; two items per thread in flight
   float *score = C.at<float>(C.off_score, C.st_score, unit) + (size_t)g * C.n_windows;
   const int total = 1 + nL + nF + nQ;
-  for (int it = 1 + threadIdx.x; it < total; it += blockDim.x) {
-    int w;
-    if (it <= nL) w = j0 + it - 1;
-    else if (it <= nL + nF) w = ftab[it - 1 - nL].x;
-    else w = qtab[it - 1 - nL - nF].x;
-    float mass = 0.f;
-    for (int h = 0; h < G; ++h) mass += exp2f(__ldcg(mu + (size_t)it * 8 + h) - Mh[h]) / Lh[h];
-    score[w] += mass * io.inv_hq;
+  auto wid_of = [&](int it) -> int {
+    return it <= nL ? j0 + it - 1 : (it <= nL + nF ? __ldg(&ftab[it - 1 - nL].x) : __ldg(&qtab[it - 1 - nL - nF].x));
+  };
+  auto mass_of = [&](int it) -> float {
+    float m = 0.f;
+    for (int h = 0; h < G; ++h) m = fmaf(exp2f(__ldcg(mu + (size_t)it * 8 + h) - Mh[h]), iL[h], m);
+    return m * io.inv_hq;
+  };
+  for (int it = 1 + threadIdx.x; it < total; it += 2 * blockDim.x) {
+    const int it2 = it + blockDim.x;
+    const bool two = it2 < total;
+    const int w1 = wid_of(it), w2 = two ? wid_of(it2) : w1;
+    const float a1 = mass_of(it), a2 = two ? mass_of(it2) : 0.f;
+    const float s1 = score[w1], s2 = two ? score[w2] : 0.f;
+    score[w1] = s1 + a1;
+    if (two) score[w2] = s2 + a2;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     *splitctr = 0u;
-    __threadfence();
     unsigned *headctr = reinterpret_cast<unsigned *>(C.arena + C.off_headctr) + (size_t)io.layer * C.B + b;
-    if (atomicAdd(headctr, 1u) == (unsigned)(C.h_kv - 1)) {
+    unsigned prev;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(prev) : "l"(headctr) : "memory");
+    if (prev == (unsigned)(C.h_kv - 1)) {
       *headctr = 0u;
       meta[M_T] = T + 1;     // every CTA of this unit has read T by now
     }
@@ -666,9 +721,17 @@ cudaError_t launch_decode(const CacheDev &C, const DecodeIO &io, cudaStream_t st
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(C.n_split, C.h_kv, C.B);
-  kern<<<grid, DEC_WARPS * 32, DEC_SMEM, stream>>>(C, io);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C.n_split, C.h_kv, C.B);
+  cfg.blockDim = dim3(DEC_WARPS * 32);
+  cfg.dynamicSmemBytes = DEC_SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, C, io);
 }
 
 }  // namespace qv
