@@ -188,6 +188,27 @@ qevict_status qevict_read_counters(qevict_cache *cache, int64_t *host7, qevict_s
  * CUDA graphs of decode steps) and returns QEVICT_EDEVICE if the device status word is set. */
 qevict_status qevict_check(qevict_cache *cache, qevict_stream_t stream);
 
+/* Scratch size, in floats, of qevict_prefill_scores_noalloc: 2 * batch * h_q * prompt_len must not
+ * exceed it (2 Mi floats = 8 MiB, e.g. 32 query heads x 32768 prompt tokens for one sequence). */
+#define QEVICT_NOALLOC_SCRATCH_FLOATS (2LL * 1024 * 1024)
+
+/* Prefill scores without any device allocation (the paper has no counterpart; this is an
+ * interface for callers).  Computes exactly what qevict_prefill_scores computes, but takes plain
+ * sizes instead of a cache, for callers that cannot allocate device memory at all: code inside a
+ * framework that owns every byte of device memory through its own pool, or plugins handed only their
+ * input and output buffers.  Its scratch is a fixed 8 MiB array inside the library image, held on
+ * every GPU that loads the library until the process exits; nothing is allocated per call.
+ *   q_prompt [batch][prompt_len][h_q][128], k_prompt [batch][prompt_len][h_kv][128] bf16 (device);
+ *   s0_out [batch][ceil((prompt_len - n_sink) / window)] fp32 (device).
+ * Errors: QEVICT_EINVAL for bad sizes or NULL pointers; QEVICT_ENOMEM when
+ * 2 * batch * h_q * prompt_len > QEVICT_NOALLOC_SCRATCH_FLOATS (nothing is enqueued then).
+ * The first call on a device looks up the scratch address with that device current; make that first
+ * call before capturing a stream.  All calls share the scratch: calls that can overlap on the GPU
+ * (e.g. on two streams) race and must be ordered by the caller. */
+qevict_status qevict_prefill_scores_noalloc(int32_t batch, int32_t prompt_len, int32_t h_q, int32_t h_kv,
+                                            int32_t n_sink, int32_t window, const void *q_prompt,
+                                            const void *k_prompt, float *s0_out, qevict_stream_t stream);
+
 /* Frees the host handle (the arena stays the caller's). */
 qevict_status qevict_destroy(qevict_cache *cache);
 

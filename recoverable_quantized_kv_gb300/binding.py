@@ -68,6 +68,7 @@ def load() -> ctypes.CDLL:
         "qevict_read_counters": [P, ctypes.POINTER(I64), P],
         "qevict_check": [P, P],
         "qevict_destroy": [P],
+        "qevict_prefill_scores_noalloc": [I32, I32, I32, I32, I32, I32, P, P, P, P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -83,7 +84,8 @@ def exported_symbols():
     """Names of the C ABI entry points declared in include/qevict.h."""
     return ["qevict_budget", "qevict_cache_bytes", "qevict_init_cache", "qevict_get_layout",
             "qevict_prefill_scores", "qevict_prefill_route", "qevict_decode_step", "qevict_route",
-            "qevict_read_counters", "qevict_check", "qevict_destroy", "qevict_status_string"]
+            "qevict_read_counters", "qevict_check", "qevict_destroy", "qevict_status_string",
+            "qevict_prefill_scores_noalloc"]
 
 
 def _check(status: int, where: str):
@@ -118,6 +120,13 @@ def _stream(stream=None) -> int:
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
     return s.cuda_stream
+
+
+def prefill_scores_noalloc(batch, prompt_len, h_q, h_kv, n_sink, window, q_prompt, k_prompt, s0_out, stream=None):
+    """Prefill scores through the allocation-free entry point (scratch inside the library image)."""
+    _check(load().qevict_prefill_scores_noalloc(batch, prompt_len, h_q, h_kv, n_sink, window, _ptr(q_prompt),
+                                                _ptr(k_prompt), _ptr(s0_out), _stream(stream)),
+           "qevict_prefill_scores_noalloc")
 
 
 class Cache:

@@ -1,0 +1,77 @@
+// Prefill window scoring for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc at all: code that runs inside a framework owning every byte
+// of device memory through its own pool, plugins handed only their input and output buffers, or
+// code paths where an allocation would synchronise the device.  qevict_prefill_scores needs a
+// cache (and its arena) only for scratch space; this entry point takes plain sizes and the caller's
+// inputs and output, and keeps its scratch in a fixed array that is part of the library image.
+//
+// The scratch is a file-scope device array of QEVICT_NOALLOC_SCRATCH_FLOATS floats (8 MiB); every
+// GPU that loads the library holds it until the process exits.  Host code cannot use the array's
+// name as a device address, so the first call on each device looks the address up once, with that
+// device current, and later calls reuse it.  Every call shares the array: the two kernels overwrite
+// every element they later read, so nothing has to be cleared between calls, but calls that overlap
+// on the GPU (for example on two streams) race on the scratch and must be ordered by the caller.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "cache_dev.cuh"
+#include "common.cuh"
+#include "qevict.h"
+
+namespace qv {
+cudaError_t launch_prefill_scores(const CacheDev &C, const __nv_bfloat16 *q, const __nv_bfloat16 *k, float *s0,
+                                  cudaStream_t s);
+}
+
+namespace {
+
+constexpr long long kScratchFloats = QEVICT_NOALLOC_SCRATCH_FLOATS;
+static __device__ __align__(256) float g_noalloc_scratch[kScratchFloats];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+float *g_scratch_addr[kMaxDevices] = {};   // device address of g_noalloc_scratch, per device
+
+}  // namespace
+
+extern "C" qevict_status qevict_prefill_scores_noalloc(int32_t batch, int32_t prompt_len, int32_t h_q, int32_t h_kv,
+                                                       int32_t n_sink, int32_t window, const void *q_prompt,
+                                                       const void *k_prompt, float *s0_out, qevict_stream_t stream) {
+  if (!q_prompt || !k_prompt || !s0_out || batch < 1 || h_kv < 1 || h_q < h_kv || h_q % h_kv || window < 1 ||
+      n_sink < 0 || prompt_len <= n_sink)
+    return QEVICT_EINVAL;
+  const int G = h_q / h_kv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return QEVICT_EINVAL;
+  const long long per_array = (long long)batch * h_q * prompt_len;   // row statistics, then column sums
+  if (2 * per_array > kScratchFloats) return QEVICT_ENOMEM;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return QEVICT_ECUDA;
+  if (dev < 0 || dev >= kMaxDevices) return QEVICT_EINVAL;
+  float *scratch;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_scratch_addr[dev]) {
+      void *p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return QEVICT_ECUDA;
+      g_scratch_addr[dev] = static_cast<float *>(p);
+    }
+    scratch = g_scratch_addr[dev];
+  }
+  qv::CacheDev C = {};
+  C.arena = reinterpret_cast<uint8_t *>(scratch);
+  C.off_rowstat = 0;
+  C.off_colsum = per_array * (long long)sizeof(float);
+  C.B = batch;
+  C.h_q = h_q;
+  C.h_kv = h_kv;
+  C.G = G;
+  C.n_sink = n_sink;
+  C.W = window;
+  C.prompt_len = prompt_len;
+  const cudaError_t e = qv::launch_prefill_scores(C, static_cast<const __nv_bfloat16 *>(q_prompt),
+                                                  static_cast<const __nv_bfloat16 *>(k_prompt), s0_out,
+                                                  reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QEVICT_OK : QEVICT_ECUDA;
+}
