@@ -4,26 +4,36 @@
 // QEvict (arXiv 2608.05326) §4.1: o = softmax(q K_acc^T / sqrt(d)) V_acc over the accessible set;
 // §4.2 Eq. (1): the window score accumulates (1/H_q) sum_h sum_{i in w} a^h(i).
 //
-// Grid (n_split, h_kv, batch).  Each CTA owns a byte-balanced contiguous range of the work list of
-// one (sequence, KV head); each warp owns a sub-range and streams its windows through a private
-// 4-stage shared-memory ring filled by 1-D bulk copies (TMA) signalled on mbarriers.  The G query
-// heads of the KV head ride on the N side of mma.m16n8k16 (tokens on M for Q K^T, dims on M for
-// P V), so both products run on tensor cores.  Softmax is online per warp; per-window masses are
-// kept as log2-sum-exp values, which the last CTA of the (sequence, KV head) to finish (counted
-// with one atomic, no waiting) normalises into the window scores while it merges the splits.
+// Grid (n_split, h_kv, batch).  Each CTA owns a proportional slice of the recent, Full and
+// Quantized windows of one (sequence, KV head).  One producer warp streams the slice's windows
+// through a CTA-wide ring of 4 KB shared-memory slots with 1-D bulk copies (TMA), each completing on
+// an mbarrier; fifteen consumer warps take windows from a shared queue, wait for their chunks,
+// compute, and release the slots.  The G query heads of the KV head ride on the N side of
+// mma.m16n8k16 (tokens on M for Q K^T, dims on M for P V), so both products run on tensor cores.
+// Softmax is online per warp; per-window masses are kept as log2-sum-exp values, which the last CTA
+// of the (sequence, KV head) to finish (counted with one atomic, no waiting) normalises into the
+// window scores while it merges the splits.
 #include "cache_dev.cuh"
 #include "common.cuh"
 
 namespace qv {
 
-constexpr int DEC_WARPS = 16;
-constexpr int DEC_STAGES = 3;
+constexpr int DEC_WARPS = 16;          // 15 consumer warps + 1 producer warp
+constexpr int DEC_CONSUMERS = DEC_WARPS - 1;
+constexpr int DEC_SLOTS = 44;          // CTA-wide ring of 4 KB slots filled by bulk copies
 constexpr int DEC_STAGE_BYTES = 4096;
-constexpr int DEC_TBL_BYTES = 1024;   // per-warp key lookup tables: 8 k-steps x 4 lane classes x 32 B
-constexpr int DEC_SLICE_CAP = 2048;   // table entries of one CTA's slices kept in shared memory
-constexpr int DEC_SLICE_OFF = DEC_WARPS * (DEC_STAGES * DEC_STAGE_BYTES + DEC_TBL_BYTES) + DEC_WARPS * DEC_STAGES * 8 +
-                              DEC_WARPS * 8 * 4;
-constexpr int DEC_SMEM = DEC_SLICE_OFF + DEC_SLICE_CAP * 8;
+constexpr int DEC_MAX_CHUNKS = 4;      // chunks of one window (a bf16 window: 2 K + 2 V)
+// Consumers take windows from a queue, so a consumer can wait on a chunk up to
+// DEC_CONSUMERS * DEC_MAX_CHUNKS chunks past the first one not yet issued.  Giving every slot
+// DEC_PHASES "full" barriers used in turn keeps every parity wait unambiguous: the chunk
+// DEC_PHASES * DEC_SLOTS earlier on the same barrier has always landed by then.
+constexpr int DEC_PHASES = 3;
+static_assert((DEC_PHASES - 1) * DEC_SLOTS >= DEC_CONSUMERS * DEC_MAX_CHUNKS, "too few full barriers per slot");
+constexpr int DEC_FULL = DEC_PHASES * DEC_SLOTS;
+constexpr int DEC_TBL_BYTES = 1024;    // per consumer warp key lookup tables: 8 k-steps x 4 lane classes x 32 B
+constexpr int DEC_TBL_OFF = DEC_SLOTS * DEC_STAGE_BYTES;
+constexpr int DEC_BAR_OFF = DEC_TBL_OFF + DEC_CONSUMERS * DEC_TBL_BYTES;
+constexpr int DEC_SMEM = DEC_BAR_OFF + (DEC_FULL + DEC_SLOTS) * 8;
 
 // Work list of one (sequence, KV head): item 0 = the sink tokens, items 1..nL = recent windows
 // j0 .. j0+nL-1, then the F-table entries, then the Q-table entries.  Item costs are the bytes
@@ -222,43 +232,33 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
     return 1 + nL + nF + Q0 + k;
   };
 
-  uint8_t *stage = smem + warp * DEC_STAGES * DEC_STAGE_BYTES;
-  uint8_t *tbl = smem + DEC_WARPS * DEC_STAGES * DEC_STAGE_BYTES + warp * DEC_TBL_BYTES;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + DEC_WARPS * (DEC_STAGES * DEC_STAGE_BYTES + DEC_TBL_BYTES)) +
-                   warp * DEC_STAGES;
-  int *gring = reinterpret_cast<int *>(smem + DEC_WARPS * (DEC_STAGES * DEC_STAGE_BYTES + DEC_TBL_BYTES) +
-                                       DEC_WARPS * DEC_STAGES * 8) + warp * 8;
-  __shared__ int q_next;
-  if (threadIdx.x == 0) q_next = 0;
-  // this CTA's table slices, staged once in shared memory (one coalesced round trip)
-  int2 *sft = reinterpret_cast<int2 *>(smem + DEC_SLICE_OFF);
-  int2 *sqt = sft + (F1 - F0);
-  const bool slices_in_smem = (F1 - F0) + (Q1 - Q0) <= DEC_SLICE_CAP;
-  if (slices_in_smem) {
-    for (int i = threadIdx.x; i < F1 - F0; i += blockDim.x) sft[i] = ftab[F0 + i];
-    for (int i = threadIdx.x; i < Q1 - Q0; i += blockDim.x) sqt[i] = qtab[Q0 + i];
-  }
-  auto f_entry = [&](int idx) -> int2 {
-    return (slices_in_smem && idx >= F0 && idx < F1) ? sft[idx - F0] : ftab[idx];
-  };
-  auto q_entry = [&](int idx) -> int2 {
-    return (slices_in_smem && idx >= Q0 && idx < Q1) ? sqt[idx - Q0] : qtab[idx];
-  };
-  if (lane == 0) {
-#pragma unroll
-    for (int st = 0; st < DEC_STAGES; ++st) mbar_init(&bars[st], 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
+  uint8_t *slots = smem;
+  uint8_t *tbl = smem + DEC_TBL_OFF + (warp < DEC_CONSUMERS ? warp : 0) * DEC_TBL_BYTES;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + DEC_BAR_OFF);   // [DEC_FULL]
+  uint64_t *empty = full + DEC_FULL;                                    // [DEC_SLOTS]
+  __shared__ int q_next;    // next queue position to hand to a consumer warp
 
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f}, macc[2] = {0.f, 0.f};
-  float o[8][4];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-
-  // ---- chunk stream.  bf16 window: NMT K chunks then NMT V chunks (4 KB each).  Q window: 1 chunk.
-  auto n_chunks = [&](int it) -> int { return it == 0 ? 0 : (it <= nL + nF ? 2 * NMT : 1); };
-  auto chunk_src = [&](int it, int sub, const void *&src, uint32_t &bytes) {
+  // ---- chunk stream.  The CTA's windows in queue order [sink][recent][Full][Quantized]; a bf16
+  // window is NMT K chunks then NMT V chunks (4 KB each), a Quantized window one chunk, the sink
+  // none.  Chunk c lives in slot c % DEC_SLOTS and completes on full[c % DEC_FULL].
+  const int nb = (L1 - L0) + (F1 - F0);          // bf16 windows of this CTA
+  const int n_total = 2 * NMT * nb + (Q1 - Q0);  // chunks of this CTA
+  auto chunk_start = [&](int pos) -> int {
+    const int k = pos - has_sink;
+    if (k <= 0) return 0;
+    return k <= nb ? 2 * NMT * k : 2 * NMT * nb + (k - nb);
+  };
+  // global source of chunk c
+  auto chunk_src = [&](int c, const void *&src, uint32_t &bytes) {
+    int pos, sub;
+    if (c < 2 * NMT * nb) {
+      pos = has_sink + c / (2 * NMT);
+      sub = c % (2 * NMT);
+    } else {
+      pos = has_sink + nb + (c - 2 * NMT * nb);
+      sub = 0;
+    }
+    const int it = item_of(pos);
     if (it <= nL) {
       const int rs = (j0 + it - 1) % C.ring_windows;
       const __nv_bfloat16 *kb = ring + (size_t)rs * Gm::BLK;
@@ -266,72 +266,93 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
       src = sub < NMT ? (const void *)(kb + sub * 2048) : (const void *)(vb + (sub - NMT) * 2048);
       bytes = DEC_STAGE_BYTES;
     } else if (it <= nL + nF) {
-      const int slot = f_entry(it - 1 - nL).y;
+      const int slot = __ldg(&ftab[it - 1 - nL].y);
       src = fpool + ((size_t)slot * C.h_kv + g) * 2 * Gm::BLK * 2 + (size_t)sub * DEC_STAGE_BYTES;
       bytes = DEC_STAGE_BYTES;
     } else {
-      const int slot = q_entry(it - 1 - nL - nF).y;
+      const int slot = __ldg(&qtab[it - 1 - nL - nF].y);
       src = ledger + ((size_t)slot * C.h_kv + g) * Gm::QB;
       bytes = Gm::QB;
     }
   };
-  int issued = 0, consumed = 0;      // chunks
-  int ngrab = 0, p_idx = 0, p_sub = 0, c_idx = 0;
-  bool exhausted = false, ok = true;
-  auto grab = [&]() {
-    int k = 0;
-    if (lane == 0) k = atomicAdd(&q_next, 1);
-    k = __shfl_sync(0xffffffffu, k, 0);
-    if (k >= cta_items) {
-      exhausted = true;
-      return;
-    }
-    gring[ngrab & 7] = item_of(k);
-    __syncwarp();
-    ++ngrab;
-  };
-  auto issue = [&]() {
-    while (issued - consumed < DEC_STAGES) {
-      if (p_idx == ngrab) {
-        if (exhausted || ngrab - c_idx >= 7) break;
-        grab();
-        if (exhausted) break;
-      }
-      const int it = gring[p_idx & 7];
-      const int nc = n_chunks(it);
-      if (nc == 0) {
-        ++p_idx;
-        p_sub = 0;
-        continue;
-      }
-      if (lane == 0) {
-        const void *src;
-        uint32_t bytes;
-        chunk_src(it, p_sub, src, bytes);
-        const int st = issued % DEC_STAGES;
-        fence_proxy_async();
-        mbar_arrive_expect_tx(&bars[st], bytes);
-        bulk_g2s(stage + st * DEC_STAGE_BYTES, src, bytes, &bars[st]);
-      }
-      ++issued;
-      if (++p_sub == nc) {
-        ++p_idx;
-        p_sub = 0;
-      }
-    }
-  };
+  // the producer's first batch: one chunk per lane, its source looked up before the barrier
+  const bool producer = warp == DEC_CONSUMERS;
+  const void *src0 = nullptr;
+  uint32_t bytes0 = 0;
+  if (producer && lane < n_total) chunk_src(lane, src0, bytes0);
+  if (threadIdx.x < DEC_FULL + DEC_SLOTS) {
+    mbar_init(&full[threadIdx.x], 1);
+    fence_mbar_init();
+  }
+  if (threadIdx.x == 0) q_next = 0;
+  __syncthreads();
+
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f}, macc[2] = {0.f, 0.f};
+  float o[8][4];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+  bool ok = true;
   auto wait_chunk = [&](int c) -> const uint8_t * {
-    const int st = c % DEC_STAGES;
-    if (!mbar_wait(&bars[st], (uint32_t)((c / DEC_STAGES) & 1), status)) ok = false;
-    return stage + st * DEC_STAGE_BYTES;
+    if (!mbar_wait(&full[c % DEC_FULL], (uint32_t)((c / DEC_FULL) & 1), status)) ok = false;
+    return slots + (c % DEC_SLOTS) * DEC_STAGE_BYTES;
+  };
+  auto release_chunk = [&](int c) {
+    if (lane == 0) mbar_arrive(&empty[c % DEC_SLOTS]);
   };
 
-  issue();
+  if (producer) {
+    // ---------------- producer warp: lane l issues chunk base + l of every batch of 32; a chunk
+    // reuses its slot once the consumer of the chunk DEC_SLOTS earlier has released it
+    bool waited = io.wait_first;
+    int done = n_total;           // chunks before this one were all issued
+    bool mine = false;            // this lane issued its chunk of the batch that stopped early
+    for (int base = 0; base < n_total; base += 32) {
+      const int c = base + lane;
+      bool good = true;
+      mine = false;
+      if (c < n_total) {
+        const void *src = src0;
+        uint32_t bytes = bytes0;
+        if (base > 0) chunk_src(c, src, bytes);
+        if (c >= DEC_SLOTS) good = mbar_wait(&empty[c % DEC_SLOTS], (uint32_t)(((c / DEC_SLOTS) - 1) & 1), status);
+        if (good) {
+          uint64_t *bar = &full[c % DEC_FULL];
+          mbar_arrive_expect_tx(bar, bytes);
+          bulk_g2s(slots + (c % DEC_SLOTS) * DEC_STAGE_BYTES, src, bytes, bar);
+          mine = true;
+        }
+      }
+      // the step's inputs come from the previous kernel in a model: wait for it once the first
+      // batch is in flight, then let the next kernel start
+      if (!waited) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        waited = true;
+      }
+      if (!__all_sync(0xffffffffu, good)) {   // a wait ran out: stop issuing
+        done = base;
+        break;
+      }
+      mine = false;
+    }
+    if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // no copy may still be landing when the CTA ends.  Every earlier chunk of a slot landed before
+    // the slot was reused, so only the last DEC_SLOTS chunks issued in order (and those of a batch
+    // that stopped early) can still be in flight; none of them shares a barrier phase with another.
+    for (int k = (done > DEC_SLOTS ? done - DEC_SLOTS : 0) + lane; k < done; k += 32)
+      mbar_wait(&full[k % DEC_FULL], (uint32_t)((k / DEC_FULL) & 1), status);
+    if (mine) {
+      const int k = done + lane;
+      mbar_wait(&full[k % DEC_FULL], (uint32_t)((k / DEC_FULL) & 1), status);
+    }
+    __syncwarp();
+  } else {
+  // ---------------- consumer warps
   // the step's inputs come from the previous kernel in a model: wait for it, then let the next start
   if (!io.wait_first) asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // q as the B operand of S^T = K q^T: b0 = q[head gl][16j+2tl .. +1], b1 = the same at +8
-  // (loaded while the first bulk copies are in flight)
   uint32_t qb[8][2];
   {
     const __nv_bfloat16 *qh = io.q + ((size_t)b * C.h_q + (size_t)g * G + gl) * D;
@@ -342,15 +363,12 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
     }
   }
   while (ok) {
-    if (c_idx == ngrab) {
-      issue();
-      if (c_idx == ngrab) {
-        if (exhausted) break;
-        grab();
-        if (exhausted) break;
-      }
-    }
-    const int it = gring[c_idx & 7];
+    int pos = 0;
+    if (lane == 0) pos = atomicAdd(&q_next, 1);
+    pos = __shfl_sync(0xffffffffu, pos, 0);
+    if (pos >= cta_items) break;
+    const int c0 = chunk_start(pos);
+    const int it = item_of(pos);
     float tsum[2], mnew[2];
     if (it == 0) {
       // ---------------- sink tokens (no mass): fragments straight from the compact sink rows
@@ -385,7 +403,6 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
         const uint32_t a3 = vv(t1, d1) | (vv(t1 + 1, d1) << 16);
         mma_bf16(o[i], a0, a1, a2, a3, pb[0][0], pb[0][1]);
       }
-      ++c_idx;
       continue;
     }
 
@@ -397,11 +414,11 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
     if (it <= nL + nF) {
       // ---------------- bf16 window (recent or Full)
       const bool is_local = it <= nL;
-      const int wid = is_local ? j0 + it - 1 : f_entry(it - 1 - nL).x;
+      const int wid = j0 + it - 1;   // the recent window (meaningful only when is_local)
       const int newtok = (is_local && wid == jn) ? T - (C.n_sink + jn * W) : -1;
       const uint8_t *kc[NMT];
 #pragma unroll
-      for (int mt = 0; mt < NMT; ++mt) kc[mt] = wait_chunk(consumed + mt);
+      for (int mt = 0; mt < NMT; ++mt) kc[mt] = wait_chunk(c0 + mt);
       if (newtok >= 0 && ok) {
         // append: the new token enters the recent ring (global) and this warp's staged copy
         const int rs = jn % C.ring_windows;
@@ -416,6 +433,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
           *reinterpret_cast<uint32_t *>(kb + idx) = pair;
           *reinterpret_cast<uint32_t *>(kst + (idx - (newtok >> 4) * 2048) * 2) = pair;
         }
+        fence_proxy_async();   // this generic write must precede the slot's next bulk copy
         __syncwarp();
       }
 #pragma unroll
@@ -427,8 +445,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
         }
       }
       __syncwarp();
-      consumed += NMT;
-      issue();
+#pragma unroll
+      for (int mt = 0; mt < NMT; ++mt) release_chunk(c0 + mt);
 #pragma unroll
       for (int mt = 0; mt < NMT; ++mt) {
         const int tok0 = 16 * mt + gl;
@@ -450,7 +468,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
       p_to_b<NMT>(s, pb);
       const uint8_t *vc[NMT];
 #pragma unroll
-      for (int kk = 0; kk < NMT; ++kk) vc[kk] = wait_chunk(consumed + kk);
+      for (int kk = 0; kk < NMT; ++kk) vc[kk] = wait_chunk(c0 + NMT + kk);
       if (newtok >= 0 && ok) {
         const int rs = jn % C.ring_windows;
         __nv_bfloat16 *vb = ring + (size_t)(C.ring_windows + rs) * Gm::BLK;
@@ -464,6 +482,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
           reinterpret_cast<unsigned short *>(vb)[idx] = x;
           reinterpret_cast<unsigned short *>(vst)[idx - (newtok >> 4) * 2048] = x;
         }
+        fence_proxy_async();
         __syncwarp();
       }
 #pragma unroll
@@ -475,11 +494,11 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
         }
       }
       __syncwarp();
-      consumed += NMT;
-      issue();
+#pragma unroll
+      for (int kk = 0; kk < NMT; ++kk) release_chunk(c0 + NMT + kk);
     } else {
       // ---------------- Quantized window: INT2 codes + fp16 scale/offset
-      const uint8_t *ch = wait_chunk(consumed);
+      const uint8_t *ch = wait_chunk(c0);
       // key tables: channel d = 4*lane + k, values bf16(fp32(c*s + m)), c = 0..3, split in lo / hi bytes
       {
         const uint2 sp = *reinterpret_cast<const uint2 *>(ch + Gm::OFF_KS + 8 * lane);
@@ -553,8 +572,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
         }
       }
       __syncwarp();
-      consumed += 1;
-      issue();
+      release_chunk(c0);
     }
     // log2-sum-exp of this window's logits per head: its mass is 2^(mu - M) / L after the merge
     if (gl == 0) {
@@ -564,13 +582,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
         if (head < G) mu[(size_t)it * 8 + head] = tsum[h] > 0.f ? mnew[h] + __log2f(tsum[h]) : -INFINITY;
       }
     }
-    ++c_idx;
   }
-  // drain: never leave a bulk copy in flight into shared memory
-  while (consumed < issued) {
-    wait_chunk(consumed);
-    ++consumed;
-  }
+  }   // consumer warps
 
   // ---------------- merge the warps of this CTA into one split partial
   __syncthreads();
