@@ -45,6 +45,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample-steps", type=int, default=8)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="run the workload with fewer layers (a smaller case for profiler captures; "
+                         "the JSON line then reports that layer count)")
     ap.add_argument("--oracle-child", default=None, help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -239,7 +242,7 @@ def run_gpu(args, rank, world):
     build.build()
     binding.load()
     dev = torch.device("cuda", torch.cuda.current_device())
-    wl = synth.workload(args.workload)
+    wl = synth.workload(args.workload) if args.layers is None else synth.workload(args.workload, n_layers=args.layers)
     K, Wm = args.steps, args.warmup
     Om = wl.omega
     K_kern = 2 * Om

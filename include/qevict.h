@@ -55,7 +55,7 @@ typedef enum {
  * {1, 2, 4, 8}; 1 <= n_sink <= 16; n_recent >= window; prompt_len > n_sink. */
 typedef struct {
   int32_t batch, n_layers, h_q, h_kv, d_head;
-  int32_t n_sink, n_recent, window, bits, omega;
+  int32_t n_sink, n_recent, window, bits, omega;  /* omega: decode steps between routing events, 1..256 */
   int32_t q_num, q_den;           /* quantised-tier fraction q = q_num / q_den (QEvict §4.3 Eq. (3)) */
   int32_t budget_num, budget_den; /* B_total = floor(budget_num * M_FullKV / budget_den) when b_total == 0 */
   int64_t b_total;                /* bytes per (sequence, layer); 0 = use the fraction above */
@@ -163,8 +163,10 @@ qevict_status qevict_prefill_route(qevict_cache *cache, int32_t layer, const voi
  * set) and §4.2 Eq. (1): appends k_new, v_new [batch][h_kv][d] at position T (the recent region),
  * computes out[batch][h_q][d] = softmax(q K_acc^T / sqrt(d)) V_acc over sink + Full + dequantised
  * Quantized + recent tokens (the new token included; query head h reads KV head h / (h_q/h_kv)),
- * and adds (1/h_q) * sum_h (attention mass of window w) to every accessible non-sink window's
- * score.  q [batch][h_q][d].  Fails with QEVICT_ESCHEDULE if the cache is full (T = max_len). */
+ * and records the attention mass of every accessible non-sink window.  The window scores absorb
+ * these masses, (1/h_q) * sum_h (mass of window w) per step and in step order, at the next
+ * qevict_flush_scores or qevict_route.  q [batch][h_q][d].  Fails with QEVICT_ESCHEDULE if the
+ * cache is full (T = max_len) or a routing event is due. */
 qevict_status qevict_decode_step(qevict_cache *cache, int32_t layer, const void *q, const void *k_new,
                                  const void *v_new, void *out, qevict_stream_t stream);
 
@@ -177,6 +179,12 @@ qevict_status qevict_decode_step(qevict_cache *cache, int32_t layer, const void 
  * in window order.  Legal only when every layer has taken the same multiple of omega decode
  * steps since its prefill (else QEVICT_ESCHEDULE). */
 qevict_status qevict_route(qevict_cache *cache, qevict_stream_t stream);
+
+/* QEvict §4.2 Eq. (1), applied lazily: adds the window masses recorded by every decode step since
+ * the previous flush (of any layer) to the window scores, one step at a time in decode order, so
+ * the scores equal those of an update after every step.  qevict_route flushes by itself; call this
+ * only to read scores between routing events.  QEVICT_ESCHEDULE before every layer is prefilled. */
+qevict_status qevict_flush_scores(qevict_cache *cache, qevict_stream_t stream);
 
 /* Copies the 7 cumulative transition counters (promotions Q->F, demotions F->Q, first-time
  * quantisations, ledger reactivations, evictions, aged->F, aged->Q), summed over all units, to

@@ -65,6 +65,7 @@ def load() -> ctypes.CDLL:
         "qevict_prefill_route": [P, I32, P, P, P, P, P],
         "qevict_decode_step": [P, I32, P, P, P, P, P],
         "qevict_route": [P, P],
+        "qevict_flush_scores": [P, P],
         "qevict_read_counters": [P, ctypes.POINTER(I64), P],
         "qevict_check": [P, P],
         "qevict_destroy": [P],
@@ -85,7 +86,7 @@ def exported_symbols():
     return ["qevict_budget", "qevict_cache_bytes", "qevict_init_cache", "qevict_get_layout",
             "qevict_prefill_scores", "qevict_prefill_route", "qevict_decode_step", "qevict_route",
             "qevict_read_counters", "qevict_check", "qevict_destroy", "qevict_status_string",
-            "qevict_prefill_scores_noalloc"]
+            "qevict_prefill_scores_noalloc", "qevict_flush_scores"]
 
 
 def _check(status: int, where: str):
@@ -175,6 +176,9 @@ class Cache:
 
     def route(self, stream=None):
         _check(load().qevict_route(self.handle, _stream(stream)), "qevict_route")
+
+    def flush_scores(self, stream=None):
+        _check(load().qevict_flush_scores(self.handle, _stream(stream)), "qevict_flush_scores")
 
     def counters(self, stream=None) -> dict:
         buf = (ctypes.c_int64 * 7)()

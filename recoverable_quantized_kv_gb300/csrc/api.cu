@@ -21,6 +21,7 @@ cudaError_t launch_prefill_setup(const CacheDev &C, const __nv_bfloat16 *kp, con
 cudaError_t launch_prefill_scores(const CacheDev &C, const __nv_bfloat16 *q, const __nv_bfloat16 *k, float *s0,
                                   cudaStream_t s);
 cudaError_t launch_decode(const CacheDev &C, const DecodeIO &io, cudaStream_t s);
+cudaError_t launch_flush(const CacheDev &C, cudaStream_t s);
 int route_max_windows();
 int decode_warps();
 }  // namespace qv
@@ -60,7 +61,9 @@ qevict_status check_config(const qevict_config *c) {
   if (G != 1 && G != 2 && G != 4 && G != 8) return QEVICT_EINVAL;
   if (c->d_head != D) return QEVICT_EINVAL;
   if (!(c->window == 32 && c->bits == 2)) return QEVICT_EINVAL;
-  if (c->n_sink < 1 || c->n_sink > 16 || c->n_recent < c->window || c->omega < 1) return QEVICT_EINVAL;
+  if (c->n_sink < 1 || c->n_sink > 16 || c->n_recent < c->window || c->omega < 1 ||
+      c->omega > 256)
+    return QEVICT_EINVAL;
   if (c->q_den < 1 || c->q_num < 0 || c->q_num > c->q_den) return QEVICT_EINVAL;
   if (c->b_total < 0 || (c->b_total == 0 && (c->budget_den < 1 || c->budget_num < 0))) return QEVICT_EINVAL;
   if (c->prompt_len <= c->n_sink || c->max_len < c->prompt_len) return QEVICT_EINVAL;
@@ -147,8 +150,11 @@ void make_plan(const qevict_config *c, const qevict_budget_info *b, Plan *p) {
   C.off_headctr = global(4LL * c->n_layers * c->batch);
   C.st_part_layer = align256(4LL * c->batch * c->h_kv * n_split * qv::PART_FLOATS);
   C.off_part = global(C.st_part_layer * c->n_layers);
-  C.st_mu_layer = align256(4LL * c->batch * c->h_kv * max_items * 8);
+  C.st_mu_layer = align256(4LL * c->batch * c->h_kv * c->omega * max_items * 8);
   C.off_mu = global(C.st_mu_layer * c->n_layers);
+  C.st_mstat_layer = align256(4LL * c->batch * c->h_kv * c->omega * 16);
+  C.off_mstat = global(C.st_mstat_layer * c->n_layers);
+  C.off_flushctr = global(4LL * c->n_layers * c->batch);
   C.off_rowstat = global(4LL * c->batch * c->h_q * c->prompt_len);
   C.off_colsum = global(4LL * c->batch * c->h_q * c->prompt_len);
   const int npw = (c->prompt_len - c->n_sink + W - 1) / W;
@@ -307,10 +313,21 @@ qevict_status qevict_route(qevict_cache *cache, qevict_stream_t stream) {
   const int due = cache->cfg.prompt_len + (cache->routes_done + 1) * cache->cfg.omega;
   for (int l = 0; l < cache->cfg.n_layers; ++l)
     if (!cache->prefilled[l] || cache->t_host[l] != due) return QEVICT_ESCHEDULE;
-  cudaError_t e = qv::launch_route(cache->dev, 0, cache->cfg.batch * cache->cfg.n_layers, nullptr, nullptr, 0, 8,
-                                   reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = qv::launch_flush(cache->dev, reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaSuccess)
+    e = qv::launch_route(cache->dev, 0, cache->cfg.batch * cache->cfg.n_layers, nullptr, nullptr, 0, 8,
+                         reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return QEVICT_ECUDA;
   cache->routes_done += 1;
+  cache->last_decode_layer = -1;
+  return QEVICT_OK;
+}
+
+qevict_status qevict_flush_scores(qevict_cache *cache, qevict_stream_t stream) {
+  if (!cache) return QEVICT_EINVAL;
+  for (int l = 0; l < cache->cfg.n_layers; ++l)
+    if (!cache->prefilled[l]) return QEVICT_ESCHEDULE;
+  if (qv::launch_flush(cache->dev, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return QEVICT_ECUDA;
   cache->last_decode_layer = -1;
   return QEVICT_OK;
 }

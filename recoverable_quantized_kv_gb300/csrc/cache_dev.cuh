@@ -29,12 +29,21 @@ struct CacheDev {
   int64_t off_splitctr;            // uint32 [L][B][h_kv]
   int64_t off_headctr;             // uint32 [L][B]
   int64_t off_part, st_part_layer; // float [L][B][h_kv][n_split][PART_FLOATS]
-  int64_t off_mu, st_mu_layer;     // float [L][B][h_kv][max_items][8]
+  // per-window log2-sum-exp of the decode steps since the last score flush, by step slot
+  // (tokens cached at the step minus those at the flush) and stable item index
+  int64_t off_mu, st_mu_layer;     // float [L][B][h_kv][omega][max_items][8]
+  int64_t off_mstat, st_mstat_layer;   // float [L][B][h_kv][omega][16]: merged max M[8], 1/L[8] per step
+  int64_t off_flushctr;            // uint32 [L][B] score-flush arrivals
   int64_t off_rowstat;             // float [B][h_q][P] prefill row log2-sum-exp
   int64_t off_colsum;              // float [B][h_q][P] prefill column sums
   // sizes
   int B, L, h_q, h_kv, G, n_sink, n_recent, W, bits, omega;
   int k_f, k_q, n_windows, ring_windows, n_split, max_items, prompt_len, max_len;
+
+  // Stable index of a window's mass record between two routing events: 1 + i for the i-th recent
+  // window from the first unrouted one, then the Full table entries, then the Quantized ones.
+  __host__ __device__ int loc_items() const { return ring_windows + 1; }
+  __host__ __device__ int kf_cap() const { return k_f < n_windows ? k_f : n_windows; }
 
   template <typename T>
   __host__ __device__ T *at(int64_t off, int64_t st, int u) const {

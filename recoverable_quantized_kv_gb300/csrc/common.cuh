@@ -15,7 +15,8 @@ namespace qv {
 
 constexpr int D = 128;            // head dimension (fixed)
 constexpr int META_INTS = 16;     // per-unit meta words
-enum : int { M_T = 0, M_NROUTE = 1, M_FCOUNT = 2, M_QCOUNT = 3, M_NQUANT = 4, M_NMOVE = 5, M_NEVENT = 6 };
+// M_FLUSHT: tokens cached when the window scores last absorbed the decode steps' masses
+enum : int { M_T = 0, M_NROUTE = 1, M_FCOUNT = 2, M_QCOUNT = 3, M_NQUANT = 4, M_NMOVE = 5, M_NEVENT = 6, M_FLUSHT = 7 };
 
 enum : int { TIER_LOCAL = 0, TIER_FULL = 1, TIER_QUANT = 2, TIER_EVICT = 3 };
 enum : int { LED_NONE = 0, LED_ACTIVE = 1, LED_DORMANT = 2 };

@@ -63,11 +63,13 @@ __device__ __forceinline__ uint32_t ldg16(const void *p) { return __ldg(reinterp
 
 // One online-softmax step over NMT 16-token groups of S^T fragments (rows tokens, cols heads).
 // s is in log2 units; rows flagged invalid are excluded.  On return s holds the probabilities
-// (relative to the new running max), tsum the per-head sum over this item, mnew the new max.
+// relative to the running max m_run, tsum the per-head sum over this item.  The running max only
+// moves when some logit of the item exceeds it (one warp vote decides); otherwise every
+// probability is already <= 1 and nothing accumulated so far (o, macc, l_run) needs rescaling.
 template <int NMT>
 __device__ __forceinline__ void online_step(float (&s)[NMT][4], const bool (&valid)[NMT][2], float (&m_run)[2],
-                                            float (&l_run)[2], float (&o)[8][4], float (&tsum)[2],
-                                            float (&mnew)[2]) {
+                                            float (&l_run)[2], float (&o)[8][4], float (&macc)[2],
+                                            float (&tsum)[2]) {
   float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
   for (int mt = 0; mt < NMT; ++mt)
@@ -77,17 +79,27 @@ __device__ __forceinline__ void online_step(float (&s)[NMT][4], const bool (&val
         mx[0] = fmaxf(mx[0], s[mt][2 * r]);
         mx[1] = fmaxf(mx[1], s[mt][2 * r + 1]);
       }
+  if (!__all_sync(0xffffffffu, mx[0] <= m_run[0] && mx[1] <= m_run[1])) {
+    float corr[2];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    mx[h] = warp_max_xor_g(mx[h]);
-    mnew[h] = fmaxf(m_run[h], mx[h]);
-  }
-  float base[2], corr[2], ps[2] = {0.f, 0.f};
+    for (int h = 0; h < 2; ++h) {
+      const float mnew = fmaxf(m_run[h], warp_max_xor_g(mx[h]));
+      corr[h] = exp2f(m_run[h] - (mnew == -INFINITY ? 0.f : mnew));
+      m_run[h] = mnew;
+      l_run[h] *= corr[h];
+      macc[h] *= corr[h];
+    }
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    base[h] = (mnew[h] == -INFINITY) ? 0.f : mnew[h];
-    corr[h] = exp2f(m_run[h] - base[h]);
+    for (int i = 0; i < 8; ++i) {
+      o[i][0] *= corr[0];
+      o[i][2] *= corr[0];
+      o[i][1] *= corr[1];
+      o[i][3] *= corr[1];
+    }
   }
+  float base[2], ps[2] = {0.f, 0.f};
+#pragma unroll
+  for (int h = 0; h < 2; ++h) base[h] = m_run[h] == -INFINITY ? 0.f : m_run[h];
 #pragma unroll
   for (int mt = 0; mt < NMT; ++mt)
 #pragma unroll
@@ -101,15 +113,7 @@ __device__ __forceinline__ void online_step(float (&s)[NMT][4], const bool (&val
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     tsum[h] = warp_sum_xor_g(ps[h]);
-    l_run[h] = l_run[h] * corr[h] + tsum[h];
-    m_run[h] = mnew[h];
-  }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    o[i][0] *= corr[0];
-    o[i][2] *= corr[0];
-    o[i][1] *= corr[1];
-    o[i][3] *= corr[1];
+    l_run[h] += tsum[h];
   }
 }
 
@@ -139,11 +143,10 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int k) {
 }
 
 // Exact bf16(fp32(code * s + m)) for keys via per-channel byte tables: lo/hi bytes of the 4
-// dequantised values of channel pair A (2t, 2t+1) and B (2t+8, 2t+9) of k-step j.
-__device__ __forceinline__ void lut_k_regs(uint32_t f, const uint4 &TA, const uint4 &TB, uint32_t &a0, uint32_t &a1,
-                                           uint32_t &a2, uint32_t &a3) {
-  const uint32_t sel01 = (f & 0x3333u) | 0x4040u;
-  const uint32_t sel23 = ((f >> 2) & 0x3333u) | 0x4040u;
+// dequantised values of channel pair A (2t, 2t+1) and B (2t+8, 2t+9) of k-step j.  sel01 / sel23
+// are the byte-permute selectors of the field (its low 16 bits are used).
+__device__ __forceinline__ void lut_k_regs(uint32_t sel01, uint32_t sel23, const uint4 &TA, const uint4 &TB,
+                                           uint32_t &a0, uint32_t &a1, uint32_t &a2, uint32_t &a3) {
   uint32_t lo = __byte_perm(TA.x, TA.y, sel01), hi = __byte_perm(TA.z, TA.w, sel01);
   a0 = __byte_perm(lo, hi, 0x5140);
   a1 = __byte_perm(lo, hi, 0x7362);
@@ -199,6 +202,12 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   int *status = C.status();
   int *meta = C.at<int>(C.off_meta, C.st_meta, unit);
   const int T = meta[M_T], n_route = meta[M_NROUTE], nF = meta[M_FCOUNT], nQ = meta[M_QCOUNT];
+  // this step's slot in the per-step mass records: steps since the scores last absorbed them
+  int mslot = T - meta[M_FLUSHT];
+  if (mslot < 0 || mslot >= C.omega) {
+    if (threadIdx.x == 0) atomicOr(C.status(), QV_ERR_STATE);
+    mslot = mslot < 0 ? 0 : C.omega - 1;
+  }
   const int2 *ftab = C.at<const int2>(C.off_ftab, C.st_ftab, unit);
   const int2 *qtab = C.at<const int2>(C.off_qtab, C.st_qtab, unit);
   const __nv_bfloat16 *sink = C.at<const __nv_bfloat16>(C.off_sink, C.st_sink, unit) + (size_t)g * 2 * C.n_sink * D;
@@ -206,7 +215,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   const uint8_t *fpool = C.at<const uint8_t>(C.off_fpool, C.st_fpool, unit);
   const uint8_t *ledger = C.at<const uint8_t>(C.off_ledger, C.st_ledger, unit);
   const int bg = b * C.h_kv + g;
-  float *mu = reinterpret_cast<float *>(C.arena + C.off_mu + C.st_mu_layer * io.layer) + (size_t)bg * C.max_items * 8;
+  float *mu = reinterpret_cast<float *>(C.arena + C.off_mu + C.st_mu_layer * io.layer) +
+              ((size_t)bg * C.omega + mslot) * C.max_items * 8;
   float *part = reinterpret_cast<float *>(C.arena + C.off_part + C.st_part_layer * io.layer) +
                 (size_t)bg * C.n_split * PART_FLOATS;
 
@@ -369,7 +379,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
     if (pos >= cta_items) break;
     const int c0 = chunk_start(pos);
     const int it = item_of(pos);
-    float tsum[2], mnew[2];
+    float tsum[2];
     if (it == 0) {
       // ---------------- sink tokens (no mass): fragments straight from the compact sink rows
       float sacc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
@@ -386,10 +396,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
 #pragma unroll
       for (int k = 0; k < 4; ++k) sacc[0][k] *= io.scale_log2;
       const bool valid[1][2] = {{r0, r1}};
-      const float mold0 = m_run[0], mold1 = m_run[1];
-      online_step<1>(sacc, valid, m_run, l_run, o, tsum, mnew);
-      macc[0] *= exp2f(mold0 - (m_run[0] == -INFINITY ? 0.f : m_run[0]));
-      macc[1] *= exp2f(mold1 - (m_run[1] == -INFINITY ? 0.f : m_run[1]));
+      online_step<1>(sacc, valid, m_run, l_run, o, macc, tsum);
       uint32_t pb[1][2];
       p_to_b<1>(sacc, pb);
       const int t0 = 2 * tl, t1 = 2 * tl + 8;
@@ -460,10 +467,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
 #pragma unroll
         for (int k = 0; k < 4; ++k) s[mt][k] *= io.scale_log2;
       }
-      const float mold0 = m_run[0], mold1 = m_run[1];
-      online_step<NMT>(s, valid, m_run, l_run, o, tsum, mnew);
-      macc[0] *= exp2f(mold0 - (m_run[0] == -INFINITY ? 0.f : m_run[0]));
-      macc[1] *= exp2f(mold1 - (m_run[1] == -INFINITY ? 0.f : m_run[1]));
+      online_step<NMT>(s, valid, m_run, l_run, o, macc, tsum);
       uint32_t pb[NMT][2];
       p_to_b<NMT>(s, pb);
       const uint8_t *vc[NMT];
@@ -521,16 +525,26 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
       __syncwarp();
       const uint4 kcw0 = lds128(ch + lane * 16), kcw1 = lds128(ch + 512 + lane * 16);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint4 TA = lds128(tbl + (j * 4 + tl) * 32);
-        const uint4 TB = lds128(tbl + (j * 4 + tl) * 32 + 16);
+      for (int jp = 0; jp < 4; ++jp) {
+        // selectors of both fields of a code word at once: k-step 2jp in the low half, 2jp+1 high
+        uint32_t sa[NMT], sb[NMT];
 #pragma unroll
         for (int mt = 0; mt < NMT; ++mt) {
-          const uint32_t wd = word_of(mt == 0 ? kcw0 : kcw1, j >> 1);
-          const uint32_t f = (j & 1) ? (wd >> 16) : wd;
-          uint32_t a0, a1, a2, a3;
-          lut_k_regs(f, TA, TB, a0, a1, a2, a3);
-          mma_bf16(s[mt], a0, a1, a2, a3, qb[j][0], qb[j][1]);
+          const uint32_t wd = word_of(mt == 0 ? kcw0 : kcw1, jp);
+          sa[mt] = (wd & 0x33333333u) | 0x40404040u;
+          sb[mt] = ((wd >> 2) & 0x33333333u) | 0x40404040u;
+        }
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int j = 2 * jp + hf;
+          const uint4 TA = lds128(tbl + (j * 4 + tl) * 32);
+          const uint4 TB = lds128(tbl + (j * 4 + tl) * 32 + 16);
+#pragma unroll
+          for (int mt = 0; mt < NMT; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            lut_k_regs(hf ? sa[mt] >> 16 : sa[mt], hf ? sb[mt] >> 16 : sb[mt], TA, TB, a0, a1, a2, a3);
+            mma_bf16(s[mt], a0, a1, a2, a3, qb[j][0], qb[j][1]);
+          }
         }
       }
 #pragma unroll
@@ -539,10 +553,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
 #pragma unroll
         for (int k = 0; k < 4; ++k) s[mt][k] *= io.scale_log2;
       }
-      const float mold0 = m_run[0], mold1 = m_run[1];
-      online_step<NMT>(s, valid, m_run, l_run, o, tsum, mnew);
-      macc[0] *= exp2f(mold0 - m_run[0]);
-      macc[1] *= exp2f(mold1 - m_run[1]);
+      online_step<NMT>(s, valid, m_run, l_run, o, macc, tsum);
       // values: o += sum_tok (p * s_tok) * code + (sum_tok p * m_tok) in every dim
       uint32_t pbh[NMT][2];
       float pm0 = 0.f, pm1 = 0.f;
@@ -574,64 +585,66 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
       __syncwarp();
       release_chunk(c0);
     }
-    // log2-sum-exp of this window's logits per head: its mass is 2^(mu - M) / L after the merge
+    // log2-sum-exp of this window's logits per head: its mass is 2^(mu - M) / L with the merged
+    // max M and sum L; recorded under the window's stable index (recent, then Full, then Quantized)
     if (gl == 0) {
+      const int sidx = it <= nL ? it : (it <= nL + nF ? it - nL + C.loc_items() : it - nL - nF + C.loc_items() + C.kf_cap());
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int head = 2 * tl + h;
-        if (head < G) mu[(size_t)it * 8 + head] = tsum[h] > 0.f ? mnew[h] + __log2f(tsum[h]) : -INFINITY;
+        if (head < G) mu[(size_t)sidx * 8 + head] = tsum[h] > 0.f ? m_run[h] + __log2f(tsum[h]) : -INFINITY;
       }
     }
   }
   }   // consumer warps
 
-  // ---------------- merge the warps of this CTA into one split partial
+  // ---------------- merge the consumer warps of this CTA into one split partial
   __syncthreads();
-  float *cm = reinterpret_cast<float *>(smem);            // [warp][8] running max
-  float *cl = cm + DEC_WARPS * 8;                           // [warp][8] running sum
-  float *cf = cl + DEC_WARPS * 8;                           // [warp][8] rescale factor
-  float *sM = cf + DEC_WARPS * 8;                           // [8] CTA max per head
-  float *cO = sM + 16;                                      // [warp][8][D]
-  if (gl == 0) {
+  const int lgG = __ffs(G) - 1;
+  float *cm = reinterpret_cast<float *>(smem);   // [DEC_CONSUMERS][8] running max
+  float *cl = cm + DEC_CONSUMERS * 8;            // [DEC_CONSUMERS][8] running sum
+  float *cf = cl + DEC_CONSUMERS * 8;            // [DEC_CONSUMERS][8] rescale factor to the CTA max
+  float *sM = cf + DEC_CONSUMERS * 8;            // [16] CTA max per head, then the merged max and 1/L
+  float *cO = sM + 16;                           // [DEC_CONSUMERS][D][8] unnormalised outputs
+  if (warp < DEC_CONSUMERS) {
+    if (gl == 0) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      cm[warp * 8 + 2 * tl + h] = m_run[h];
-      cl[warp * 8 + 2 * tl + h] = l_run[h];
+      for (int h = 0; h < 2; ++h) {
+        cm[warp * 8 + 2 * tl + h] = m_run[h];
+        cl[warp * 8 + 2 * tl + h] = l_run[h];
+      }
+    }
+    if (2 * tl < G) {   // heads 2tl, 2tl+1 of dims 16i+gl and 16i+gl+8, as float2
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        float *r = cO + ((size_t)warp * D + 16 * i + gl) * 8 + 2 * tl;
+        *reinterpret_cast<float2 *>(r) = make_float2(o[i][0] + macc[0], o[i][1] + macc[1]);
+        *reinterpret_cast<float2 *>(r + 64) = make_float2(o[i][2] + macc[0], o[i][3] + macc[1]);
+      }
     }
   }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    float *w0 = cO + (warp * 8 + 2 * tl) * D, *w1 = w0 + D;
-    w0[16 * i + gl] = o[i][0] + macc[0];
-    w1[16 * i + gl] = o[i][1] + macc[1];
-    w0[16 * i + gl + 8] = o[i][2] + macc[0];
-    w1[16 * i + gl + 8] = o[i][3] + macc[1];
-  }
   __syncthreads();
-  if (threadIdx.x < 8) {
+  if (threadIdx.x < DEC_CONSUMERS * 8) {
+    const int h = threadIdx.x & 7;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < DEC_WARPS; ++w) M = fmaxf(M, cm[w * 8 + threadIdx.x]);
-    sM[threadIdx.x] = M;
-  }
-  __syncthreads();
-  if (threadIdx.x < DEC_WARPS * 8) {
-    const float M = sM[threadIdx.x & 7];
+    for (int w = 0; w < DEC_CONSUMERS; ++w) M = fmaxf(M, cm[w * 8 + h]);
     cf[threadIdx.x] = M == -INFINITY ? 0.f : exp2f(cm[threadIdx.x] - M);
+    if (threadIdx.x < 8) sM[h] = M;
   }
   __syncthreads();
   float *mypart = part + (size_t)split * PART_FLOATS;
   for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-    const int h = idx / D, d = idx % D;
+    const int h = idx & (G - 1), d = idx >> lgG;
     float acc = 0.f;
 #pragma unroll
-    for (int w = 0; w < DEC_WARPS; ++w) acc = fmaf(cO[(w * 8 + h) * D + d], cf[w * 8 + h], acc);
+    for (int w = 0; w < DEC_CONSUMERS; ++w) acc = fmaf(cO[((size_t)w * D + d) * 8 + h], cf[w * 8 + h], acc);
     mypart[16 + h * D + d] = acc;
   }
   if (threadIdx.x < G) {
     float l = 0.f;
 #pragma unroll
-    for (int w = 0; w < DEC_WARPS; ++w) l = fmaf(cl[w * 8 + threadIdx.x], cf[w * 8 + threadIdx.x], l);
+    for (int w = 0; w < DEC_CONSUMERS; ++w) l = fmaf(cl[w * 8 + threadIdx.x], cf[w * 8 + threadIdx.x], l);
     mypart[threadIdx.x] = sM[threadIdx.x];
     mypart[8 + threadIdx.x] = l;
   }
@@ -648,67 +661,47 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   __syncthreads();
   if (!s_last) return;
 
+  // outputs: one warp covers 32 dims of one head; lane sp holds split sp's (m, l), the merged max
+  // M and sum L come from warp reductions, and each lane folds every split's output for its dim
   const int nsp = C.n_split;
-  float *sml = cO;                         // [nsp][16]: m[8], l[8] of every split
-  float *sf = sml + nsp * 16;              // [nsp][8]: 2^(m - M) / L
-  float *Mh = sM, *iL = sM + 8;
-  for (int i = threadIdx.x; i < nsp * 16; i += blockDim.x) sml[i] = __ldcg(part + (size_t)(i >> 4) * PART_FLOATS + (i & 15));
-  __syncthreads();
-  if (threadIdx.x < G) {
-    const int h = threadIdx.x;
-    float M = -INFINITY;
-    for (int sp = 0; sp < nsp; ++sp)
-      if (sml[sp * 16 + 8 + h] > 0.f) M = fmaxf(M, sml[sp * 16 + h]);
-    float L = 0.f;
-    for (int sp = 0; sp < nsp; ++sp) {
-      const float l = sml[sp * 16 + 8 + h];
-      if (l > 0.f) L = fmaf(l, exp2f(sml[sp * 16 + h] - M), L);
-    }
-    Mh[h] = M;
-    iL[h] = 1.f / L;
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < nsp * 8; i += blockDim.x) {
-    const int sp = i >> 3, h = i & 7;
-    const float l = sml[sp * 16 + 8 + h];
-    sf[i] = (h < G && l > 0.f) ? exp2f(sml[sp * 16 + h] - Mh[h]) * iL[h] : 0.f;
-  }
-  __syncthreads();
   for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
     const int h = idx / D, d = idx % D;
-    const float *po = part + 16 + h * D + d;
-    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-    int sp = 0;
-    for (; sp + 4 <= nsp; sp += 4) {
-      const float o0 = __ldcg(po + (size_t)sp * PART_FLOATS), o1 = __ldcg(po + (size_t)(sp + 1) * PART_FLOATS);
-      const float o2 = __ldcg(po + (size_t)(sp + 2) * PART_FLOATS), o3 = __ldcg(po + (size_t)(sp + 3) * PART_FLOATS);
-      acc0 = fmaf(o0, sf[sp * 8 + h], acc0);
-      acc1 = fmaf(o1, sf[(sp + 1) * 8 + h], acc1);
-      acc2 = fmaf(o2, sf[(sp + 2) * 8 + h], acc2);
-      acc3 = fmaf(o3, sf[(sp + 3) * 8 + h], acc3);
+    const float *ph = part + h, *po = part + 16 + h * D + d;
+    float M = -INFINITY, L = 0.f, O = 0.f;
+    for (int s0 = 0; s0 < nsp; s0 += 32) {
+      const int n = min(32, nsp - s0);
+      float ov[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) ov[k] = k < n ? __ldcg(po + (size_t)(s0 + k) * PART_FLOATS) : 0.f;
+      const float l = lane < n ? __ldcg(ph + (size_t)(s0 + lane) * PART_FLOATS + 8) : 0.f;
+      const float m = lane < n ? __ldcg(ph + (size_t)(s0 + lane) * PART_FLOATS) : -INFINITY;
+      float Mc = l > 0.f ? m : -INFINITY;
+#pragma unroll
+      for (int x = 16; x >= 1; x >>= 1) Mc = fmaxf(Mc, __shfl_xor_sync(0xffffffffu, Mc, x));
+      const float Mn = fmaxf(M, Mc);   // finite: the newest token's window always holds mass
+      const float cold = M == -INFINITY ? 0.f : exp2f(M - Mn);
+      const float e = l > 0.f ? exp2f(m - Mn) : 0.f;
+      float Lc = l * e;
+#pragma unroll
+      for (int x = 16; x >= 1; x >>= 1) Lc += __shfl_xor_sync(0xffffffffu, Lc, x);
+      float Oc0 = 0.f, Oc1 = 0.f;
+#pragma unroll
+      for (int k = 0; k < 32; k += 2) {
+        Oc0 = fmaf(ov[k], __shfl_sync(0xffffffffu, e, k), Oc0);
+        Oc1 = fmaf(ov[k + 1], __shfl_sync(0xffffffffu, e, k + 1), Oc1);
+      }
+      L = fmaf(L, cold, Lc);
+      O = fmaf(O, cold, Oc0 + Oc1);
+      M = Mn;
     }
-    for (; sp < nsp; ++sp) acc0 = fmaf(__ldcg(po + (size_t)sp * PART_FLOATS), sf[sp * 8 + h], acc0);
-    io.out[((size_t)b * C.h_q + (size_t)g * G + h) * D + d] = __float2bfloat16_rn((acc0 + acc1) + (acc2 + acc3));
-  }
-  // window scores: S_g[w] += (1/H_q) * sum_{h in group} 2^(mu - M_h) / L_h; two items per thread in flight
-  float *score = C.at<float>(C.off_score, C.st_score, unit) + (size_t)g * C.n_windows;
-  const int total = 1 + nL + nF + nQ;
-  auto wid_of = [&](int it) -> int {
-    return it <= nL ? j0 + it - 1 : (it <= nL + nF ? __ldg(&ftab[it - 1 - nL].x) : __ldg(&qtab[it - 1 - nL - nF].x));
-  };
-  auto mass_of = [&](int it) -> float {
-    float m = 0.f;
-    for (int h = 0; h < G; ++h) m = fmaf(exp2f(__ldcg(mu + (size_t)it * 8 + h) - Mh[h]), iL[h], m);
-    return m * io.inv_hq;
-  };
-  for (int it = 1 + threadIdx.x; it < total; it += 2 * blockDim.x) {
-    const int it2 = it + blockDim.x;
-    const bool two = it2 < total;
-    const int w1 = wid_of(it), w2 = two ? wid_of(it2) : w1;
-    const float a1 = mass_of(it), a2 = two ? mass_of(it2) : 0.f;
-    const float s1 = score[w1], s2 = two ? score[w2] : 0.f;
-    score[w1] = s1 + a1;
-    if (two) score[w2] = s2 + a2;
+    const float inv = 1.f / L;
+    io.out[((size_t)b * C.h_q + (size_t)g * G + h) * D + d] = __float2bfloat16_rn(O * inv);
+    if (d == 0) {   // this step's merged max and 1/L: the window masses are applied when scores are flushed
+      float *ms = reinterpret_cast<float *>(C.arena + C.off_mstat + C.st_mstat_layer * io.layer) +
+                  ((size_t)bg * C.omega + mslot) * 16;
+      ms[h] = M;
+      ms[8 + h] = inv;
+    }
   }
   __syncthreads();
   if (threadIdx.x == 0) {

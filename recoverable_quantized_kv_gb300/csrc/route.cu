@@ -526,6 +526,7 @@ __global__ void prefill_setup_kernel(const CacheDev C, const PromptIO pio, const
     if (threadIdx.x == 0) {
       int *meta = C.at<int>(C.off_meta, C.st_meta, unit);
       meta[M_T] = P;
+      meta[M_FLUSHT] = P;
       meta[M_NROUTE] = 0;
       meta[M_FCOUNT] = 0;
       meta[M_QCOUNT] = 0;

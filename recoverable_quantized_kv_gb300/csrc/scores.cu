@@ -135,4 +135,83 @@ cudaError_t launch_prefill_scores(const CacheDev &C, const __nv_bfloat16 *q, con
   return cudaGetLastError();
 }
 
+
+// ----------------------------------------------------------------------------- deferred score updates
+//
+// QEvict §4.2 Eq. (1): after every decode step the score of window w grows by the attention mass
+// the step put on it, S(w) += (1/H_q) sum_h sum_{i in w} a^h(i).  The decode kernel records, per
+// step, every window's log2-sum-exp per query head (mu) and the merged max M and 1/L per head; this
+// kernel turns them into masses 2^(mu - M) / L and adds them to the per-KV-head score partials one
+// step at a time in decode order, the same floating-point sequence as adding after every step.
+// Scores are read only by the router, which flushes first.  One CTA per (KV head, sequence, layer).
+__global__ void __launch_bounds__(256) flush_kernel(const CacheDev C, float inv_hq) {
+  extern __shared__ float st[];   // [omega][16]
+  const int g = blockIdx.x, b = blockIdx.y, layer = blockIdx.z;
+  const int unit = layer * C.B + b, bg = b * C.h_kv + g;
+  int *meta = C.at<int>(C.off_meta, C.st_meta, unit);
+  __shared__ int s_meta[8];
+  if (threadIdx.x < 8) s_meta[threadIdx.x] = meta[threadIdx.x];
+  __syncthreads();
+  const int T = s_meta[M_T], F = s_meta[M_FLUSHT], j0 = s_meta[M_NROUTE];
+  const int nF = s_meta[M_FCOUNT], nQ = s_meta[M_QCOUNT];
+  const int nk = T - F;
+  if (nk < 0 || nk > C.omega) {
+    if (threadIdx.x == 0) atomicOr(C.status(), QV_ERR_STATE);
+  } else if (nk > 0) {
+    const float *ms = reinterpret_cast<const float *>(C.arena + C.off_mstat + C.st_mstat_layer * layer) +
+                      (size_t)bg * C.omega * 16;
+    for (int i = threadIdx.x; i < nk * 16; i += blockDim.x) st[i] = ms[i];
+    __syncthreads();
+    const float *mu = reinterpret_cast<const float *>(C.arena + C.off_mu + C.st_mu_layer * layer) +
+                      (size_t)bg * C.omega * C.max_items * 8;
+    float *score = C.at<float>(C.off_score, C.st_score, unit) + (size_t)g * C.n_windows;
+    const int2 *ftab = C.at<const int2>(C.off_ftab, C.st_ftab, unit);
+    const int2 *qtab = C.at<const int2>(C.off_qtab, C.st_qtab, unit);
+    const int LOC = C.loc_items(), KFC = C.kf_cap();
+    const int G = C.G;
+    for (int idx = 1 + threadIdx.x; idx < C.max_items; idx += blockDim.x) {
+      int w, k0 = 0;
+      if (idx <= LOC) {   // recent window j0 + idx - 1: in the step of T_k tokens once T_k >= n_sink + w W
+        w = j0 + idx - 1;
+        if (w >= C.n_windows) continue;
+        k0 = max(0, C.n_sink + w * C.W - F);
+        if (k0 >= nk) continue;
+      } else if (idx <= LOC + KFC) {
+        const int f = idx - 1 - LOC;
+        if (f >= nF) continue;
+        w = ftab[f].x;
+      } else {
+        const int q = idx - 1 - LOC - KFC;
+        if (q >= nQ) continue;
+        w = qtab[q].x;
+      }
+      float s = score[w];
+      for (int k = k0; k < nk; ++k) {
+        const float *m = mu + ((size_t)k * C.max_items + idx) * 8;
+        const float *Mk = st + k * 16;
+        float a = 0.f;
+        for (int h = 0; h < G; ++h) a = fmaf(exp2f(m[h] - Mk[h]), Mk[8 + h], a);
+        s = s + a * inv_hq;
+      }
+      score[w] = s;
+    }
+  }
+  // the last of the unit's CTAs to finish records the flush (every CTA has read M_FLUSHT by then)
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned *ctr = reinterpret_cast<unsigned *>(C.arena + C.off_flushctr) + unit;
+    unsigned prev;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(prev) : "l"(ctr) : "memory");
+    if (prev == (unsigned)(C.h_kv - 1)) {
+      *ctr = 0u;
+      if (nk >= 0 && nk <= C.omega) meta[M_FLUSHT] = T;
+    }
+  }
+}
+
+cudaError_t launch_flush(const CacheDev &C, cudaStream_t s) {
+  flush_kernel<<<dim3(C.h_kv, C.B, C.L), 256, (size_t)C.omega * 16 * sizeof(float), s>>>(C, 1.0f / (float)C.h_q);
+  return cudaGetLastError();
+}
+
 }  // namespace qv

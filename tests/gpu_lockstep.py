@@ -29,7 +29,9 @@ def close_rel(gpu, ref, what, rel=REL_TOL, floor_frac=1e-6, abs_small=1e-9):
 
 
 class Lockstep:
-    def __init__(self, wl, check_state=True, oracle_prefill_scores=True, layers=None):
+    def __init__(self, wl, check_state=True, oracle_prefill_scores=True, layers=None, per_step=True):
+        """per_step: flush the scores after every decode step and check that step's window masses;
+        otherwise scores absorb the steps' masses only inside route(), checked after routing."""
         self.wl = wl
         self.cfg = binding.make_config(wl)
         self.cache = binding.Cache(self.cfg)
@@ -46,6 +48,7 @@ class Lockstep:
         self.step = 0
         self.oracle_prefill_scores = oracle_prefill_scores
         self.max_out_err = 0.0
+        self.per_step = per_step
 
     # ---- views of one unit's state
     def _u(self, l, b):
@@ -169,17 +172,16 @@ class Lockstep:
                 v = torch.stack([self.dec[(l, b)]["v"][s] for b in range(self.B)]).cuda()
                 out = torch.empty(self.B, wl.h_q, 128, dtype=torch.bfloat16, device="cuda")
                 saved = {}
-                for b in range(self.B):   # zero the score partials so this step's masses can be read alone
-                    reg = self.cache.region("score", self._u(l, b), 4 * H * self.N)
-                    saved[b] = reg.clone()
-                    reg.zero_()
+                if self.per_step:
+                    for b in range(self.B):   # zero the score partials so this step's masses can be read alone
+                        reg = self.cache.region("score", self._u(l, b), 4 * H * self.N)
+                        saved[b] = reg.clone()
+                        reg.zero_()
                 self.cache.decode_step(l, q, k, v, out)
+                if self.per_step:
+                    self.cache.flush_scores()   # scores absorb this step's masses
                 torch.cuda.synchronize()
                 for b in range(self.B):
-                    reg = self.cache.region("score", self._u(l, b), 4 * H * self.N)
-                    delta = reg.view(torch.float32).view(H, self.N).clone()
-                    base = saved[b].view(torch.float32).view(H, self.N)
-                    reg.view(torch.float32).view(H, self.N).copy_(base + delta)   # what the kernel adds
                     u = self.units[(l, b)]
                     o_ref, masses, sink = u.decode_step(self.dec[(l, b)]["q"][s].float().numpy(),
                                                         self.dec[(l, b)]["k"][s].float().numpy(),
@@ -189,6 +191,13 @@ class Lockstep:
                         err = np.abs(o - o_ref).max()
                         self.max_out_err = max(self.max_out_err, float(err))
                         assert err <= OUT_TOL, f"step {s + 1} layer {l} seq {b}: output max-abs err {err:.3e}"
+                    if not self.per_step:
+                        continue
+                    reg = self.cache.region("score", self._u(l, b), 4 * H * self.N)
+                    delta = reg.view(torch.float32).view(H, self.N).clone()
+                    base = saved[b].view(torch.float32).view(H, self.N)
+                    reg.view(torch.float32).view(H, self.N).copy_(base + delta)   # what the kernel adds
+                    if l in self.layers:
                         gm = delta.sum(dim=0).cpu().numpy().astype(np.float64)
                         close_rel(gm[:len(u.S)], masses.sum(axis=0)[:self.N] / wl.h_q,
                                   f"step {s + 1} layer {l} seq {b} window masses")
@@ -199,18 +208,21 @@ class Lockstep:
 
     def route(self):
         # scores before routing: sum of the KV-head partials, against the oracle's cumulative S
-        for l in self.layers:
-            for b in range(self.B):
-                sg = self.scores(l, b).astype(np.float32)
-                tot = sg[0].copy()
-                for g in range(1, sg.shape[0]):
-                    tot = (tot + sg[g]).astype(np.float32)
-                close_rel(tot, self.units[(l, b)].S[:self.N], f"scores before event {self.step} layer {l} seq {b}")
-        self.cache.route()
+        if self.per_step:
+            for l in self.layers:
+                for b in range(self.B):
+                    sg = self.scores(l, b).astype(np.float32)
+                    tot = sg[0].copy()
+                    for g in range(1, sg.shape[0]):
+                        tot = (tot + sg[g]).astype(np.float32)
+                    close_rel(tot, self.units[(l, b)].S[:self.N], f"scores before event {self.step} layer {l} seq {b}")
+        self.cache.route()   # absorbs the pending steps' masses, then ranks on the collapsed scores
         torch.cuda.synchronize()
         for l in range(self.L):
             for b in range(self.B):
                 s0 = self.scores(l, b)[0]
+                if not self.per_step and l in self.layers:
+                    close_rel(s0, self.units[(l, b)].S[:self.N], f"scores at event {self.step} layer {l} seq {b}")
                 self.units[(l, b)].route(scores=s0.astype(np.float64))
         if self.check_state:
             for l in self.layers:

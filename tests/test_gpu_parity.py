@@ -42,6 +42,14 @@ def test_edge_shapes(lib, shape):
     _run(base.replace(**shape), 24)
 
 
+def test_scores_absorbed_only_at_routing(lib):
+    """Window masses of Omega decode steps absorbed by the router's own flush, no flush in between,
+    reach the oracle's per-step cumulative scores (QEvict §4.2 Eq. (1))."""
+    base = synth.workload("tiny_4k", prompt_len=1500, steps=32, n_plant=4)
+    _run(base, 32, per_step=False)
+    _run(base.replace(h_q=16, h_kv=2, batch=2, omega=5), 20, per_step=False)
+
+
 def test_two_tier_and_quantized_only(lib):
     """q = 0: Full/Evicted only (two-tier window eviction); q = 1: K_f = 0 (quantised retention)."""
     base = synth.workload("tiny_4k", prompt_len=1200, steps=16, n_plant=4)
