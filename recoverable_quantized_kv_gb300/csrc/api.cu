@@ -147,7 +147,7 @@ void make_plan(const qevict_config *c, const qevict_budget_info *b, Plan *p) {
   C.off_counters = global(8LL * qv::N_COUNTERS * U);
   C.off_status = global(256);
   C.off_splitctr = global(4LL * c->n_layers * c->batch * c->h_kv);
-  C.off_headctr = global(4LL * c->n_layers * c->batch);
+  C.off_thead = global(4LL * c->n_layers * c->batch * c->h_kv);
   C.st_part_layer = align256(4LL * c->batch * c->h_kv * n_split * qv::PART_FLOATS);
   C.off_part = global(C.st_part_layer * c->n_layers);
   C.st_mu_layer = align256(4LL * c->batch * c->h_kv * c->omega * max_items * 8);

@@ -27,7 +27,8 @@ struct CacheDev {
   int64_t off_counters;            // int64 [U][N_COUNTERS]
   int64_t off_status;              // int32
   int64_t off_splitctr;            // uint32 [L][B][h_kv]
-  int64_t off_headctr;             // uint32 [L][B]
+  int64_t off_thead;               // int32 [L][B][h_kv] tokens cached, one copy per KV head: the decode
+                                   // CTAs of a head read theirs, its last CTA advances it
   int64_t off_part, st_part_layer; // float [L][B][h_kv][n_split][PART_FLOATS]
   // per-window log2-sum-exp of the decode steps since the last score flush, by step slot
   // (tokens cached at the step minus those at the flush) and stable item index

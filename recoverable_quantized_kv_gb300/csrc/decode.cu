@@ -20,7 +20,7 @@ namespace qv {
 
 constexpr int DEC_WARPS = 16;          // 15 consumer warps + 1 producer warp
 constexpr int DEC_CONSUMERS = DEC_WARPS - 1;
-constexpr int DEC_SLOTS = 44;          // CTA-wide ring of 4 KB slots filled by bulk copies
+constexpr int DEC_SLOTS = 36;          // CTA-wide ring of 4 KB slots filled by bulk copies
 constexpr int DEC_STAGE_BYTES = 4096;
 constexpr int DEC_MAX_CHUNKS = 4;      // chunks of one window (a bf16 window: 2 K + 2 V)
 // Consumers take windows from a queue, so a consumer can wait on a chunk up to
@@ -33,7 +33,10 @@ constexpr int DEC_FULL = DEC_PHASES * DEC_SLOTS;
 constexpr int DEC_TBL_BYTES = 1024;    // per consumer warp key lookup tables: 8 k-steps x 4 lane classes x 32 B
 constexpr int DEC_TBL_OFF = DEC_SLOTS * DEC_STAGE_BYTES;
 constexpr int DEC_BAR_OFF = DEC_TBL_OFF + DEC_CONSUMERS * DEC_TBL_BYTES;
-constexpr int DEC_SMEM = DEC_BAR_OFF + (DEC_FULL + DEC_SLOTS) * 8;
+constexpr int DEC_MRG_OFF = DEC_BAR_OFF + (DEC_FULL + DEC_SLOTS) * 8;
+// CTA merge: running max / sum / rescale per (warp, head), CTA max, and every warp's outputs
+constexpr int DEC_MRG_FLOATS = 3 * DEC_CONSUMERS * 8 + 16 + DEC_CONSUMERS * 128 * 8;
+constexpr int DEC_SMEM = DEC_MRG_OFF + DEC_MRG_FLOATS * 4;
 
 // Work list of one (sequence, KV head): item 0 = the sink tokens, items 1..nL = recent windows
 // j0 .. j0+nL-1, then the F-table entries, then the Q-table entries.  Item costs are the bytes
@@ -195,13 +198,14 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   // Programmatic dependent launch.  This kernel may start while the previous kernel in the stream
   // (the decode of another layer) finishes; that kernel writes only its own layer's state, and every
   // kernel before it has completed (each decode kernel lets its successor start only after its own
-  // wait below).  So this layer's tables and windows can be read and prefetched right away, and
-  // only the step's inputs (q, k_new, v_new) wait.  When the previous decode was the same layer,
+  // wait below).  So this layer's meta record and tables can be read right away; the window copies
+  // and the step's inputs (q, k_new, v_new) wait.  When the previous decode was the same layer,
   // wait first.
   if (io.wait_first) asm volatile("griddepcontrol.wait;" ::: "memory");
   int *status = C.status();
   int *meta = C.at<int>(C.off_meta, C.st_meta, unit);
-  const int T = meta[M_T], n_route = meta[M_NROUTE], nF = meta[M_FCOUNT], nQ = meta[M_QCOUNT];
+  int *thead = reinterpret_cast<int *>(C.arena + C.off_thead) + (size_t)unit * C.h_kv + g;
+  const int T = *thead, n_route = meta[M_NROUTE], nF = meta[M_FCOUNT], nQ = meta[M_QCOUNT];
   // this step's slot in the per-step mass records: steps since the scores last absorbed them
   int mslot = T - meta[M_FLUSHT];
   if (mslot < 0 || mslot >= C.omega) {
@@ -314,7 +318,11 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   if (producer) {
     // ---------------- producer warp: lane l issues chunk base + l of every batch of 32; a chunk
     // reuses its slot once the consumer of the chunk DEC_SLOTS earlier has released it
-    bool waited = io.wait_first;
+    // The step's inputs come from the previous kernel in a model, and that kernel's last CTAs are
+    // still merging when this one starts: a burst of window copies now would slow their loads
+    // more than it would gain here.  So the copies start once the previous kernel has completed.
+    if (!io.wait_first) asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     int done = n_total;           // chunks before this one were all issued
     bool mine = false;            // this lane issued its chunk of the batch that stopped early
     for (int base = 0; base < n_total; base += 32) {
@@ -333,20 +341,12 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
           mine = true;
         }
       }
-      // the step's inputs come from the previous kernel in a model: wait for it once the first
-      // batch is in flight, then let the next kernel start
-      if (!waited) {
-        asm volatile("griddepcontrol.wait;" ::: "memory");
-        waited = true;
-      }
       if (!__all_sync(0xffffffffu, good)) {   // a wait ran out: stop issuing
         done = base;
         break;
       }
       mine = false;
     }
-    if (!waited) asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // no copy may still be landing when the CTA ends.  Every earlier chunk of a slot landed before
     // the slot was reused, so only the last DEC_SLOTS chunks issued in order (and those of a batch
     // that stopped early) can still be in flight; none of them shares a barrier phase with another.
@@ -598,10 +598,10 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   }
   }   // consumer warps
 
-  // ---------------- merge the consumer warps of this CTA into one split partial
-  __syncthreads();
+  // ---------------- merge the consumer warps of this CTA into one split partial; each consumer
+  // warp stores its state as soon as its queue runs dry, into a region of its own
   const int lgG = __ffs(G) - 1;
-  float *cm = reinterpret_cast<float *>(smem);   // [DEC_CONSUMERS][8] running max
+  float *cm = reinterpret_cast<float *>(smem + DEC_MRG_OFF);   // [DEC_CONSUMERS][8] running max
   float *cl = cm + DEC_CONSUMERS * 8;            // [DEC_CONSUMERS][8] running sum
   float *cf = cl + DEC_CONSUMERS * 8;            // [DEC_CONSUMERS][8] rescale factor to the CTA max
   float *sM = cf + DEC_CONSUMERS * 8;            // [16] CTA max per head, then the merged max and 1/L
@@ -623,7 +623,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
       }
     }
   }
-  __syncthreads();
+  __syncthreads();   // also: every bulk copy into the slot ring has landed (producer drain)
   if (threadIdx.x < DEC_CONSUMERS * 8) {
     const int h = threadIdx.x & 7;
     float M = -INFINITY;
@@ -703,16 +703,12 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
       ms[8 + h] = inv;
     }
   }
-  __syncthreads();
+  // every CTA of this KV head has read T and arrived: the head's copy of T advances (head 0's also
+  // in the unit's meta record, which the router and the score flush read)
   if (threadIdx.x == 0) {
     *splitctr = 0u;
-    unsigned *headctr = reinterpret_cast<unsigned *>(C.arena + C.off_headctr) + (size_t)io.layer * C.B + b;
-    unsigned prev;
-    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(prev) : "l"(headctr) : "memory");
-    if (prev == (unsigned)(C.h_kv - 1)) {
-      *headctr = 0u;
-      meta[M_T] = T + 1;     // every CTA of this unit has read T by now
-    }
+    *thead = T + 1;
+    if (g == 0) meta[M_T] = T + 1;
   }
 }
 

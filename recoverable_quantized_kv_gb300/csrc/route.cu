@@ -520,6 +520,7 @@ __global__ void prefill_setup_kernel(const CacheDev C, const PromptIO pio, const
     ring[((size_t)(g * 2 + 0) * C.ring_windows + rs) * Gm::BLK + fnk_index(tok, d)] = pio.k[o];
     ring[((size_t)(g * 2 + 1) * C.ring_windows + rs) * Gm::BLK + fnv_index(tok, d)] = pio.v[o];
   }
+  if (threadIdx.x == 0) reinterpret_cast<int *>(C.arena + C.off_thead)[(size_t)unit * C.h_kv + g] = P;
   if (g == 0) {
     float *score = C.at<float>(C.off_score, C.st_score, unit);
     for (int w = threadIdx.x; w < npw; w += blockDim.x) score[w] = s0[(size_t)b * npw + w];
