@@ -217,6 +217,37 @@ qevict_status qevict_prefill_scores_noalloc(int32_t batch, int32_t prompt_len, i
                                             int32_t n_sink, int32_t window, const void *q_prompt,
                                             const void *k_prompt, float *s0_out, qevict_stream_t stream);
 
+/* Device views of one unit's cache tuple, QEvict §4.1 Eq. (2): C_t = (S, L_t, F_t, Q_t, E_t) of
+ * (layer, seq).  Each pointer is the unit's region inside the arena, with the layout documented
+ * with the layout struct above; E_t is the set of windows whose state tier is 3.  Host only;
+ * nothing is enqueued. */
+typedef struct {
+  void *sink;        /* S:   [h_kv][2][n_sink][d] bf16 */
+  void *ring;        /* L_t: recent windows, fragment-native bf16 blocks */
+  void *fpool;       /* F_t data: [k_f][h_kv][2][window*d] fragment-native bf16 */
+  void *ledger;      /* Q_t data and dormant ledgers: [k_f+k_q][h_kv][qblock] */
+  float *score;      /* [h_kv][n_windows] per-KV-head partial scores */
+  uint8_t *state;    /* [n_windows] tier (bits 0-1) and ledger status (bits 2-3) */
+  int32_t *f_slot;   /* [n_windows] F-pool slot or -1 */
+  int32_t *l_slot;   /* [n_windows] ledger slot or -1 */
+  int32_t *f_table;  /* [k_f] (window id, F slot), ascending window id; meta[2] entries valid */
+  int32_t *q_table;  /* [k_q] (window id, ledger slot), ascending window id; meta[3] entries valid */
+  int32_t *meta;     /* [16]: [0] T, [1] windows routed, [2] f_count, [3] q_count, [6] routing events,
+                        [7] T when the scores last absorbed the decode steps' masses */
+} qevict_tuple;
+qevict_status qevict_get_tuple(const qevict_cache *cache, int32_t layer, int32_t seq, qevict_tuple *out);
+
+/* Checkpoint / resume (the paper has none; an interface for serving systems).  The export is a
+ * header (format tag, the cache configuration, the arena size) followed by a byte copy of the whole
+ * arena, pending decode-step mass records and counters included, written to HOST memory.
+ * qevict_export_bytes gives its size.  qevict_export_state synchronises `stream` after the copy
+ * (QEVICT_ENOMEM when `bytes` is too small).  qevict_import_state loads an export into a cache
+ * created with the identical configuration (else QEVICT_EINVAL), synchronises `stream`, and resumes
+ * its host bookkeeping (per-layer T, routing events) from the imported meta records. */
+qevict_status qevict_export_bytes(const qevict_cache *cache, size_t *bytes);
+qevict_status qevict_export_state(const qevict_cache *cache, void *host_buf, size_t bytes, qevict_stream_t stream);
+qevict_status qevict_import_state(qevict_cache *cache, const void *host_buf, size_t bytes, qevict_stream_t stream);
+
 /* Frees the host handle (the arena stays the caller's). */
 qevict_status qevict_destroy(qevict_cache *cache);
 

@@ -44,6 +44,12 @@ class Layout(ctypes.Structure):
                [("qblock", ctypes.c_int64), ("arena_bytes", ctypes.c_int64), ("n_split", ctypes.c_int32)]
 
 
+class Tuple(ctypes.Structure):
+    """Device views of one (layer, sequence) cache tuple (qevict_tuple)."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("sink", "ring", "fpool", "ledger", "score", "state", "f_slot",
+                                               "l_slot", "f_table", "q_table", "meta")]
+
+
 _lib = None
 
 
@@ -66,6 +72,10 @@ def load() -> ctypes.CDLL:
         "qevict_decode_step": [P, I32, P, P, P, P, P],
         "qevict_route": [P, P],
         "qevict_flush_scores": [P, P],
+        "qevict_get_tuple": [P, I32, I32, ctypes.POINTER(Tuple)],
+        "qevict_export_bytes": [P, ctypes.POINTER(ctypes.c_size_t)],
+        "qevict_export_state": [P, P, ctypes.c_size_t, P],
+        "qevict_import_state": [P, P, ctypes.c_size_t, P],
         "qevict_read_counters": [P, ctypes.POINTER(I64), P],
         "qevict_check": [P, P],
         "qevict_destroy": [P],
@@ -86,7 +96,8 @@ def exported_symbols():
     return ["qevict_budget", "qevict_cache_bytes", "qevict_init_cache", "qevict_get_layout",
             "qevict_prefill_scores", "qevict_prefill_route", "qevict_decode_step", "qevict_route",
             "qevict_read_counters", "qevict_check", "qevict_destroy", "qevict_status_string",
-            "qevict_prefill_scores_noalloc", "qevict_flush_scores"]
+            "qevict_prefill_scores_noalloc", "qevict_flush_scores", "qevict_get_tuple", "qevict_export_bytes",
+            "qevict_export_state", "qevict_import_state"]
 
 
 def _check(status: int, where: str):
@@ -179,6 +190,28 @@ class Cache:
 
     def flush_scores(self, stream=None):
         _check(load().qevict_flush_scores(self.handle, _stream(stream)), "qevict_flush_scores")
+
+    def tuple(self, layer: int, seq: int) -> Tuple:
+        t = Tuple()
+        _check(load().qevict_get_tuple(self.handle, layer, seq, ctypes.byref(t)), "qevict_get_tuple")
+        return t
+
+    def export_state(self, stream=None):
+        """Checkpoint of the whole cache as a host uint8 numpy array (synchronises the stream)."""
+        import numpy as np
+        n = ctypes.c_size_t()
+        _check(load().qevict_export_bytes(self.handle, ctypes.byref(n)), "qevict_export_bytes")
+        buf = np.empty(n.value, dtype=np.uint8)
+        _check(load().qevict_export_state(self.handle, buf.ctypes.data, buf.nbytes, _stream(stream)),
+               "qevict_export_state")
+        return buf
+
+    def import_state(self, buf, stream=None):
+        """Loads a checkpoint made by export_state of a cache with the same configuration."""
+        import numpy as np
+        buf = np.ascontiguousarray(buf, dtype=np.uint8)
+        _check(load().qevict_import_state(self.handle, buf.ctypes.data, buf.nbytes, _stream(stream)),
+               "qevict_import_state")
 
     def counters(self, stream=None) -> dict:
         buf = (ctypes.c_int64 * 7)()

@@ -378,6 +378,84 @@ qevict_status qevict_check(qevict_cache *cache, qevict_stream_t stream) {
   return st;
 }
 
+qevict_status qevict_get_tuple(const qevict_cache *cache, int32_t layer, int32_t seq, qevict_tuple *out) {
+  if (!cache || !out || layer < 0 || layer >= cache->cfg.n_layers || seq < 0 || seq >= cache->cfg.batch)
+    return QEVICT_EINVAL;
+  const qv::CacheDev &C = cache->dev;
+  const int u = layer * cache->cfg.batch + seq;
+  out->sink = C.at<uint8_t>(C.off_sink, C.st_sink, u);
+  out->ring = C.at<uint8_t>(C.off_ring, C.st_ring, u);
+  out->fpool = C.at<uint8_t>(C.off_fpool, C.st_fpool, u);
+  out->ledger = C.at<uint8_t>(C.off_ledger, C.st_ledger, u);
+  out->score = C.at<float>(C.off_score, C.st_score, u);
+  out->state = C.at<uint8_t>(C.off_state, C.st_state, u);
+  out->f_slot = C.at<int32_t>(C.off_fslot, C.st_fslot, u);
+  out->l_slot = C.at<int32_t>(C.off_lslot, C.st_lslot, u);
+  out->f_table = C.at<int32_t>(C.off_ftab, C.st_ftab, u);
+  out->q_table = C.at<int32_t>(C.off_qtab, C.st_qtab, u);
+  out->meta = C.at<int32_t>(C.off_meta, C.st_meta, u);
+  return QEVICT_OK;
+}
+
+namespace {
+struct ExportHeader {
+  char magic[8];
+  int64_t arena_bytes;
+  qevict_config cfg;
+};
+constexpr char kExportMagic[8] = {'Q', 'E', 'V', 'I', 'C', 'T', 'S', '1'};
+}  // namespace
+
+qevict_status qevict_export_bytes(const qevict_cache *cache, size_t *bytes) {
+  if (!cache || !bytes) return QEVICT_EINVAL;
+  *bytes = sizeof(ExportHeader) + (size_t)cache->lay.arena_bytes;
+  return QEVICT_OK;
+}
+
+qevict_status qevict_export_state(const qevict_cache *cache, void *host_buf, size_t bytes, qevict_stream_t stream) {
+  if (!cache || !host_buf) return QEVICT_EINVAL;
+  if (bytes < sizeof(ExportHeader) + (size_t)cache->lay.arena_bytes) return QEVICT_ENOMEM;
+  ExportHeader h;
+  std::memset(&h, 0, sizeof(h));
+  std::memcpy(h.magic, kExportMagic, sizeof(h.magic));
+  h.arena_bytes = cache->lay.arena_bytes;
+  h.cfg = cache->cfg;
+  std::memcpy(host_buf, &h, sizeof(h));
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(static_cast<uint8_t *>(host_buf) + sizeof(h), cache->dev.arena, (size_t)h.arena_bytes,
+                      cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return QEVICT_ECUDA;
+  return QEVICT_OK;
+}
+
+qevict_status qevict_import_state(qevict_cache *cache, const void *host_buf, size_t bytes, qevict_stream_t stream) {
+  if (!cache || !host_buf || bytes < sizeof(ExportHeader)) return QEVICT_EINVAL;
+  ExportHeader h;
+  std::memcpy(&h, host_buf, sizeof(h));
+  if (std::memcmp(h.magic, kExportMagic, sizeof(h.magic)) != 0 || h.arena_bytes != cache->lay.arena_bytes ||
+      std::memcmp(&h.cfg, &cache->cfg, sizeof(qevict_config)) != 0 ||
+      bytes < sizeof(ExportHeader) + (size_t)h.arena_bytes)
+    return QEVICT_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(cache->dev.arena, static_cast<const uint8_t *>(host_buf) + sizeof(h), (size_t)h.arena_bytes,
+                      cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return QEVICT_ECUDA;
+  // host bookkeeping follows the imported meta records: a layer is prefilled once T > 0
+  const int L = cache->cfg.n_layers;
+  const uint8_t *arena = static_cast<const uint8_t *>(host_buf) + sizeof(h);
+  for (int l = 0; l < L; ++l) {
+    int32_t m[qv::META_INTS];
+    std::memcpy(m, arena + cache->dev.off_meta + cache->dev.st_meta * (int64_t)(l * cache->cfg.batch), sizeof(m));
+    cache->prefilled[l] = m[qv::M_T] > 0 ? 1 : 0;
+    cache->t_host[l] = m[qv::M_T];
+    if (m[qv::M_T] > 0) cache->routes_done = m[qv::M_NEVENT];
+  }
+  cache->last_decode_layer = -1;
+  return QEVICT_OK;
+}
+
 qevict_status qevict_destroy(qevict_cache *cache) {
   delete cache;
   return QEVICT_OK;

@@ -29,7 +29,7 @@ def close_rel(gpu, ref, what, rel=REL_TOL, floor_frac=1e-6, abs_small=1e-9):
 
 
 class Lockstep:
-    def __init__(self, wl, check_state=True, oracle_prefill_scores=True, layers=None, per_step=True):
+    def __init__(self, wl, check_state=True, oracle_prefill_scores=True, layers=None, per_step=True, state_seqs=None):
         """per_step: flush the scores after every decode step and check that step's window masses;
         otherwise scores absorb the steps' masses only inside route(), checked after routing."""
         self.wl = wl
@@ -49,6 +49,9 @@ class Lockstep:
         self.oracle_prefill_scores = oracle_prefill_scores
         self.max_out_err = 0.0
         self.per_step = per_step
+        # sequences whose full tier state / tables / window data are compared (outputs, masses, scores
+        # and counters are compared for every sequence)
+        self.state_seqs = list(range(self.B)) if state_seqs is None else state_seqs
 
     # ---- views of one unit's state
     def _u(self, l, b):
@@ -87,7 +90,7 @@ class Lockstep:
         torch.cuda.synchronize()
         if self.check_state:
             for l in self.layers:
-                for b in range(self.B):
+                for b in self.state_seqs:
                     self.compare_state(l, b)
 
     def _sink_share(self, ins):
@@ -226,7 +229,7 @@ class Lockstep:
                 self.units[(l, b)].route(scores=s0.astype(np.float64))
         if self.check_state:
             for l in self.layers:
-                for b in range(self.B):
+                for b in self.state_seqs:
                     self.compare_state(l, b)
 
     def counters(self):

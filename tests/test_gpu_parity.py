@@ -93,6 +93,24 @@ def test_full_size_llama_shape(lib):
     assert ls.max_out_err <= OUT_TOL
 
 
+@pytest.mark.parametrize("name,over,steps,check_state", [
+    # 16 sequences of the 32K shape: 128 (sequence, KV head) units, 2 splits each
+    ("batched_32k", dict(n_layers=1, steps=16), 16, True),
+    # 131K prompt, lognormal per-window key scales (INT2, 20%, q = 0.7): outputs, masses and the
+    # transition counters of every unit every step; tier-state dumps are skipped at this size
+    ("long_131k", dict(n_layers=1, batch=2, steps=8), 8, False),
+    # random-walk queries, 12.5% budget, 256 recent tokens, batch 8: three routing events
+    ("drift_16k", dict(n_layers=1, steps=24), 24, True),
+])
+def test_full_size_workloads(lib, name, over, steps, check_state):
+    """The other workloads at their full per-layer shapes (one layer each), in lockstep: outputs,
+    window masses, scores and counters of every sequence; full state of the first, middle and last."""
+    wl = synth.workload(name, **over)
+    seqs = sorted({0, wl.batch // 2, wl.batch - 1})
+    ls = _run(wl, steps, oracle_prefill_scores=False, check_state=check_state, state_seqs=seqs)
+    assert ls.max_out_err <= OUT_TOL
+
+
 def test_status_codes(lib):
     wl = synth.workload("tiny_4k", prompt_len=600, steps=16, n_plant=2, budget_num=60)
     cfg = binding.make_config(wl)
@@ -130,3 +148,50 @@ def test_status_codes(lib):
     c.route()
     c.decode_step(0, q, kv, kv, out)
     c.check()
+
+
+def test_tuple_views_and_checkpoint(lib):
+    """qevict_get_tuple points at each unit's regions; an exported cache imported into a fresh arena
+    resumes the run: the same next steps and routing event as the original cache."""
+    wl = synth.workload("tiny_4k", prompt_len=1200, steps=32, n_plant=4, batch=2)
+    ls = Lockstep(wl)
+    ls.prefill()
+    ls.decode(10)                      # one routing event, then two steps with pending masses
+    cache, lay = ls.cache, ls.cache.layout
+    base = cache.arena.data_ptr()
+    for layer in range(wl.n_layers):
+        for b in range(wl.batch):
+            t = cache.tuple(layer, b)
+            u = layer * wl.batch + b
+            for name, region in (("sink", "sink"), ("ring", "ring"), ("fpool", "fpool"), ("ledger", "ledger"),
+                                 ("score", "score"), ("state", "state"), ("f_slot", "fslot"), ("l_slot", "lslot"),
+                                 ("f_table", "ftab"), ("q_table", "qtab"), ("meta", "meta")):
+                assert getattr(t, name) == base + getattr(lay, f"off_{region}") + u * getattr(lay, f"stride_{region}")
+    snap = cache.export_state()
+    twin = binding.Cache(ls.cfg)
+    twin.import_state(snap)
+    assert np.array_equal(twin.export_state(), snap)
+    with pytest.raises(binding.QEvictError):   # a different configuration is refused
+        other = binding.Cache(binding.make_config(wl.replace(omega=4)))
+        other.import_state(snap)
+    # both caches take the same six steps (a routing event after the sixth)
+    outs = {}
+    for name, c in (("orig", cache), ("twin", twin)):
+        res = []
+        for s in range(10, 16):
+            for layer in range(wl.n_layers):
+                d = [ls.dec[(layer, b)] for b in range(wl.batch)]
+                q = torch.stack([x["q"][s] for x in d]).cuda()
+                k = torch.stack([x["k"][s] for x in d]).cuda()
+                v = torch.stack([x["v"][s] for x in d]).cuda()
+                out = torch.empty(wl.batch, wl.h_q, 128, dtype=torch.bfloat16, device="cuda")
+                c.decode_step(layer, q, k, v, out)
+                res.append(out.float().cpu())
+        c.route()
+        torch.cuda.synchronize()
+        outs[name] = torch.stack(res)
+    assert (outs["orig"] - outs["twin"]).abs().max().item() <= 1e-2
+    for region in ("state", "fslot", "lslot", "ftab", "qtab", "meta"):
+        n = getattr(lay, f"stride_{region}")
+        for u in range(wl.n_layers * wl.batch):
+            assert torch.equal(cache.region(region, u, n), twin.region(region, u, n)), region
