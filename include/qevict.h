@@ -108,6 +108,11 @@ typedef struct {
  *   V element (tok, dim): with r = dim%16, c = tok%16, lane and reg as above, i = dim/16,
  *     rr = (i%2)*4 + reg, word w = (tok/16)*4 + i/2 (lane bytes 4w .. 4w+3, little-endian),
  *     bit = (rr < 5 ? 2*rr : 10 + 2*(rr-5)) + 16*(tok%2) inside that word.
+ * Fragment-native INT4 codes (W = 64; 4 KB per K or V block): one little-endian 32-bit word per
+ * (16x16 tile, lane), tile = (tok/16)*8 + dim/16, stored at word ((tile/4)*32 + lane)*4 + tile%4.
+ *   K element (tok, dim): r = tok%16, c = dim%16, lane and reg as above, bits 4*(reg*2 + dim%2).
+ *   V element (tok, dim): r = dim%16, c = tok%16, lane and reg as above, bits 4*reg + 16*(tok%2).
+ * A W = 64 ledger record (qblock 8960 B) is K codes | V codes | parameters, each code block 4 KB.
  */
 typedef struct {
   int64_t off_sink, stride_sink;

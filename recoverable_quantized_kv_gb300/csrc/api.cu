@@ -60,7 +60,7 @@ qevict_status check_config(const qevict_config *c) {
   const int G = c->h_q / c->h_kv;
   if (G != 1 && G != 2 && G != 4 && G != 8) return QEVICT_EINVAL;
   if (c->d_head != D) return QEVICT_EINVAL;
-  if (!(c->window == 32 && c->bits == 2)) return QEVICT_EINVAL;
+  if (!((c->window == 32 && c->bits == 2) || (c->window == 64 && c->bits == 4))) return QEVICT_EINVAL;
   if (c->n_sink < 1 || c->n_sink > 16 || c->n_recent < c->window || c->omega < 1 ||
       c->omega > 256)
     return QEVICT_EINVAL;

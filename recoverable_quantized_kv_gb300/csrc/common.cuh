@@ -71,6 +71,30 @@ __host__ __device__ __forceinline__ void code_pos2(bool is_v, int tok, int dim, 
   shift = bit & 7;
 }
 
+// Position of the INT4 code of element (tok, dim) inside a window's K or V code block (4 KB for
+// W = 64): one 32-bit word per (16x16 tile, lane), tile = (tok/16)*8 + dim/16, stored at word
+// ((tile/4)*32 + lane)*4 + tile%4 (a lane's four consecutive tiles are one 128-bit load).
+//  K: element e = reg*2 + dim%2 of the lane's A registers sits at bits 4e.
+//  V: register reg's two codes (even, odd token) sit at bits 4*reg and 16 + 4*reg, so registers
+//     0, 1 (and 2, 3 after a shift by 8) are one mask away from fp16 mantissas.
+__host__ __device__ __forceinline__ void code_pos4(bool is_v, int tok, int dim, int &byte, int &shift) {
+  const int tile = (tok >> 4) * 8 + (dim >> 4);
+  const int r = is_v ? (dim & 15) : (tok & 15), c = is_v ? (tok & 15) : (dim & 15);
+  const int lane = frag_lane(r, c);
+  const int word = ((tile >> 2) * 32 + lane) * 4 + (tile & 3);
+  const int bit = is_v ? 4 * frag_reg(r, c) + 16 * (c & 1) : 4 * ((frag_reg(r, c) << 1) | (c & 1));
+  byte = word * 4 + (bit >> 3);
+  shift = bit & 7;
+}
+
+template <int BITS>
+__host__ __device__ __forceinline__ void code_pos(bool is_v, int tok, int dim, int &byte, int &shift) {
+  if (BITS == 2)
+    code_pos2(is_v, tok, dim, byte, shift);
+  else
+    code_pos4(is_v, tok, dim, byte, shift);
+}
+
 template <int W, int BITS>
 struct Geo {
   static constexpr int BLK = W * D;                     // elements of one K or V block

@@ -22,21 +22,34 @@ constexpr int DEC_WARPS = 16;          // 15 consumer warps + 1 producer warp
 constexpr int DEC_CONSUMERS = DEC_WARPS - 1;
 constexpr int DEC_SLOTS = 36;          // CTA-wide ring of 4 KB slots filled by bulk copies
 constexpr int DEC_STAGE_BYTES = 4096;
-constexpr int DEC_MAX_CHUNKS = 4;      // chunks of one window (a bf16 window: 2 K + 2 V)
-// Consumers take windows from a queue, so a consumer can wait on a chunk up to
-// DEC_CONSUMERS * DEC_MAX_CHUNKS chunks past the first one not yet issued.  Giving every slot
-// DEC_PHASES "full" barriers used in turn keeps every parity wait unambiguous: the chunk
-// DEC_PHASES * DEC_SLOTS earlier on the same barrier has always landed by then.
-constexpr int DEC_PHASES = 3;
-static_assert((DEC_PHASES - 1) * DEC_SLOTS >= DEC_CONSUMERS * DEC_MAX_CHUNKS, "too few full barriers per slot");
-constexpr int DEC_FULL = DEC_PHASES * DEC_SLOTS;
-constexpr int DEC_TBL_BYTES = 1024;    // per consumer warp key lookup tables: 8 k-steps x 4 lane classes x 32 B
+// per consumer warp: the key look-up table of the window in hand (INT2: bf16 bytes of the 4 values
+// of 128 channels; INT4: fp32 scale and offset of 128 channels), 8 k-steps x 4 lane classes x 32 B
+constexpr int DEC_TBL_BYTES = 1024;
 constexpr int DEC_TBL_OFF = DEC_SLOTS * DEC_STAGE_BYTES;
-constexpr int DEC_BAR_OFF = DEC_TBL_OFF + DEC_CONSUMERS * DEC_TBL_BYTES;
-constexpr int DEC_MRG_OFF = DEC_BAR_OFF + (DEC_FULL + DEC_SLOTS) * 8;
 // CTA merge: running max / sum / rescale per (warp, head), CTA max, and every warp's outputs
 constexpr int DEC_MRG_FLOATS = 3 * DEC_CONSUMERS * 8 + 16 + DEC_CONSUMERS * 128 * 8;
-constexpr int DEC_SMEM = DEC_MRG_OFF + DEC_MRG_FLOATS * 4;
+
+// Chunk stream geometry of one (window, bits) format.  A bf16 window streams its K block then its
+// V block in 4 KB chunks; a Quantized window streams its ledger record (codes, then parameters).
+// Consumers take windows from a queue, so a consumer can wait on a chunk up to
+// DEC_CONSUMERS * MAX_CHUNKS chunks past the first one not yet issued.  Giving every slot PHASES
+// "full" barriers used in turn keeps every parity wait unambiguous: the chunk PHASES * DEC_SLOTS
+// earlier on the same barrier has always landed by then.
+template <int W, int BITS>
+struct DecGeo {
+  static constexpr int HALVES = W / 32;                        // 32-token halves of a window
+  static constexpr int KCH = W / 16;                           // 4 KB chunks of one K (or V) block
+  static constexpr int BF_CHUNKS = 2 * KCH;
+  static constexpr int Q_CHUNKS = (Geo<W, BITS>::QB + DEC_STAGE_BYTES - 1) / DEC_STAGE_BYTES;
+  static constexpr int MAX_CHUNKS = BF_CHUNKS > Q_CHUNKS ? BF_CHUNKS : Q_CHUNKS;
+  static constexpr int PHASES = 1 + (DEC_CONSUMERS * MAX_CHUNKS + DEC_SLOTS - 1) / DEC_SLOTS;
+  static constexpr int FULL = PHASES * DEC_SLOTS;
+  static constexpr int BAR_OFF = DEC_TBL_OFF + DEC_CONSUMERS * DEC_TBL_BYTES;
+  static constexpr int MRG_OFF = BAR_OFF + (FULL + DEC_SLOTS) * 8;
+  static constexpr int SMEM = MRG_OFF + DEC_MRG_FLOATS * 4;
+  static_assert((PHASES - 1) * DEC_SLOTS >= DEC_CONSUMERS * MAX_CHUNKS, "too few full barriers per slot");
+  static_assert(W == 32 || Geo<W, BITS>::CODE_BYTES == DEC_STAGE_BYTES, "INT4 code blocks fill one chunk each");
+};
 
 // Work list of one (sequence, KV head): item 0 = the sink tokens, items 1..nL = recent windows
 // j0 .. j0+nL-1, then the F-table entries, then the Q-table entries.  Item costs are the bytes
@@ -170,6 +183,22 @@ __device__ __forceinline__ uint32_t dq_v(uint32_t w, int p) {
   return r;
 }
 
+// INT4 value codes as exact fp16 integers: the codes at nibble p (0 or 1) of both fp16 halves land
+// in the mantissas under exponent 2^10 (value 1024 + 16^p c); one packed fma recovers c.
+__device__ __forceinline__ uint32_t dq_v4(uint32_t w, int p) {
+  static constexpr uint32_t SCL[2] = {0x3C003C00u, 0x2C002C00u};   // 1, 1/16
+  static constexpr uint32_t OFF[2] = {0xE400E400u, 0xD400D400u};   // -1024, -64
+  const uint32_t x = (w & (0x000F000Fu << (4 * p))) | 0x64006400u;
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(SCL[p]), "r"(OFF[p]));
+  return r;
+}
+
+// Byte r of a word holding one 4-bit code per byte, as an exact float (mantissa of 2^23 + c).
+__device__ __forceinline__ float nib_f(uint32_t bytes4, int r) {
+  return __uint_as_float(__byte_perm(bytes4, 0x4B000000u, 0x7540u | r)) - 8388608.0f;
+}
+
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                         uint32_t b1) {
   asm volatile(
@@ -185,9 +214,12 @@ __device__ __forceinline__ uint32_t pack_half(float lo, float hi) {
 
 template <int W, int BITS>
 __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDev C, const DecodeIO io) {
-  static_assert(W == 32 && BITS == 2, "decode kernel instantiated for W=32, INT2");
+  static_assert((W == 32 && BITS == 2) || (W == 64 && BITS == 4), "formats: W=32 INT2, W=64 INT4");
   using Gm = Geo<W, BITS>;
-  constexpr int NMT = W / 16;
+  using Dg = DecGeo<W, BITS>;
+  constexpr int NMT = 2;                 // 16-token groups of a 32-token half
+  constexpr int HALVES = Dg::HALVES;
+  constexpr int KCH = Dg::KCH, BFC = Dg::BF_CHUNKS, QCH = Dg::Q_CHUNKS;
   extern __shared__ __align__(128) uint8_t smem[];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -248,36 +280,37 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
 
   uint8_t *slots = smem;
   uint8_t *tbl = smem + DEC_TBL_OFF + (warp < DEC_CONSUMERS ? warp : 0) * DEC_TBL_BYTES;
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + DEC_BAR_OFF);   // [DEC_FULL]
-  uint64_t *empty = full + DEC_FULL;                                    // [DEC_SLOTS]
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + Dg::BAR_OFF);   // [Dg::FULL]
+  uint64_t *empty = full + Dg::FULL;                                    // [DEC_SLOTS]
   __shared__ int q_next;    // next queue position to hand to a consumer warp
 
   // ---- chunk stream.  The CTA's windows in queue order [sink][recent][Full][Quantized]; a bf16
-  // window is NMT K chunks then NMT V chunks (4 KB each), a Quantized window one chunk, the sink
-  // none.  Chunk c lives in slot c % DEC_SLOTS and completes on full[c % DEC_FULL].
-  const int nb = (L1 - L0) + (F1 - F0);          // bf16 windows of this CTA
-  const int n_total = 2 * NMT * nb + (Q1 - Q0);  // chunks of this CTA
+  // window is KCH K chunks then KCH V chunks (4 KB each), a Quantized window QCH chunks of its
+  // ledger record, the sink none.  Chunk c lives in slot c % DEC_SLOTS and completes on
+  // full[c % Dg::FULL].
+  const int nb = (L1 - L0) + (F1 - F0);            // bf16 windows of this CTA
+  const int n_total = BFC * nb + QCH * (Q1 - Q0);  // chunks of this CTA
   auto chunk_start = [&](int pos) -> int {
     const int k = pos - has_sink;
     if (k <= 0) return 0;
-    return k <= nb ? 2 * NMT * k : 2 * NMT * nb + (k - nb);
+    return k <= nb ? BFC * k : BFC * nb + QCH * (k - nb);
   };
   // global source of chunk c
   auto chunk_src = [&](int c, const void *&src, uint32_t &bytes) {
     int pos, sub;
-    if (c < 2 * NMT * nb) {
-      pos = has_sink + c / (2 * NMT);
-      sub = c % (2 * NMT);
+    if (c < BFC * nb) {
+      pos = has_sink + c / BFC;
+      sub = c % BFC;
     } else {
-      pos = has_sink + nb + (c - 2 * NMT * nb);
-      sub = 0;
+      pos = has_sink + nb + (c - BFC * nb) / QCH;
+      sub = (c - BFC * nb) % QCH;
     }
     const int it = item_of(pos);
     if (it <= nL) {
       const int rs = (j0 + it - 1) % C.ring_windows;
       const __nv_bfloat16 *kb = ring + (size_t)rs * Gm::BLK;
       const __nv_bfloat16 *vb = ring + (size_t)(C.ring_windows + rs) * Gm::BLK;
-      src = sub < NMT ? (const void *)(kb + sub * 2048) : (const void *)(vb + (sub - NMT) * 2048);
+      src = sub < KCH ? (const void *)(kb + sub * 2048) : (const void *)(vb + (sub - KCH) * 2048);
       bytes = DEC_STAGE_BYTES;
     } else if (it <= nL + nF) {
       const int slot = __ldg(&ftab[it - 1 - nL].y);
@@ -285,8 +318,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
       bytes = DEC_STAGE_BYTES;
     } else {
       const int slot = __ldg(&qtab[it - 1 - nL - nF].y);
-      src = ledger + ((size_t)slot * C.h_kv + g) * Gm::QB;
-      bytes = Gm::QB;
+      src = ledger + ((size_t)slot * C.h_kv + g) * Gm::QB + (size_t)sub * DEC_STAGE_BYTES;
+      bytes = min(DEC_STAGE_BYTES, Gm::QB - sub * DEC_STAGE_BYTES);
     }
   };
   // the producer's first batch: one chunk per lane, its source looked up before the barrier
@@ -294,7 +327,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   const void *src0 = nullptr;
   uint32_t bytes0 = 0;
   if (producer && lane < n_total) chunk_src(lane, src0, bytes0);
-  if (threadIdx.x < DEC_FULL + DEC_SLOTS) {
+  if (threadIdx.x < Dg::FULL + DEC_SLOTS) {
     mbar_init(&full[threadIdx.x], 1);
     fence_mbar_init();
   }
@@ -308,7 +341,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
 
   bool ok = true;
   auto wait_chunk = [&](int c) -> const uint8_t * {
-    if (!mbar_wait(&full[c % DEC_FULL], (uint32_t)((c / DEC_FULL) & 1), status)) ok = false;
+    if (!mbar_wait(&full[c % Dg::FULL], (uint32_t)((c / Dg::FULL) & 1), status)) ok = false;
     return slots + (c % DEC_SLOTS) * DEC_STAGE_BYTES;
   };
   auto release_chunk = [&](int c) {
@@ -335,7 +368,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
         if (base > 0) chunk_src(c, src, bytes);
         if (c >= DEC_SLOTS) good = mbar_wait(&empty[c % DEC_SLOTS], (uint32_t)(((c / DEC_SLOTS) - 1) & 1), status);
         if (good) {
-          uint64_t *bar = &full[c % DEC_FULL];
+          uint64_t *bar = &full[c % Dg::FULL];
           mbar_arrive_expect_tx(bar, bytes);
           bulk_g2s(slots + (c % DEC_SLOTS) * DEC_STAGE_BYTES, src, bytes, bar);
           mine = true;
@@ -351,10 +384,10 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
     // the slot was reused, so only the last DEC_SLOTS chunks issued in order (and those of a batch
     // that stopped early) can still be in flight; none of them shares a barrier phase with another.
     for (int k = (done > DEC_SLOTS ? done - DEC_SLOTS : 0) + lane; k < done; k += 32)
-      mbar_wait(&full[k % DEC_FULL], (uint32_t)((k / DEC_FULL) & 1), status);
+      mbar_wait(&full[k % Dg::FULL], (uint32_t)((k / Dg::FULL) & 1), status);
     if (mine) {
       const int k = done + lane;
-      mbar_wait(&full[k % DEC_FULL], (uint32_t)((k / DEC_FULL) & 1), status);
+      mbar_wait(&full[k % Dg::FULL], (uint32_t)((k / Dg::FULL) & 1), status);
     }
     __syncwarp();
   } else {
@@ -413,95 +446,114 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
       continue;
     }
 
-    bool valid[NMT][2];
-    float s[NMT][4];
+    // log2-sum-exp of the window's logits per head, over its 32-token halves
+    float wmu[2] = {-INFINITY, -INFINITY};
+    auto add_half_mass = [&]() {
 #pragma unroll
-    for (int mt = 0; mt < NMT; ++mt) s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
+      for (int h = 0; h < 2; ++h) {
+        const float x = tsum[h] > 0.f ? m_run[h] + __log2f(tsum[h]) : -INFINITY;
+        const float hi = fmaxf(wmu[h], x), lo = fminf(wmu[h], x);
+        wmu[h] = lo == -INFINITY ? hi : hi + __log2f(1.f + exp2f(lo - hi));
+      }
+    };
 
     if (it <= nL + nF) {
-      // ---------------- bf16 window (recent or Full)
+      // ---------------- bf16 window (recent or Full), one 32-token half at a time
       const bool is_local = it <= nL;
       const int wid = j0 + it - 1;   // the recent window (meaningful only when is_local)
       const int newtok = (is_local && wid == jn) ? T - (C.n_sink + jn * W) : -1;
-      const uint8_t *kc[NMT];
+#pragma unroll 1
+      for (int hv = 0; hv < HALVES; ++hv) {
+        bool valid[NMT][2];
+        float s[NMT][4];
 #pragma unroll
-      for (int mt = 0; mt < NMT; ++mt) kc[mt] = wait_chunk(c0 + mt);
-      if (newtok >= 0 && ok) {
-        // append: the new token enters the recent ring (global) and this warp's staged copy
-        const int rs = jn % C.ring_windows;
-        __nv_bfloat16 *kb = ring + (size_t)rs * Gm::BLK;
-        const __nv_bfloat16 *kn = io.k_new + ((size_t)b * C.h_kv + g) * D;
-        uint8_t *kst = const_cast<uint8_t *>(kc[newtok >> 4]);
+        for (int mt = 0; mt < NMT; ++mt) s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
+        const bool patch = newtok >= 0 && (newtok >> 5) == hv;
+        const uint8_t *kc[NMT];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int d = 4 * lane + 2 * h;
-          const uint32_t pair = ldg32(kn + d);
-          const int idx = fnk_index(newtok, d);
-          *reinterpret_cast<uint32_t *>(kb + idx) = pair;
-          *reinterpret_cast<uint32_t *>(kst + (idx - (newtok >> 4) * 2048) * 2) = pair;
+        for (int mt = 0; mt < NMT; ++mt) kc[mt] = wait_chunk(c0 + 2 * hv + mt);
+        if (patch && ok) {
+          // append: the new token enters the recent ring (global) and this warp's staged copy
+          const int rs = jn % C.ring_windows;
+          __nv_bfloat16 *kb = ring + (size_t)rs * Gm::BLK;
+          const __nv_bfloat16 *kn = io.k_new + ((size_t)b * C.h_kv + g) * D;
+          uint8_t *kst = const_cast<uint8_t *>(kc[(newtok >> 4) & 1]);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int d = 4 * lane + 2 * h;
+            const uint32_t pair = ldg32(kn + d);
+            const int idx = fnk_index(newtok, d);
+            *reinterpret_cast<uint32_t *>(kb + idx) = pair;
+            *reinterpret_cast<uint32_t *>(kst + (idx - (newtok >> 4) * 2048) * 2) = pair;
+          }
+          fence_proxy_async();   // this generic write must precede the slot's next bulk copy
+          __syncwarp();
         }
-        fence_proxy_async();   // this generic write must precede the slot's next bulk copy
+#pragma unroll
+        for (int mt = 0; mt < NMT; ++mt) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint4 a = lds128(kc[mt] + (j * 32 + lane) * 16);
+            mma_bf16(s[mt], a.x, a.y, a.z, a.w, qb[j][0], qb[j][1]);
+          }
+        }
         __syncwarp();
-      }
 #pragma unroll
-      for (int mt = 0; mt < NMT; ++mt) {
+        for (int mt = 0; mt < NMT; ++mt) release_chunk(c0 + 2 * hv + mt);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint4 a = lds128(kc[mt] + (j * 32 + lane) * 16);
-          mma_bf16(s[mt], a.x, a.y, a.z, a.w, qb[j][0], qb[j][1]);
+        for (int mt = 0; mt < NMT; ++mt) {
+          const int tok0 = 32 * hv + 16 * mt + gl;
+          if (is_local) {
+            const int p0 = C.n_sink + wid * W + tok0;
+            valid[mt][0] = p0 <= T;
+            valid[mt][1] = p0 + 8 <= T;
+          } else {
+            valid[mt][0] = valid[mt][1] = true;
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) s[mt][k] *= io.scale_log2;
         }
-      }
-      __syncwarp();
+        online_step<NMT>(s, valid, m_run, l_run, o, macc, tsum);
+        uint32_t pb[NMT][2];
+        p_to_b<NMT>(s, pb);
+        const uint8_t *vc[NMT];
 #pragma unroll
-      for (int mt = 0; mt < NMT; ++mt) release_chunk(c0 + mt);
+        for (int kk = 0; kk < NMT; ++kk) vc[kk] = wait_chunk(c0 + KCH + 2 * hv + kk);
+        if (patch && ok) {
+          const int rs = jn % C.ring_windows;
+          __nv_bfloat16 *vb = ring + (size_t)(C.ring_windows + rs) * Gm::BLK;
+          const __nv_bfloat16 *vn = io.v_new + ((size_t)b * C.h_kv + g) * D;
+          uint8_t *vst = const_cast<uint8_t *>(vc[(newtok >> 4) & 1]);
 #pragma unroll
-      for (int mt = 0; mt < NMT; ++mt) {
-        const int tok0 = 16 * mt + gl;
-        if (is_local) {
-          const int p0 = C.n_sink + wid * W + tok0;
-          valid[mt][0] = p0 <= T;
-          valid[mt][1] = p0 + 8 <= T;
-        } else {
-          valid[mt][0] = valid[mt][1] = true;
+          for (int h = 0; h < 4; ++h) {
+            const int d = 4 * lane + h;
+            const unsigned short x = (unsigned short)ldg16(vn + d);
+            const int idx = fnv_index(newtok, d);
+            reinterpret_cast<unsigned short *>(vb)[idx] = x;
+            reinterpret_cast<unsigned short *>(vst)[idx - (newtok >> 4) * 2048] = x;
+          }
+          fence_proxy_async();
+          __syncwarp();
         }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) s[mt][k] *= io.scale_log2;
-      }
-      online_step<NMT>(s, valid, m_run, l_run, o, macc, tsum);
-      uint32_t pb[NMT][2];
-      p_to_b<NMT>(s, pb);
-      const uint8_t *vc[NMT];
+        for (int kk = 0; kk < NMT; ++kk) {
 #pragma unroll
-      for (int kk = 0; kk < NMT; ++kk) vc[kk] = wait_chunk(c0 + NMT + kk);
-      if (newtok >= 0 && ok) {
-        const int rs = jn % C.ring_windows;
-        __nv_bfloat16 *vb = ring + (size_t)(C.ring_windows + rs) * Gm::BLK;
-        const __nv_bfloat16 *vn = io.v_new + ((size_t)b * C.h_kv + g) * D;
-        uint8_t *vst = const_cast<uint8_t *>(vc[newtok >> 4]);
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          const int d = 4 * lane + h;
-          const unsigned short x = (unsigned short)ldg16(vn + d);
-          const int idx = fnv_index(newtok, d);
-          reinterpret_cast<unsigned short *>(vb)[idx] = x;
-          reinterpret_cast<unsigned short *>(vst)[idx - (newtok >> 4) * 2048] = x;
+          for (int i = 0; i < 8; ++i) {
+            const uint4 a = lds128(vc[kk] + (i * 32 + lane) * 16);
+            mma_bf16(o[i], a.x, a.y, a.z, a.w, pb[kk][0], pb[kk][1]);
+          }
         }
-        fence_proxy_async();
         __syncwarp();
+#pragma unroll
+        for (int kk = 0; kk < NMT; ++kk) release_chunk(c0 + KCH + 2 * hv + kk);
+        add_half_mass();
       }
+    } else if constexpr (BITS == 2) {
+      // ---------------- Quantized window, W = 32: INT2 codes + fp16 scale/offset in one chunk
+      bool valid[NMT][2];
+      float s[NMT][4];
 #pragma unroll
-      for (int kk = 0; kk < NMT; ++kk) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 a = lds128(vc[kk] + (i * 32 + lane) * 16);
-          mma_bf16(o[i], a.x, a.y, a.z, a.w, pb[kk][0], pb[kk][1]);
-        }
-      }
-      __syncwarp();
-#pragma unroll
-      for (int kk = 0; kk < NMT; ++kk) release_chunk(c0 + NMT + kk);
-    } else {
-      // ---------------- Quantized window: INT2 codes + fp16 scale/offset
+      for (int mt = 0; mt < NMT; ++mt) s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
       const uint8_t *ch = wait_chunk(c0);
       // key tables: channel d = 4*lane + k, values bf16(fp32(c*s + m)), c = 0..3, split in lo / hi bytes
       {
@@ -584,15 +636,106 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
       }
       __syncwarp();
       release_chunk(c0);
+      add_half_mass();
+    } else {
+      // ---------------- Quantized window, W = 64: INT4 codes; chunks K codes | V codes | parameters
+      const uint8_t *kch = wait_chunk(c0);
+      const uint8_t *vch = wait_chunk(c0 + 1);
+      const uint8_t *pch = wait_chunk(c0 + 2);
+      // per-channel fp32 (scale, offset) for the four channels 2t, 2t+1, 2t+8, 2t+9 of every
+      // (k-step j, lane class t): 8 floats, scales then offsets
+      {
+        const uint2 sp = *reinterpret_cast<const uint2 *>(pch + (Gm::OFF_KS - 2 * Gm::CODE_BYTES) + 8 * lane);
+        const uint2 mp = *reinterpret_cast<const uint2 *>(pch + (Gm::OFF_KM - 2 * Gm::CODE_BYTES) + 8 * lane);
+        float *tf = reinterpret_cast<float *>(tbl);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t sw = k < 2 ? sp.x : sp.y, mw = k < 2 ? mp.x : mp.y;
+          const int d = 4 * lane + k, j = d >> 4, c16 = d & 15;
+          const int t = (c16 & 7) >> 1, which = c16 >> 3, half = c16 & 1;
+          const int base = (j * 4 + t) * 8 + which * 2 + half;
+          tf[base] = (k & 1) ? h2f_hi(sw) : h2f_lo(sw);
+          tf[base + 4] = (k & 1) ? h2f_hi(mw) : h2f_lo(mw);
+        }
+      }
+      __syncwarp();
+      const __half *vsp = reinterpret_cast<const __half *>(pch + (Gm::OFF_VS - 2 * Gm::CODE_BYTES));
+      const __half *vmp = reinterpret_cast<const __half *>(pch + (Gm::OFF_VM - 2 * Gm::CODE_BYTES));
+#pragma unroll 1
+      for (int hv = 0; hv < HALVES; ++hv) {
+        bool valid[NMT][2];
+        float s[NMT][4];
+#pragma unroll
+        for (int mt = 0; mt < NMT; ++mt) s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
+        // keys: tile (token group tg, k-step j) is word ((tile/4)*32 + lane)*4 + tile%4 of the K codes
+#pragma unroll
+        for (int mt = 0; mt < NMT; ++mt) {
+          const int tg = 2 * hv + mt;
+          const uint4 w03 = lds128(kch + (((2 * tg) * 32 + lane) * 4) * 4);
+          const uint4 w47 = lds128(kch + (((2 * tg + 1) * 32 + lane) * 4) * 4);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t w = word_of(j < 4 ? w03 : w47, j & 3);
+            const uint32_t E = w & 0x0F0F0F0Fu, Od = (w >> 4) & 0x0F0F0F0Fu;
+            const float4 sc = *reinterpret_cast<const float4 *>(tbl + (j * 4 + tl) * 32);
+            const float4 mn = *reinterpret_cast<const float4 *>(tbl + (j * 4 + tl) * 32 + 16);
+            const uint32_t a0 = pack_bf16(__fmaf_rn(nib_f(E, 0), sc.x, mn.x), __fmaf_rn(nib_f(Od, 0), sc.y, mn.y));
+            const uint32_t a1 = pack_bf16(__fmaf_rn(nib_f(E, 1), sc.x, mn.x), __fmaf_rn(nib_f(Od, 1), sc.y, mn.y));
+            const uint32_t a2 = pack_bf16(__fmaf_rn(nib_f(E, 2), sc.z, mn.z), __fmaf_rn(nib_f(Od, 2), sc.w, mn.w));
+            const uint32_t a3 = pack_bf16(__fmaf_rn(nib_f(E, 3), sc.z, mn.z), __fmaf_rn(nib_f(Od, 3), sc.w, mn.w));
+            mma_bf16(s[mt], a0, a1, a2, a3, qb[j][0], qb[j][1]);
+          }
+        }
+#pragma unroll
+        for (int mt = 0; mt < NMT; ++mt) {
+          valid[mt][0] = valid[mt][1] = true;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) s[mt][k] *= io.scale_log2;
+        }
+        online_step<NMT>(s, valid, m_run, l_run, o, macc, tsum);
+        uint32_t pbh[NMT][2];
+        float pm0 = 0.f, pm1 = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < NMT; ++kk) {
+          const int t0 = 32 * hv + 16 * kk + gl, t1 = t0 + 8;
+          const float s0v = __half2float(vsp[t0]), s1v = __half2float(vsp[t1]);
+          const float m0v = __half2float(vmp[t0]), m1v = __half2float(vmp[t1]);
+          pm0 = fmaf(s[kk][0], m0v, fmaf(s[kk][2], m1v, pm0));
+          pm1 = fmaf(s[kk][1], m0v, fmaf(s[kk][3], m1v, pm1));
+          pbh[kk][0] = movmatrix_trans(pack_half(s[kk][0] * s0v, s[kk][1] * s0v));
+          pbh[kk][1] = movmatrix_trans(pack_half(s[kk][2] * s1v, s[kk][3] * s1v));
+        }
+        macc[0] += warp_sum_xor_g(pm0);
+        macc[1] += warp_sum_xor_g(pm1);
+        // values: tile (token group tg, dim tile i) is word ((tile/4)*32 + lane)*4 + tile%4 of the V
+        // codes; its registers 0, 1 sit at nibbles 0, 1 of each half, registers 2, 3 at nibbles 2, 3
+#pragma unroll
+        for (int kk = 0; kk < NMT; ++kk) {
+          const int tg = 2 * hv + kk;
+          const uint4 w03 = lds128(vch + (((2 * tg) * 32 + lane) * 4) * 4);
+          const uint4 w47 = lds128(vch + (((2 * tg + 1) * 32 + lane) * 4) * 4);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const uint32_t w = word_of(i < 4 ? w03 : w47, i & 3);
+            const uint32_t w8 = w >> 8;
+            mma_f16(o[i], dq_v4(w, 0), dq_v4(w, 1), dq_v4(w8, 0), dq_v4(w8, 1), pbh[kk][0], pbh[kk][1]);
+          }
+        }
+        add_half_mass();
+      }
+      __syncwarp();
+      release_chunk(c0);
+      release_chunk(c0 + 1);
+      release_chunk(c0 + 2);
     }
-    // log2-sum-exp of this window's logits per head: its mass is 2^(mu - M) / L with the merged
-    // max M and sum L; recorded under the window's stable index (recent, then Full, then Quantized)
+    // the window's log2-sum-exp per head: its mass is 2^(mu - M) / L with the merged max M and sum
+    // L; recorded under the window's stable index (recent, then Full, then Quantized)
     if (gl == 0) {
       const int sidx = it <= nL ? it : (it <= nL + nF ? it - nL + C.loc_items() : it - nL - nF + C.loc_items() + C.kf_cap());
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int head = 2 * tl + h;
-        if (head < G) mu[(size_t)sidx * 8 + head] = tsum[h] > 0.f ? m_run[h] + __log2f(tsum[h]) : -INFINITY;
+        if (head < G) mu[(size_t)sidx * 8 + head] = wmu[h];
       }
     }
   }
@@ -601,7 +744,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   // ---------------- merge the consumer warps of this CTA into one split partial; each consumer
   // warp stores its state as soon as its queue runs dry, into a region of its own
   const int lgG = __ffs(G) - 1;
-  float *cm = reinterpret_cast<float *>(smem + DEC_MRG_OFF);   // [DEC_CONSUMERS][8] running max
+  float *cm = reinterpret_cast<float *>(smem + Dg::MRG_OFF);   // [DEC_CONSUMERS][8] running max
   float *cl = cm + DEC_CONSUMERS * 8;            // [DEC_CONSUMERS][8] running sum
   float *cf = cl + DEC_CONSUMERS * 8;            // [DEC_CONSUMERS][8] rescale factor to the CTA max
   float *sM = cf + DEC_CONSUMERS * 8;            // [16] CTA max per head, then the merged max and 1/L
@@ -712,21 +855,26 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   }
 }
 
-int decode_smem_bytes() { return DEC_SMEM; }
 int decode_warps() { return DEC_WARPS; }
 
-cudaError_t launch_decode(const CacheDev &C, const DecodeIO &io, cudaStream_t stream) {
-  static bool attr_set = false;
-  auto kern = decode_kernel<32, 2>;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DEC_SMEM);
+template <int W, int BITS>
+static cudaError_t launch_decode_fmt(const CacheDev &C, const DecodeIO &io, cudaStream_t stream) {
+  using Dg = DecGeo<W, BITS>;
+  auto kern = decode_kernel<W, BITS>;
+  static bool attr_set[64] = {};   // per device: the dynamic shared memory opt-in of this kernel
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Dg::SMEM);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[dev] = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C.n_split, C.h_kv, C.B);
   cfg.blockDim = dim3(DEC_WARPS * 32);
-  cfg.dynamicSmemBytes = DEC_SMEM;
+  cfg.dynamicSmemBytes = Dg::SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -734,6 +882,12 @@ cudaError_t launch_decode(const CacheDev &C, const DecodeIO &io, cudaStream_t st
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, C, io);
+}
+
+cudaError_t launch_decode(const CacheDev &C, const DecodeIO &io, cudaStream_t stream) {
+  if (C.W == 32 && C.bits == 2) return launch_decode_fmt<32, 2>(C, io, stream);
+  if (C.W == 64 && C.bits == 4) return launch_decode_fmt<64, 4>(C, io, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace qv

@@ -348,19 +348,28 @@ __device__ void load_window(const CacheDev &C, const PromptIO &pio, int unit, in
   }
 }
 
-// code = clamp(rint((x - m) / s), 0, 3) in float32 with IEEE subtraction and division, 0 when s == 0
+// code = clamp(rint((x - m) / s), 0, 2^BITS - 1) in float32 with IEEE subtraction and division,
+// 0 when s == 0
+template <int BITS>
 __device__ __forceinline__ unsigned quant_code(float x, float s, float m) {
   if (s == 0.f) return 0u;
   const float t = rintf(__fdiv_rn(__fsub_rn(x, m), s));
-  return (unsigned)fminf(fmaxf(t, 0.f), 3.f);
+  return (unsigned)fminf(fmaxf(t, 0.f), (float)((1 << BITS) - 1));
 }
 
-template <int W>
+template <int W, int BITS>
+constexpr int quant_smem_bytes() {   // xk, xv [W][D+1] fp32 + the packed K and V codes
+  return 2 * W * (D + 1) * 4 + 2 * Geo<W, BITS>::CODE_BYTES;
+}
+
+template <int W, int BITS>
 __global__ void __launch_bounds__(MIG_THREADS) quant_kernel(const CacheDev C, const PromptIO pio, int unit0) {
-  using Gm = Geo<W, 2>;
-  __shared__ float xk[W][D + 1], xv[W][D + 1];
-  __shared__ unsigned char ck[W][D], cv[W][D];
-  __shared__ uint32_t cw[2 * Gm::CODE_BYTES / 4];
+  using Gm = Geo<W, BITS>;
+  constexpr float LEVELS = (float)((1 << BITS) - 1);
+  extern __shared__ __align__(16) uint8_t qsm[];
+  auto xk = reinterpret_cast<float(*)[D + 1]>(qsm);
+  auto xv = reinterpret_cast<float(*)[D + 1]>(qsm + W * (D + 1) * 4);
+  uint32_t *cw = reinterpret_cast<uint32_t *>(qsm + 2 * W * (D + 1) * 4);
   const int unit = unit0 + blockIdx.y;
   const int b = unit % C.B;
   const int *meta = C.at<const int>(C.off_meta, C.st_meta, unit);
@@ -373,8 +382,16 @@ __global__ void __launch_bounds__(MIG_THREADS) quant_kernel(const CacheDev C, co
     const int g = job % C.h_kv;
     __syncthreads();
     load_window<W>(C, pio, unit, b, g, tk.y, tk.z, xk, xv);
+    for (int i = threadIdx.x; i < 2 * Gm::CODE_BYTES / 4; i += blockDim.x) cw[i] = 0u;
     __syncthreads();
     uint8_t *blk = ledger + ((size_t)tk.w * C.h_kv + g) * Gm::QB;
+    // scatter a code into its fragment-native position (shared-memory words, copied out below)
+    auto put = [&](bool is_v, int tok, int dim, unsigned c) {
+      int byte, shift;
+      code_pos<BITS>(is_v, tok, dim, byte, shift);
+      const int gb = byte + (is_v ? Gm::CODE_BYTES : 0);
+      atomicOr(&cw[gb >> 2], c << (8 * (gb & 3) + shift));
+    };
     // keys: one group per channel across the window's tokens
     {
       const int dim = tid;   // MIG_THREADS == D
@@ -383,12 +400,12 @@ __global__ void __launch_bounds__(MIG_THREADS) quant_kernel(const CacheDev C, co
         mn = fminf(mn, xk[t][dim]);
         mx = fmaxf(mx, xk[t][dim]);
       }
-      const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+      const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), LEVELS));
       const __half m16 = __float2half_rn(mn);
       const float s = __half2float(s16), m = __half2float(m16);
       reinterpret_cast<__half *>(blk + Gm::OFF_KS)[dim] = s16;
       reinterpret_cast<__half *>(blk + Gm::OFF_KM)[dim] = m16;
-      for (int t = 0; t < W; ++t) ck[t][dim] = (unsigned char)quant_code(xk[t][dim], s, m);
+      for (int t = 0; t < W; ++t) put(false, t, dim, quant_code<BITS>(xk[t][dim], s, m));
     }
     // values: one group per token across the channels
     for (int t = warp; t < W; t += MIG_THREADS / 32) {
@@ -402,27 +419,14 @@ __global__ void __launch_bounds__(MIG_THREADS) quant_kernel(const CacheDev C, co
         mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
       }
-      const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+      const __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), LEVELS));
       const __half m16 = __float2half_rn(mn);
       const float s = __half2float(s16), m = __half2float(m16);
       if (lane == 0) {
         reinterpret_cast<__half *>(blk + Gm::OFF_VS)[t] = s16;
         reinterpret_cast<__half *>(blk + Gm::OFF_VM)[t] = m16;
       }
-      for (int d = lane; d < D; d += 32) cv[t][d] = (unsigned char)quant_code(xv[t][d], s, m);
-    }
-    __syncthreads();
-    // scatter the codes into their fragment-native positions (shared-memory words, then copy out)
-    for (int i = tid; i < 2 * Gm::CODE_BYTES / 4; i += blockDim.x) cw[i] = 0u;
-    __syncthreads();
-    for (int idx = tid; idx < 2 * W * D; idx += blockDim.x) {
-      const bool is_v = idx >= W * D;
-      const int e = is_v ? idx - W * D : idx, tok = e / D, dim = e % D;
-      int byte, shift;
-      code_pos2(is_v, tok, dim, byte, shift);
-      const unsigned c = is_v ? cv[tok][dim] : ck[tok][dim];
-      const int gb = byte + (is_v ? Gm::CODE_BYTES : 0);
-      atomicOr(&cw[gb >> 2], c << (8 * (gb & 3) + shift));
+      for (int d = lane; d < D; d += 32) put(true, t, d, quant_code<BITS>(xv[t][d], s, m));
     }
     __syncthreads();
     for (int i = tid; i < 2 * Gm::CODE_BYTES / 4; i += blockDim.x) reinterpret_cast<uint32_t *>(blk)[i] = cw[i];
@@ -431,9 +435,9 @@ __global__ void __launch_bounds__(MIG_THREADS) quant_kernel(const CacheDev C, co
 
 // ----------------------------------------------------------------------------- promote / copy
 
-template <int W>
+template <int W, int BITS>
 __global__ void __launch_bounds__(MIG_THREADS) move_kernel(const CacheDev C, const PromptIO pio, int unit0) {
-  using Gm = Geo<W, 2>;
+  using Gm = Geo<W, BITS>;
   __shared__ __align__(16) uint8_t led[Gm::QB];
   const int unit = unit0 + blockIdx.y;
   const int b = unit % C.B;
@@ -465,8 +469,8 @@ __global__ void __launch_bounds__(MIG_THREADS) move_kernel(const CacheDev C, con
         const bool is_v = idx >= W * D;
         const int e = is_v ? idx - W * D : idx, tok = e / D, dim = e % D;
         int byte, shift;
-        code_pos2(is_v, tok, dim, byte, shift);
-        const float c = (float)((led[byte + (is_v ? Gm::OFF_VCODE : 0)] >> shift) & 3u);
+        code_pos<BITS>(is_v, tok, dim, byte, shift);
+        const float c = (float)((led[byte + (is_v ? Gm::OFF_VCODE : 0)] >> shift) & ((1u << BITS) - 1u));
         const float s = __half2float(is_v ? vsp[tok] : ks[dim]);
         const float m = __half2float(is_v ? vmp[tok] : km[dim]);
         const __nv_bfloat16 x = __float2bfloat16_rn(__fmaf_rn(c, s, m));
@@ -555,27 +559,55 @@ cudaError_t launch_init(const CacheDev &C, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+template <int W, int BITS>
+static cudaError_t launch_migrate(const CacheDev &C, const PromptIO &pio, int unit0, int n_units, int mig_blocks,
+                                  cudaStream_t s) {
+  constexpr int qsm = quant_smem_bytes<W, BITS>();
+  static bool attr_set[64] = {};   // per device: the dynamic shared memory opt-in
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (qsm > 48 * 1024 && !attr_set[dev]) {
+    e = cudaFuncSetAttribute(quant_kernel<W, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, qsm);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  dim3 grid(mig_blocks, n_units);
+  quant_kernel<W, BITS><<<grid, MIG_THREADS, qsm, s>>>(C, pio, unit0);
+  move_kernel<W, BITS><<<grid, MIG_THREADS, 0, s>>>(C, pio, unit0);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_route(const CacheDev &C, int unit0, int n_units, const __nv_bfloat16 *kp,
                          const __nv_bfloat16 *vp, int layer, int mig_blocks, cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, route_smem_bytes());
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, route_smem_bytes());
     if (e != cudaSuccess) return e;
-    attr = true;
+    attr_set[dev] = true;
   }
   const int prefill = kp != nullptr;
   route_kernel<<<n_units, RT_THREADS, route_smem_bytes(), s>>>(C, unit0, prefill);
   PromptIO pio{kp, vp, layer};
-  dim3 grid(mig_blocks, n_units);
-  quant_kernel<32><<<grid, MIG_THREADS, 0, s>>>(C, pio, unit0);
-  move_kernel<32><<<grid, MIG_THREADS, 0, s>>>(C, pio, unit0);
-  return cudaGetLastError();
+  if (C.W == 32 && C.bits == 2) return launch_migrate<32, 2>(C, pio, unit0, n_units, mig_blocks, s);
+  if (C.W == 64 && C.bits == 4) return launch_migrate<64, 4>(C, pio, unit0, n_units, mig_blocks, s);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_prefill_setup(const CacheDev &C, const __nv_bfloat16 *kp, const __nv_bfloat16 *vp, int layer,
                                  const float *s0, cudaStream_t s) {
   PromptIO pio{kp, vp, layer};
-  prefill_setup_kernel<32><<<dim3(C.B, C.h_kv), 256, 0, s>>>(C, pio, s0);
+  if (C.W == 32)
+    prefill_setup_kernel<32><<<dim3(C.B, C.h_kv), 256, 0, s>>>(C, pio, s0);
+  else if (C.W == 64)
+    prefill_setup_kernel<64><<<dim3(C.B, C.h_kv), 256, 0, s>>>(C, pio, s0);
+  else
+    return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 

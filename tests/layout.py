@@ -30,9 +30,16 @@ def fn_index(W, is_v):
 
 
 def code_position(W, bits, is_v):
-    """(byte offset, bit shift) of every (tok, dim) INT2 code inside a K or V code block."""
-    assert bits == 2
+    """(byte offset, bit shift) of every (tok, dim) code inside a K or V code block."""
+    assert bits in (2, 4)
     tok, dim = _maps(W)
+    if bits == 4:
+        r, c = (dim % 16, tok % 16) if is_v else (tok % 16, dim % 16)
+        lane, reg = _frag(r, c)
+        tile = (tok // 16) * 8 + dim // 16
+        word = ((tile // 4) * 32 + lane) * 4 + tile % 4
+        bit = 4 * reg + 16 * (tok % 2) if is_v else 4 * (reg * 2 + dim % 2)
+        return (word * 4 + bit // 8).reshape(W, D), (bit % 8).reshape(W, D)
     if not is_v:
         r, c = tok % 16, dim % 16
         lane, reg = _frag(r, c)

@@ -37,13 +37,25 @@ def test_budget_matches_oracle(cpu_lib, name):
 
 
 def test_budget_sweep_matches_oracle(cpu_lib):
+    """The 131K sweep (budget 10/20/40%, q 0.5/0.7/0.9) in both formats, INT2/W=32 and INT4/W=64."""
     base = synth.workload("long_131k")
-    for bn in (10, 20, 40):
-        for qn in (50, 70, 90):
-            wl = base.replace(budget_num=bn, q_num=qn)
-            b = binding.budget(binding.make_config(wl))
-            ob = O.budget(O.Config.from_obj(wl))
-            assert (b.k_f, b.k_q) == (ob.k_f, ob.k_q)
+    for fmt in (dict(window=32, bits=2), dict(window=64, bits=4)):
+        for bn in (10, 20, 40):
+            for qn in (50, 70, 90):
+                wl = base.replace(budget_num=bn, q_num=qn, **fmt)
+                b = binding.budget(binding.make_config(wl))
+                ob = O.budget(O.Config.from_obj(wl))
+                assert (b.payload, b.m_f, b.m_q, b.k_f, b.k_q, b.n_windows) == \
+                    (ob.payload, ob.m_f, ob.m_q, ob.k_f, ob.k_q, O.Config.from_obj(wl).n_windows_cap())
+
+
+def test_int4_payload_and_capacities(cpu_lib):
+    """INT4/W=64 record of the 131K shape: 2*8*64*128*4/8 code bytes + 8*128*4 key and 8*64*4 value
+    parameter bytes = 71680 per window (8960 per KV head); at 20% and q = 0.7: K_f = 95, K_q = 1036."""
+    wl = synth.workload("long_131k", window=64, bits=4)
+    b = binding.budget(binding.make_config(wl))
+    assert b.payload == 71680 and b.payload // wl.h_kv == 8960
+    assert (b.k_f, b.k_q) == (95, 1036)
 
 
 def test_rejections(cpu_lib):
@@ -57,7 +69,7 @@ def test_rejections(cpu_lib):
 
 
 def test_documented_layouts_are_bijections():
-    for W, bits in ((32, 2),):
+    for W, bits in ((32, 2), (64, 4)):
         for is_v in (False, True):
             idx = LY.fn_index(W, is_v)
             assert np.array_equal(np.sort(idx.ravel()), np.arange(W * 128))

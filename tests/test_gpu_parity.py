@@ -50,6 +50,18 @@ def test_scores_absorbed_only_at_routing(lib):
     _run(base.replace(h_q=16, h_kv=2, batch=2, omega=5), 20, per_step=False)
 
 
+@pytest.mark.parametrize("shape", [
+    dict(h_q=8, h_kv=2, prompt_len=1500, n_sink=4, batch=2),          # G = 4, batch 2
+    dict(h_q=8, h_kv=8, prompt_len=1111, n_sink=7, budget_num=40),     # G = 1, ragged prompt
+    dict(h_q=16, h_kv=2, prompt_len=2000, n_sink=16, omega=5),         # G = 8, 16 sinks
+])
+def test_int4_w64_shapes(lib, shape):
+    """The INT4 / 64-token-window format (QEvict §5 INT4 setting): 4-bit codes with fp16 scale and
+    offset, three-chunk ledger records, windows decoded as two 32-token halves."""
+    base = synth.workload("tiny_4k", window=64, bits=4, steps=24, n_plant=4, kappa=6.0)
+    _run(base.replace(**shape), 24)
+
+
 def test_two_tier_and_quantized_only(lib):
     """q = 0: Full/Evicted only (two-tier window eviction); q = 1: K_f = 0 (quantised retention)."""
     base = synth.workload("tiny_4k", prompt_len=1200, steps=16, n_plant=4)
@@ -95,12 +107,14 @@ def test_full_size_llama_shape(lib):
 
 @pytest.mark.parametrize("name,over,steps,check_state", [
     # 16 sequences of the 32K shape: 128 (sequence, KV head) units, 2 splits each
-    ("batched_32k", dict(n_layers=1, steps=16), 16, True),
+    ("batched_32k", dict(n_layers=1, steps=8), 8, True),
     # 131K prompt, lognormal per-window key scales (INT2, 20%, q = 0.7): outputs, masses and the
     # transition counters of every unit every step; tier-state dumps are skipped at this size
     ("long_131k", dict(n_layers=1, batch=2, steps=8), 8, False),
     # random-walk queries, 12.5% budget, 256 recent tokens, batch 8: three routing events
     ("drift_16k", dict(n_layers=1, steps=24), 24, True),
+    # the 131K point in the INT4 / 64-token-window format
+    ("long_131k", dict(n_layers=1, batch=1, steps=8, window=64, bits=4), 8, False),
 ])
 def test_full_size_workloads(lib, name, over, steps, check_state):
     """The other workloads at their full per-layer shapes (one layer each), in lockstep: outputs,
