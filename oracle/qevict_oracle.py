@@ -87,6 +87,13 @@ class Config:
     prompt_len: int = 4096
     max_len: int = 4160
     b_total: Optional[int] = None    # bytes per (sequence, layer); None = budget fraction of full KV
+    # window ranking (QEvict App. J): 0 cumulative attention (the default, Eq. (21)), 1 exponentially
+    # decayed attention (Eq. (22)), 2 attention p-norm (Eq. (23)), 3 key-vector norm (Eq. (24))
+    ranker: int = 0
+    decay: float = 0.99
+    pnorm: float = 3.0
+    # QEvict App. K: 1 = quantized windows may be evicted but never return to the full tier
+    no_promotion: int = 0
 
     @staticmethod
     def from_obj(o, **kw) -> "Config":
@@ -321,6 +328,8 @@ class Unit:
         self.local: Dict[int, Tuple[np.ndarray, np.ndarray]] = {}   # position -> (k, v) [H_kv][d]
         self.z = np.full(ncap, LOCAL, np.int8)
         self.S = np.zeros(ncap, np.float64)    # cumulative score, QEvict §4.2 Eq. (1)
+        self.U = np.zeros(ncap, np.float64)    # attention since the previous routing event, App. J Eq. (20)
+        self.R = np.zeros(ncap, np.float64)    # the ranker's value of every window (App. J)
         self.full: Dict[int, Tuple[np.ndarray, np.ndarray]] = {}    # wid -> (K, V) [W][H_kv][d]
         self.ledger: Dict[int, Ledger] = {}
         self.f_slot: Dict[int, int] = {}
@@ -342,6 +351,7 @@ class Unit:
         s0 = np.asarray(s0, np.float64)
         assert len(s0) == prompt_windows(cfg), "one initial score per window that starts in the prompt"
         self.S[:len(s0)] = s0
+        self.U[:len(s0)] = s0                  # the prompt's attention is the first event's u
         self.route()
 
     # ---- one decode step (QEvict §4.1 attention; §4.2 Eq. (1) score accumulation)
@@ -386,7 +396,30 @@ class Unit:
             masses[h] = np.bincount(wid[hist], weights=a[h, hist], minlength=ncap)[:ncap]
         sink_mass = a[:, ~hist].sum(axis=1)
         self.S += masses.sum(axis=0) / cfg.h_q
+        self.U += masses.sum(axis=0) / cfg.h_q
         return o, masses, sink_mass
+
+    def key_norm(self, w: int) -> float:
+        """Mean L2 norm of the window's cached keys, each token's key over all KV heads (App. J Eq. (24)
+        up to the sign, which becomes an ascending ranking)."""
+        cfg = self.cfg
+        lo = cfg.n_sink + w * cfg.window
+        return float(np.mean([np.sqrt(np.sum(np.asarray(self.local[p][0], np.float64) ** 2))
+                              for p in range(lo, lo + cfg.window)]))
+
+    def rank_values(self, cand: List[int], aged: List[int]) -> None:
+        """Fold the event's attention u = U into the ranker's value R (App. J), then reset U."""
+        cfg = self.cfg
+        if cfg.ranker == 0:      # cumulative, Eq. (21): S already holds S_prev + u
+            self.R[:] = self.S
+        elif cfg.ranker == 1:    # decayed, Eq. (22)
+            self.R[:] = cfg.decay * self.R + self.U
+        elif cfg.ranker == 2:    # p-norm, Eq. (23): ranked by sum_r u_r^p, the same order as its p-th root
+            self.R[:] = self.R + self.U ** cfg.pnorm
+        else:                    # key norm, Eq. (24): computed once, when the window leaves the recent region
+            for w in aged:
+                self.R[w] = self.key_norm(w)
+        self.U[:] = 0.0
 
     # ---- routing event (QEvict §4.3 Eq. (4)-(6), App. A Algorithm 1)
     def route(self, scores: Optional[np.ndarray] = None):
@@ -399,16 +432,30 @@ class Unit:
         K_f become Full, the next K_q Quantized, the rest Evicted.
         """
         cfg, bud = self.cfg, self.bud
-        if scores is not None:
-            self.S[:len(scores)] = np.asarray(scores, np.float64)
         n_new = n_hist(self.T, cfg)
         aged = list(range(self.n_route, n_new))
         prev = {w: int(self.z[w]) for w in range(self.n_route) if self.z[w] in (FULL, QUANT)}
         cand = sorted(list(prev) + aged)
-        order = sorted(cand, key=lambda w: (-float(self.S[w]), w))
-        new_f = set(order[:bud.k_f])
-        new_q = set(order[bud.k_f:bud.k_f + bud.k_q])
-        new_e = set(order[bud.k_f + bud.k_q:])
+        self.rank_values(cand, aged)
+        if scores is not None:                   # the "identical scores" parity mode: rank on these
+            self.R[:len(scores)] = np.asarray(scores, np.float64)
+            if cfg.ranker == 0:
+                self.S[:len(scores)] = np.asarray(scores, np.float64)
+        if cfg.ranker == 3:                      # lower key norms first (Eq. (24)'s negative sign)
+            order = sorted(cand, key=lambda w: (float(self.R[w]), w))
+        else:
+            order = sorted(cand, key=lambda w: (-float(self.R[w]), w))
+        if cfg.no_promotion:
+            # App. K: a quantized window cannot return to the full tier, so the full tier takes the
+            # best-ranked candidates that are not quantized; the quantized tier the next best of the rest
+            new_f = set([w for w in order if prev.get(w) != QUANT][:bud.k_f])
+            rest = [w for w in order if w not in new_f]
+            new_q = set(rest[:bud.k_q])
+            new_e = set(rest[bud.k_q:])
+        else:
+            new_f = set(order[:bud.k_f])
+            new_q = set(order[bud.k_f:bud.k_f + bud.k_q])
+            new_e = set(order[bud.k_f + bud.k_q:])
         ctr = dict.fromkeys(COUNTER_NAMES, 0)
         tr = {"promote": [], "demote": [], "quantize": [], "reactivate": [], "evict": [],
               "aged_full": [], "aged_quant": []}
