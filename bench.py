@@ -61,6 +61,17 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_tensor_peak():
+    """Dense bf16 TFLOP/s: the measured cuBLAS burst figure, else the recipe's fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if d.get("bf16_tflops"):
+            return float(d["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
 # --------------------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -284,6 +295,30 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     t_pre = time.time() - t_pre
 
+    # ---- prefill scoring throughput: the two causal passes over one layer's prompt (tensor cores)
+    pin = [synth.prompt_inputs(wl, b, 0, device=dev) for b in range(B)]
+    pq = torch.stack([x["q"] for x in pin])
+    pk = torch.stack([x["k"] for x in pin])
+    del pin
+    npw = (wl.prompt_len - wl.n_sink + wl.window - 1) // wl.window
+    ps0 = torch.empty(B, npw, dtype=torch.float32, device=dev)
+    cache.prefill_scores(pq, pk, ps0, stream)
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    for _ in range(3):
+        cache.prefill_scores(pq, pk, ps0, stream)
+    p1.record(stream)
+    torch.cuda.synchronize()
+    pre_ms = p0.elapsed_time(p1) / 3
+    pre_flops = 2.0 * wl.prompt_len * (wl.prompt_len + 1) * D * wl.h_q * B   # two passes of causal q.k
+    pre_tf = pre_flops / (pre_ms / 1e3) / 1e12
+    tpeak, tpeak_kind = measured_tensor_peak()
+    prefill_scores = {"ms_per_layer": pre_ms, "tflops": pre_tf, "peak_tflops": tpeak, "frac": pre_tf / tpeak,
+                      "flops_per_layer": pre_flops,
+                      "note": "causal FLOPs of both passes (row log-sum-exp, column sums), mma.m16n8k16 bf16; "
+                              f"peak = {tpeak_kind} dense bf16 burst"}
+    del pq, pk, ps0
+
     # ---- decode inputs for every step resident in HBM: [step][layer][B][...]
     qs = torch.empty(total, L, B, wl.h_q, D, dtype=torch.bfloat16, device=dev)
     ks = torch.empty(total, L, B, wl.h_kv, D, dtype=torch.bfloat16, device=dev)
@@ -468,7 +503,7 @@ def run_gpu(args, rank, world):
                      "vs_8tbs": achieved / 8000.0},
         "gpu_launches": timed_launches,
         "clocks": clocks,
-        "prefill_s": round(t_pre, 2),
+        "prefill_s": round(t_pre, 2), "prefill_scores": prefill_scores,
     }
     if e2e:
         result["e2e"] = e2e

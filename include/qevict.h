@@ -60,6 +60,16 @@ typedef struct {
   int32_t budget_num, budget_den; /* B_total = floor(budget_num * M_FullKV / budget_den) when b_total == 0 */
   int64_t b_total;                /* bytes per (sequence, layer); 0 = use the fraction above */
   int32_t prompt_len, max_len;    /* max_len = prompt_len + decode steps the cache must hold */
+  /* Window ranking at routing events (QEvict App. J; 0 everywhere = the paper's default):
+   *   ranker 0: cumulative attention S += u per event (QEvict §4.2 Eq. (1), App. J Eq. (21));
+   *   ranker 1: decayed attention S = decay * S + u (Eq. (22)); decay in (0, 1], 0 = 0.99;
+   *   ranker 2: attention p-norm, ranked by sum over events of u^pnorm (Eq. (23)); pnorm >= 1, 0 = 3;
+   *   ranker 3: key-vector norm, lower mean key L2 norm first (Eq. (24)), taken when the window
+   *             leaves the recent region.
+   * u is the window's attention since the previous event (App. J Eq. (20)).  no_promotion = 1:
+   * quantized windows may be evicted but never return to the full tier (QEvict App. K). */
+  int32_t ranker, no_promotion;
+  float decay, pnorm;
 } qevict_config;
 
 /* Byte budget of one (sequence, layer), QEvict §4.1 (constraint), §4.3 Eq. (3), App. B.4 Eq. (7)-(8).
@@ -94,6 +104,8 @@ typedef struct {
  *   ftab   [k_f] int32 pairs (window id, F slot), ascending window id; f_count valid
  *   qtab   [k_q] int32 pairs (window id, ledger slot), ascending window id; q_count valid
  *   meta   int32[16]: [0] tokens cached T, [1] windows routed so far, [2] f_count, [3] q_count
+ *   agg    [n_windows] fp32: the ranker's value of every window for rankers 1-3 (the score
+ *          region then holds only the attention since the last routing event)
  *
  * Fragment-native bf16 block of one window and KV head (W = window tokens, d = 128):
  *   K element (tok, dim), tok < W: index (((tok/16)*8 + dim/16)*32 + lane)*8 + reg*2 + (dim%2)
@@ -129,6 +141,8 @@ typedef struct {
   int64_t qblock;        /* ledger bytes per (slot, KV head) */
   int64_t arena_bytes;
   int32_t n_split;       /* decode split-K partitions per (sequence, KV head) */
+  int32_t pad_;
+  int64_t off_agg, stride_agg;
 } qevict_layout;
 
 typedef struct qevict_cache qevict_cache;

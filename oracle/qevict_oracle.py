@@ -422,7 +422,7 @@ class Unit:
         self.U[:] = 0.0
 
     # ---- routing event (QEvict §4.3 Eq. (4)-(6), App. A Algorithm 1)
-    def route(self, scores: Optional[np.ndarray] = None):
+    def route(self, scores: Optional[np.ndarray] = None, rank_hook=None):
         """Route at the current T.  `scores` overrides S (the "identical scores" parity mode).
 
         Candidates (Eq. (4)): windows now Full or Quantized plus the windows aged
@@ -437,6 +437,8 @@ class Unit:
         prev = {w: int(self.z[w]) for w in range(self.n_route) if self.z[w] in (FULL, QUANT)}
         cand = sorted(list(prev) + aged)
         self.rank_values(cand, aged)
+        if rank_hook is not None:                # lets a parity test compare the rank values first
+            rank_hook(self.R)
         if scores is not None:                   # the "identical scores" parity mode: rank on these
             self.R[:len(scores)] = np.asarray(scores, np.float64)
             if cfg.ranker == 0:

@@ -27,7 +27,9 @@ class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in ("batch", "n_layers", "h_q", "h_kv", "d_head", "n_sink", "n_recent",
                                              "window", "bits", "omega", "q_num", "q_den", "budget_num",
                                              "budget_den")] + \
-               [("b_total", ctypes.c_int64), ("prompt_len", ctypes.c_int32), ("max_len", ctypes.c_int32)]
+               [("b_total", ctypes.c_int64), ("prompt_len", ctypes.c_int32), ("max_len", ctypes.c_int32),
+                ("ranker", ctypes.c_int32), ("no_promotion", ctypes.c_int32), ("decay", ctypes.c_float),
+                ("pnorm", ctypes.c_float)]
 
 
 class BudgetInfo(ctypes.Structure):
@@ -41,7 +43,8 @@ _LAYOUT_REGIONS = ("sink", "ring", "fpool", "ledger", "score", "state", "fslot",
 
 class Layout(ctypes.Structure):
     _fields_ = [(f"{k}_{r}", ctypes.c_int64) for r in _LAYOUT_REGIONS for k in ("off", "stride")] + \
-               [("qblock", ctypes.c_int64), ("arena_bytes", ctypes.c_int64), ("n_split", ctypes.c_int32)]
+               [("qblock", ctypes.c_int64), ("arena_bytes", ctypes.c_int64), ("n_split", ctypes.c_int32),
+                ("pad_", ctypes.c_int32), ("off_agg", ctypes.c_int64), ("stride_agg", ctypes.c_int64)]
 
 
 class Tuple(ctypes.Structure):
@@ -113,6 +116,10 @@ def make_config(wl, **over) -> Config:
             c.b_total = int(over.get("b_total", getattr(wl, "b_total", 0) or 0))
         elif name == "max_len":
             c.max_len = int(over.get("max_len", wl.prompt_len + wl.steps))
+        elif name in ("decay", "pnorm"):
+            setattr(c, name, float(over.get(name, getattr(wl, name, 0.0))))
+        elif name in ("ranker", "no_promotion"):
+            setattr(c, name, int(over.get(name, getattr(wl, name, 0))))
         else:
             setattr(c, name, int(over.get(name, getattr(wl, name))))
     return c

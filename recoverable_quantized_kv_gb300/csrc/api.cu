@@ -61,6 +61,8 @@ qevict_status check_config(const qevict_config *c) {
   if (G != 1 && G != 2 && G != 4 && G != 8) return QEVICT_EINVAL;
   if (c->d_head != D) return QEVICT_EINVAL;
   if (!((c->window == 32 && c->bits == 2) || (c->window == 64 && c->bits == 4))) return QEVICT_EINVAL;
+  if (c->ranker < 0 || c->ranker > 3 || c->no_promotion < 0 || c->no_promotion > 1) return QEVICT_EINVAL;
+  if (!(c->decay >= 0.f && c->decay <= 1.f) || !(c->pnorm == 0.f || c->pnorm >= 1.f)) return QEVICT_EINVAL;
   if (c->n_sink < 1 || c->n_sink > 16 || c->n_recent < c->window || c->omega < 1 ||
       c->omega > 256)
     return QEVICT_EINVAL;
@@ -131,6 +133,7 @@ void make_plan(const qevict_config *c, const qevict_budget_info *b, Plan *p) {
   region(8LL * kf_cap, L.off_ftab, L.stride_ftab);
   region(8LL * kq_cap, L.off_qtab, L.stride_qtab);
   region(4LL * qv::META_INTS, L.off_meta, L.stride_meta);
+  region(4LL * N, L.off_agg, L.stride_agg);
   qv::CacheDev &C = p->dev;
   region(16LL * N, C.off_qtask, C.st_qtask);
   region(16LL * N, C.off_mtask, C.st_mtask);
@@ -173,6 +176,7 @@ void make_plan(const qevict_config *c, const qevict_budget_info *b, Plan *p) {
   C.off_ftab = L.off_ftab;     C.st_ftab = L.stride_ftab;
   C.off_qtab = L.off_qtab;     C.st_qtab = L.stride_qtab;
   C.off_meta = L.off_meta;     C.st_meta = L.stride_meta;
+  C.off_agg = L.off_agg;       C.st_agg = L.stride_agg;
   C.B = c->batch;
   C.L = c->n_layers;
   C.h_q = c->h_q;
@@ -191,6 +195,10 @@ void make_plan(const qevict_config *c, const qevict_budget_info *b, Plan *p) {
   C.max_items = max_items;
   C.prompt_len = c->prompt_len;
   C.max_len = c->max_len;
+  C.ranker = c->ranker;
+  C.no_promotion = c->no_promotion;
+  C.decay = c->decay == 0.f ? 0.99f : c->decay;
+  C.pnorm = c->pnorm == 0.f ? 3.0f : c->pnorm;
 }
 
 qevict_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QEVICT_OK : QEVICT_ECUDA; }

@@ -21,6 +21,7 @@ struct CacheDev {
   int64_t off_ftab, st_ftab;
   int64_t off_qtab, st_qtab;
   int64_t off_meta, st_meta;
+  int64_t off_agg, st_agg;         // float [N]: ranker value (rankers 1-3)
   int64_t off_qtask, st_qtask;     // int4 quantise tasks [n_windows]
   int64_t off_mtask, st_mtask;     // int4 promote/copy tasks [n_windows]
   // global regions
@@ -40,6 +41,8 @@ struct CacheDev {
   // sizes
   int B, L, h_q, h_kv, G, n_sink, n_recent, W, bits, omega;
   int k_f, k_q, n_windows, ring_windows, n_split, max_items, prompt_len, max_len;
+  int ranker, no_promotion;
+  float decay, pnorm;
 
   // Stable index of a window's mass record between two routing events: 1 + i for the i-th recent
   // window from the first unrouted one, then the Full table entries, then the Quantized ones.

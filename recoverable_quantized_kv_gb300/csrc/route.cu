@@ -84,7 +84,8 @@ __device__ int block_sum(int v, int *wsum) {
   return t;
 }
 
-__global__ void __launch_bounds__(RT_THREADS, 1) route_kernel(const CacheDev C, int unit0, int prefill) {
+__global__ void __launch_bounds__(RT_THREADS, 1) route_kernel(const CacheDev C, const PromptIO pio, int unit0,
+                                                              int prefill) {
   extern __shared__ __align__(16) uint8_t smem[];
   unsigned long long *keys = reinterpret_cast<unsigned long long *>(smem);          // [RT_MAXN]
   int *scanA = reinterpret_cast<int *>(smem + 8 * RT_MAXN);                          // [RT_MAXN]
@@ -113,15 +114,58 @@ __global__ void __launch_bounds__(RT_THREADS, 1) route_kernel(const CacheDev C, 
     return;
   }
 
-  // 1. the window score is the sum of the per-KV-head partials; collapse it into head 0
+  // 1. the window's attention is the sum of the per-KV-head partials.  Cumulative ranking keeps the
+  //    running score in head 0; the other rankers (QEvict App. J) fold the event's attention u
+  //    (Eq. (20)) into agg, S = decay * S + u (Eq. (22)) or S = S + u^p (Eq. (23)), and restart u.
+  const int ranker = C.ranker;
+  float *agg = C.at<float>(C.off_agg, C.st_agg, unit);
   for (int w = tid; w < n_acc; w += nt) {
     float s = score[w];
     for (int g = 1; g < C.h_kv; ++g) {
       s += score[(size_t)g * N + w];
       score[(size_t)g * N + w] = 0.f;
     }
-    score[w] = s;
+    if (ranker == 0) {
+      score[w] = s;
+    } else {
+      score[w] = 0.f;
+      if (ranker == 1) agg[w] = fmaf(C.decay, agg[w], s);
+      else if (ranker == 2) agg[w] += powf(s, C.pnorm);
+    }
   }
+  if (ranker == 3) {
+    // key norm (Eq. (24)): mean over the window's tokens of the key's L2 norm across all KV heads,
+    // taken once, when the window leaves the recent region; one warp per window, a lane per token
+    const int warp = tid >> 5, lane = tid & 31, b = unit % C.B;
+    const __nv_bfloat16 *ring = C.at<const __nv_bfloat16>(C.off_ring, C.st_ring, unit);
+    for (int w = nr_old + warp; w < n_new; w += nt / 32) {
+      float sum = 0.f;
+      for (int t = lane; t < W; t += 32) {
+        const int pos = C.n_sink + w * W + t;
+        float ss = 0.f;
+        for (int g = 0; g < C.h_kv; ++g) {
+          if (prefill) {
+            const __nv_bfloat16 *kr = pio.k + (((size_t)b * C.prompt_len + pos) * C.h_kv + g) * D;
+            for (int d = 0; d < D; ++d) {
+              const float x = __bfloat162float(kr[d]);
+              ss = fmaf(x, x, ss);
+            }
+          } else {
+            const __nv_bfloat16 *kb = ring + ((size_t)(g * 2) * C.ring_windows + w % C.ring_windows) * W * D;
+            for (int d = 0; d < D; ++d) {
+              const float x = __bfloat162float(kb[fnk_index(t, d)]);
+              ss = fmaf(x, x, ss);
+            }
+          }
+        }
+        sum += sqrtf(ss);
+      }
+#pragma unroll
+      for (int off = 16; off; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      if (lane == 0) agg[w] = sum / (float)W;
+    }
+  }
+  __syncthreads();
   // 2. candidates (Eq. (4)): windows still in F or Q plus the newly aged ones
   for (int w = tid; w < n_new; w += nt) {
     const int tier = state[w] & 3;
@@ -138,9 +182,10 @@ __global__ void __launch_bounds__(RT_THREADS, 1) route_kernel(const CacheDev C, 
   __syncthreads();
   for (int w = tid; w < n_new; w += nt)
     if (scanA[w]) {
-      // S >= +0, so its bit pattern orders like the value; ~bits sorts descending, the id ascending
-      const unsigned sb = __float_as_uint(score[w]);
-      keys[scanB[w]] = ((unsigned long long)(~sb) << 32) | (unsigned)w;
+      // the rank value is >= +0, so its bit pattern orders like the value; ~bits sorts descending
+      // (key norms: ascending), ties by window id ascending
+      const unsigned sb = __float_as_uint(ranker == 0 ? score[w] : agg[w]);
+      keys[scanB[w]] = ((unsigned long long)(ranker == 3 ? sb : ~sb) << 32) | (unsigned)w;
     }
   __syncthreads();
   // 3. bitonic sort, ascending keys = (score desc, window id asc)
@@ -159,9 +204,30 @@ __global__ void __launch_bounds__(RT_THREADS, 1) route_kernel(const CacheDev C, 
       __syncthreads();
     }
   // 4. Eq. (5): TopK_{K_f} -> Full, next K_q -> Quantized, rest -> Evicted
-  for (int r = tid; r < count; r += nt) {
-    const int w = (int)(keys[r] & 0xffffffffu);
-    newt[w] = r < C.k_f ? TIER_FULL : ((long long)r < (long long)C.k_f + C.k_q ? TIER_QUANT : TIER_EVICT);
+  if (!C.no_promotion) {
+    for (int r = tid; r < count; r += nt) {
+      const int w = (int)(keys[r] & 0xffffffffu);
+      newt[w] = r < C.k_f ? TIER_FULL : ((long long)r < (long long)C.k_f + C.k_q ? TIER_QUANT : TIER_EVICT);
+    }
+  } else {
+    // QEvict App. K: a quantized window cannot return to the full tier, so Full takes the best-ranked
+    // candidates that are not quantized and Quantized the best of the rest
+    auto eligible = [&](int w) { return !(w < nr_old && (state[w] & 3) == TIER_QUANT); };
+    for (int r = tid; r < count; r += nt) scanA[r] = eligible((int)(keys[r] & 0xffffffffu)) ? 1 : 0;
+    __syncthreads();
+    block_exscan(scanA, count, wsum);
+    for (int r = tid; r < count; r += nt) {
+      const int w = (int)(keys[r] & 0xffffffffu);
+      const bool f = eligible(w) && scanA[r] < C.k_f;
+      scanB[r] = f ? 0 : 1;
+      newt[w] = f ? TIER_FULL : 0xFE;
+    }
+    __syncthreads();
+    block_exscan(scanB, count, wsum);
+    for (int r = tid; r < count; r += nt) {
+      const int w = (int)(keys[r] & 0xffffffffu);
+      if (newt[w] != TIER_FULL) newt[w] = scanB[r] < C.k_q ? TIER_QUANT : TIER_EVICT;
+    }
   }
   __syncthreads();
 
@@ -592,8 +658,8 @@ cudaError_t launch_route(const CacheDev &C, int unit0, int n_units, const __nv_b
     attr_set[dev] = true;
   }
   const int prefill = kp != nullptr;
-  route_kernel<<<n_units, RT_THREADS, route_smem_bytes(), s>>>(C, unit0, prefill);
   PromptIO pio{kp, vp, layer};
+  route_kernel<<<n_units, RT_THREADS, route_smem_bytes(), s>>>(C, pio, unit0, prefill);
   if (C.W == 32 && C.bits == 2) return launch_migrate<32, 2>(C, pio, unit0, n_units, mig_blocks, s);
   if (C.W == 64 && C.bits == 4) return launch_migrate<64, 4>(C, pio, unit0, n_units, mig_blocks, s);
   return cudaErrorInvalidValue;

@@ -54,6 +54,11 @@ class Workload:
     switch_every: int = 16    # decode steps between changes of the active planted window
     query_walk_sigma: float = 0.0   # >0: decode queries follow a Gaussian random walk
     key_lognormal_sigma: float = 0.0  # >0: keys of each window scaled by exp(N(0, sigma^2))
+    # routing policy (QEvict App. J / K): ranker 0 cumulative, 1 decayed, 2 p-norm, 3 key norm
+    ranker: int = 0
+    decay: float = 0.99
+    pnorm: float = 3.0
+    no_promotion: int = 0
 
     @property
     def max_len(self) -> int:

@@ -210,7 +210,9 @@ class Lockstep:
                 self.route()
 
     def route(self):
-        # scores before routing: sum of the KV-head partials, against the oracle's cumulative S
+        ranker = getattr(self.wl, "ranker", 0)
+        # before routing: the sum of the KV-head partials is the oracle's cumulative S (ranker 0), or
+        # the attention since the previous event (the other rankers, QEvict App. J Eq. (20))
         if self.per_step:
             for l in self.layers:
                 for b in range(self.B):
@@ -218,15 +220,24 @@ class Lockstep:
                     tot = sg[0].copy()
                     for g in range(1, sg.shape[0]):
                         tot = (tot + sg[g]).astype(np.float32)
-                    close_rel(tot, self.units[(l, b)].S[:self.N], f"scores before event {self.step} layer {l} seq {b}")
-        self.cache.route()   # absorbs the pending steps' masses, then ranks on the collapsed scores
+                    u = self.units[(l, b)]
+                    ref = u.S if ranker == 0 else u.U
+                    close_rel(tot, ref[:self.N], f"scores before event {self.step} layer {l} seq {b}")
+        self.cache.route()   # absorbs the pending steps' masses, then ranks
         torch.cuda.synchronize()
         for l in range(self.L):
             for b in range(self.B):
-                s0 = self.scores(l, b)[0]
-                if not self.per_step and l in self.layers:
-                    close_rel(s0, self.units[(l, b)].S[:self.N], f"scores at event {self.step} layer {l} seq {b}")
-                self.units[(l, b)].route(scores=s0.astype(np.float64))
+                u = self.units[(l, b)]
+                if ranker == 0:
+                    rv = self.scores(l, b)[0]
+                    if not self.per_step and l in self.layers:
+                        close_rel(rv, u.S[:self.N], f"scores at event {self.step} layer {l} seq {b}")
+                    u.route(scores=rv.astype(np.float64))
+                else:
+                    rv = self.cache.region("agg", self._u(l, b), 4 * self.N).view(torch.float32).cpu().numpy()
+                    what = f"rank values at event {self.step} layer {l} seq {b}"
+                    hook = (lambda R, rv=rv, what=what: close_rel(rv, R[:self.N], what)) if l in self.layers else None
+                    u.route(scores=rv.astype(np.float64), rank_hook=hook)
         if self.check_state:
             for l in self.layers:
                 for b in self.state_seqs:

@@ -62,6 +62,17 @@ def test_int4_w64_shapes(lib, shape):
     _run(base.replace(**shape), 24)
 
 
+@pytest.mark.parametrize("policy", [dict(ranker=1), dict(ranker=2), dict(ranker=3), dict(no_promotion=1),
+                                    dict(ranker=1, no_promotion=1), dict(ranker=3, window=64, bits=4)])
+def test_alternative_rankers_and_no_promotion(lib, policy):
+    """QEvict App. J rankers (decayed attention, p-norm, key norm) and App. K's no-promotion policy:
+    rank values, tiers, codes and counters in lockstep with the oracle."""
+    base = synth.workload("tiny_4k", prompt_len=1500, steps=24, n_plant=4, kappa=6.0, key_lognormal_sigma=0.5)
+    ls = _run(base.replace(**policy), 24)
+    if policy.get("no_promotion"):
+        assert ls.cache.counters()["promotions"] == 0
+
+
 def test_two_tier_and_quantized_only(lib):
     """q = 0: Full/Evicted only (two-tier window eviction); q = 1: K_f = 0 (quantised retention)."""
     base = synth.workload("tiny_4k", prompt_len=1200, steps=16, n_plant=4)
