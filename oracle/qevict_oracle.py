@@ -94,6 +94,9 @@ class Config:
     pnorm: float = 3.0
     # QEvict App. K: 1 = quantized windows may be evicted but never return to the full tier
     no_promotion: int = 0
+    # QEvict §4.3: > 0 keeps quantized keys in the pre-RoPE domain (rotate-half RoPE, this base)
+    # and re-rotates them at their positions after dequantisation; 0 = keys carry no rotation
+    rope_base: float = 0.0
 
     @staticmethod
     def from_obj(o, **kw) -> "Config":
@@ -227,6 +230,21 @@ def dequantize_groups(code: np.ndarray, s16: np.ndarray, m16: np.ndarray, axis: 
     return bf16_round(code.astype(np.float32) * s + m)
 
 
+def rope_rotate(x: np.ndarray, cs: np.ndarray, inverse: bool = False) -> np.ndarray:
+    """Rotate-half RoPE of d = 128 vectors (QEvict §4.3 re-applies RoPE after dequantisation).
+
+    x [..., 128]; cs [..., 64, 2] holds (cos, sin) of pos * theta_i for the pairs (i, i + 64),
+    broadcast against x's leading axes.  Forward: x_i c - x_{i+64} s and x_{i+64} c + x_i s;
+    inverse (back to the pre-RoPE domain): x_i c + x_{i+64} s and x_{i+64} c - x_i s.  Float32,
+    every product and every sum rounded on its own (no fused multiply-add)."""
+    x = np.asarray(x, np.float32)
+    a, b = x[..., :64], x[..., 64:]
+    c, sn = np.asarray(cs[..., 0], np.float32), np.asarray(cs[..., 1], np.float32)
+    if inverse:
+        return np.concatenate([a * c + b * sn, b * c - a * sn], axis=-1).astype(np.float32)
+    return np.concatenate([a * c - b * sn, b * c + a * sn], axis=-1).astype(np.float32)
+
+
 @dataclasses.dataclass
 class Ledger:
     """Write-once quantised record of one window (QEvict §4.3, Algorithm 1 Λ_w).
@@ -242,15 +260,22 @@ class Ledger:
     status: int = ACTIVE
     slot: int = -1
 
-    def dequantize(self) -> Tuple[np.ndarray, np.ndarray]:
-        """Returns K_hat, V_hat as [W][H_kv][d] float32 (bf16 values)."""
+    def dequantize(self, cs: Optional[np.ndarray] = None) -> Tuple[np.ndarray, np.ndarray]:
+        """Returns K_hat, V_hat as [W][H_kv][d] float32 (bf16 values).  With cs ([W][64][2], the
+        window's positions) the pre-RoPE keys are re-rotated and rounded to bf16 (QEvict §4.3)."""
         k = dequantize_groups(self.codes_k, self.s_k, self.m_k, axis=1)   # [H][W][d]
         v = dequantize_groups(self.codes_v, self.s_v, self.m_v, axis=2)
-        return k.transpose(1, 0, 2).copy(), v.transpose(1, 0, 2).copy()
+        k = k.transpose(1, 0, 2).copy()
+        if cs is not None:
+            k = bf16_round(rope_rotate(k, np.asarray(cs)[:, None, :, :]))
+        return k, v.transpose(1, 0, 2).copy()
 
 
-def quantize_window(K: np.ndarray, V: np.ndarray, bits: int) -> Ledger:
-    """K, V: [W][H_kv][d] bf16 values as float32."""
+def quantize_window(K: np.ndarray, V: np.ndarray, bits: int, cs: Optional[np.ndarray] = None) -> Ledger:
+    """K, V: [W][H_kv][d] bf16 values as float32.  With cs ([W][64][2]) the keys, which carry their
+    positions' rotation, are first taken back to the pre-RoPE domain and quantised there."""
+    if cs is not None:
+        K = rope_rotate(K, np.asarray(cs)[:, None, :, :], inverse=True)
     kh = np.asarray(K, np.float32).transpose(1, 0, 2)   # [H][W][d]
     vh = np.asarray(V, np.float32).transpose(1, 0, 2)
     ck, sk, mk = quantize_groups(kh, axis=1, bits=bits)   # per (head, channel) over tokens
@@ -335,6 +360,18 @@ class Unit:
         self.f_slot: Dict[int, int] = {}
         self.counters = np.zeros(len(COUNTER_NAMES), np.int64)
         self.last_transitions: Dict[str, List[int]] = {}
+        self.rope: Optional[np.ndarray] = None   # [positions][64][2] (cos, sin), an input
+
+    def set_rope_table(self, table: np.ndarray) -> None:
+        self.rope = np.asarray(table, np.float32)
+
+    def window_cs(self, w: int) -> Optional[np.ndarray]:
+        """(cos, sin) rows of window w's positions, or None when keys carry no rotation."""
+        if self.cfg.rope_base <= 0:
+            return None
+        assert self.rope is not None, "rope_base > 0 needs a rotation table"
+        lo = self.cfg.n_sink + w * self.cfg.window
+        return self.rope[lo:lo + self.cfg.window]
 
     # ---- prefill (QEvict §4.2 last paragraph; §4.3 Eq. (2))
     def prefill_route(self, k: np.ndarray, v: np.ndarray, s0: np.ndarray):
@@ -363,7 +400,7 @@ class Unit:
             if self.z[w] == FULL:
                 Kw, Vw = self.full[w]
             elif self.z[w] == QUANT:
-                Kw, Vw = self.ledger[w].dequantize()
+                Kw, Vw = self.ledger[w].dequantize(self.window_cs(w))
             else:
                 continue
             Ks.append(Kw)
@@ -494,12 +531,12 @@ class Unit:
                     ctr["reactivations"] += 1
                     tr["reactivate"].append(w)
                 else:
-                    self.ledger[w] = quantize_window(src[0], src[1], cfg.bits)
+                    self.ledger[w] = quantize_window(src[0], src[1], cfg.bits, self.window_cs(w))
                     need_ledger.append(w)
                     ctr["first_quant"] += 1
                     tr["quantize"].append(w)
             else:                                  # aged straight into the quantized tier
-                self.ledger[w] = quantize_window(*window_data[w], cfg.bits)
+                self.ledger[w] = quantize_window(*window_data[w], cfg.bits, self.window_cs(w))
                 need_ledger.append(w)
                 ctr["first_quant"] += 1
                 ctr["aged_quant"] += 1
@@ -514,7 +551,7 @@ class Unit:
                 continue
             if was == QUANT:
                 led = self.ledger[w]
-                self.full[w] = led.dequantize()
+                self.full[w] = led.dequantize(self.window_cs(w))
                 led.status = DORMANT
                 ctr["promotions"] += 1
                 tr["promote"].append(w)

@@ -19,9 +19,10 @@ import dataclasses
 import math
 from typing import Optional
 
+import numpy as np
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "workload", "prompt_inputs", "decode_inputs", "seed_of"]
+__all__ = ["Workload", "WORKLOADS", "workload", "prompt_inputs", "decode_inputs", "seed_of", "rope_table"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -59,6 +60,8 @@ class Workload:
     decay: float = 0.99
     pnorm: float = 3.0
     no_promotion: int = 0
+    # rotate-half RoPE base of the keys (0 = keys carry no rotation); see rope_table
+    rope_base: float = 0.0
 
     @property
     def max_len(self) -> int:
@@ -136,6 +139,17 @@ def _plants(wl: Workload, b: int, layer: int, device):
     return blocks.to(device), dirs
 
 
+def _rope(x: torch.Tensor, pos0: int, base: float) -> torch.Tensor:
+    """The model's own position encoding of its queries and keys: rows of x [S][H][d] sit at positions
+    pos0 .. pos0 + S - 1; channel pair (i, i + d/2) is the complex number x_i + j x_{i+d/2}, multiplied
+    by exp(j pos base^(-2i/d)) in complex128."""
+    d = x.shape[-1]
+    theta = base ** (-2.0 * torch.arange(d // 2, dtype=torch.float64, device=x.device) / d)
+    ang = torch.arange(pos0, pos0 + x.shape[0], dtype=torch.float64, device=x.device)[:, None] * theta[None, :]
+    z = torch.complex(x[..., :d // 2].double(), x[..., d // 2:].double()) * torch.polar(torch.ones_like(ang), ang)[:, None, :]
+    return torch.cat([z.real, z.imag], dim=-1).float()
+
+
 def prompt_inputs(wl: Workload, b: int, layer: int, device="cpu", with_queries: bool = True):
     """Prompt tensors of one (sequence, layer): q [P][H_q][d], k and v [P][H_kv][d], all bf16."""
     P, d = wl.prompt_len, wl.d_head
@@ -151,9 +165,12 @@ def prompt_inputs(wl: Workload, b: int, layer: int, device="cpu", with_queries: 
         xi = _randn((nblk,), _gen(wl, b, layer, "lognorm", device), device)
         scale = torch.exp(wl.key_lognormal_sigma * xi).repeat_interleave(wl.window)[:P]
         k = k * scale.view(P, 1, 1)
+    if wl.rope_base > 0:
+        k = _rope(k, 0, wl.rope_base)
     out = {"k": k.to(torch.bfloat16), "v": v.to(torch.bfloat16)}
     if with_queries:
-        out["q"] = _randn((P, wl.h_q, d), _gen(wl, b, layer, "q_prompt", device), device).to(torch.bfloat16)
+        q = _randn((P, wl.h_q, d), _gen(wl, b, layer, "q_prompt", device), device)
+        out["q"] = (_rope(q, 0, wl.rope_base) if wl.rope_base > 0 else q).to(torch.bfloat16)
     return out
 
 
@@ -178,6 +195,9 @@ def decode_inputs(wl: Workload, b: int, layer: int, steps: Optional[int] = None,
         xi = _randn((S, wl.h_q, d), _gen(wl, b, layer, "walk", device), device)
         xi[0] = 0.0
         q = q[0:1] + wl.query_walk_sigma * torch.cumsum(xi, dim=0)
+    if wl.rope_base > 0:   # decode step s sits at position prompt_len + s
+        q = _rope(q, wl.prompt_len, wl.rope_base)
+        k = _rope(k, wl.prompt_len, wl.rope_base)
     return {"q": q.to(torch.bfloat16), "k": k.to(torch.bfloat16), "v": v.to(torch.bfloat16)}
 
 
@@ -188,3 +208,12 @@ def describe(wl: Workload) -> str:
             f"budget={wl.budget_num}/{wl.budget_den} plants={wl.plant_count()} kappa={wl.kappa:g} "
             f"walk={wl.query_walk_sigma:g} lognorm={wl.key_lognormal_sigma:g} "
             f"(context {math.ceil(wl.max_len / 1024)}K)")
+
+
+def rope_table(rows: int, base: float, d: int = 128) -> np.ndarray:
+    """Model input: (cos, sin) of pos * base^(-2i/d) for every position pos < rows and pair
+    i < d/2 of a rotate-half RoPE, computed in float64 and stored as float32 [rows][d/2][2]."""
+    pos = np.arange(rows, dtype=np.float64)[:, None]
+    theta = base ** (-2.0 * np.arange(d // 2, dtype=np.float64) / d)
+    ang = pos * theta[None, :]
+    return np.stack([np.cos(ang), np.sin(ang)], axis=-1).astype(np.float32)
