@@ -70,6 +70,12 @@ typedef struct {
    * quantized windows may be evicted but never return to the full tier (QEvict App. K). */
   int32_t ranker, no_promotion;
   float decay, pnorm;
+  /* Key domain of the Quantized tier (QEvict §4.3, "Cache Execution"): 0 = keys are quantised as
+   * given; 1 = the given keys carry rotate-half RoPE (pairs (i, i + 64), angle pos * theta_i) and
+   * are quantised in the pre-RoPE domain, RoPE being re-applied at the window's positions after
+   * dequantisation (attention and promotion).  rope = 1 needs qevict_set_rope_table before the
+   * first prefill.  reserved0 must be 0. */
+  int32_t rope, reserved0;
 } qevict_config;
 
 /* Byte budget of one (sequence, layer), QEvict §4.1 (constraint), §4.3 Eq. (3), App. B.4 Eq. (7)-(8).
@@ -143,6 +149,7 @@ typedef struct {
   int32_t n_split;       /* decode split-K partitions per (sequence, KV head) */
   int32_t pad_;
   int64_t off_agg, stride_agg;
+  int64_t off_rope;      /* rope = 1: fp32 [max_len][64][2] (cos, sin) table shared by all units */
 } qevict_layout;
 
 typedef struct qevict_cache qevict_cache;
@@ -161,6 +168,16 @@ qevict_status qevict_init_cache(const qevict_config *cfg, void *d_arena, size_t 
 /* Region offsets of the cache tuple inside the arena (see qevict_layout).  Host only. */
 qevict_status qevict_get_layout(const qevict_cache *cache, qevict_layout *out);
 
+/* RoPE table of a rope = 1 cache (QEvict §4.3: quantised keys keep their absolute positions and
+ * are rotated again after dequantisation).  d_table: fp32 [rows][64][2] on the device, row p
+ * holding (cos(p * theta_i), sin(p * theta_i)) for i = 0..63, the angles the caller's model used to
+ * rotate its keys; rows >= max_len.  The first max_len rows are copied into the arena on `stream`
+ * (the caller keeps ownership of d_table).  Keys are taken back with
+ *   x_i c + x_{i+64} s,  x_{i+64} c - x_i s    and rotated with    x_i c - x_{i+64} s,  x_{i+64} c + x_i s,
+ * every product and sum rounded to fp32 on its own.  QEVICT_EINVAL when the cache has rope = 0 or
+ * rows < max_len; call before the first qevict_prefill_route (later calls return QEVICT_ESCHEDULE). */
+qevict_status qevict_set_rope_table(qevict_cache *cache, const float *d_table, int64_t rows, qevict_stream_t stream);
+
 /* Prompt scoring, QEvict §4.2 (last paragraph): for every (sequence, window j starting in the
  * prompt) S0[j] = (1/h_q) sum_h sum_{tau < P} sum_{i in w_j, i <= tau} a_tau^h(i), dense causal
  * attention of every prompt query.  q_prompt [batch][P][h_q][d], k_prompt [batch][P][h_kv][d];
@@ -173,7 +190,8 @@ qevict_status qevict_prefill_scores(const qevict_cache *cache, const void *q_pro
  * recent region, sets the window scores (s0 [batch][ceil((P - n_sink)/window)] fp32, or computed
  * from q_prompt when s0 is NULL), routes all historical prompt windows into F / Q / E and
  * materialises F (bf16 copy) and Q (quantised once).  k_prompt, v_prompt [batch][P][h_kv][d].
- * Must be called exactly once per layer, before any decode step of that layer. */
+ * Must be called exactly once per layer, before any decode step of that layer.  A rope = 1 cache
+ * needs its RoPE table first (QEVICT_ESCHEDULE otherwise). */
 qevict_status qevict_prefill_route(qevict_cache *cache, int32_t layer, const void *k_prompt,
                                    const void *v_prompt, const float *s0, const void *q_prompt,
                                    qevict_stream_t stream);
@@ -262,7 +280,9 @@ qevict_status qevict_get_tuple(const qevict_cache *cache, int32_t layer, int32_t
  * qevict_export_bytes gives its size.  qevict_export_state synchronises `stream` after the copy
  * (QEVICT_ENOMEM when `bytes` is too small).  qevict_import_state loads an export into a cache
  * created with the identical configuration (else QEVICT_EINVAL), synchronises `stream`, and resumes
- * its host bookkeeping (per-layer T, routing events) from the imported meta records. */
+ * its host bookkeeping (per-layer T, routing events) from the imported meta records.  A rope = 1
+ * cache's RoPE table is part of the arena; an export taken before any prefill needs
+ * qevict_set_rope_table again after its import. */
 qevict_status qevict_export_bytes(const qevict_cache *cache, size_t *bytes);
 qevict_status qevict_export_state(const qevict_cache *cache, void *host_buf, size_t bytes, qevict_stream_t stream);
 qevict_status qevict_import_state(qevict_cache *cache, const void *host_buf, size_t bytes, qevict_stream_t stream);

@@ -29,7 +29,7 @@ class Config(ctypes.Structure):
                                              "budget_den")] + \
                [("b_total", ctypes.c_int64), ("prompt_len", ctypes.c_int32), ("max_len", ctypes.c_int32),
                 ("ranker", ctypes.c_int32), ("no_promotion", ctypes.c_int32), ("decay", ctypes.c_float),
-                ("pnorm", ctypes.c_float)]
+                ("pnorm", ctypes.c_float), ("rope", ctypes.c_int32), ("reserved0", ctypes.c_int32)]
 
 
 class BudgetInfo(ctypes.Structure):
@@ -44,7 +44,8 @@ _LAYOUT_REGIONS = ("sink", "ring", "fpool", "ledger", "score", "state", "fslot",
 class Layout(ctypes.Structure):
     _fields_ = [(f"{k}_{r}", ctypes.c_int64) for r in _LAYOUT_REGIONS for k in ("off", "stride")] + \
                [("qblock", ctypes.c_int64), ("arena_bytes", ctypes.c_int64), ("n_split", ctypes.c_int32),
-                ("pad_", ctypes.c_int32), ("off_agg", ctypes.c_int64), ("stride_agg", ctypes.c_int64)]
+                ("pad_", ctypes.c_int32), ("off_agg", ctypes.c_int64), ("stride_agg", ctypes.c_int64),
+                ("off_rope", ctypes.c_int64)]
 
 
 class Tuple(ctypes.Structure):
@@ -75,6 +76,7 @@ def load() -> ctypes.CDLL:
         "qevict_decode_step": [P, I32, P, P, P, P, P],
         "qevict_route": [P, P],
         "qevict_flush_scores": [P, P],
+        "qevict_set_rope_table": [P, P, I64, P],
         "qevict_get_tuple": [P, I32, I32, ctypes.POINTER(Tuple)],
         "qevict_export_bytes": [P, ctypes.POINTER(ctypes.c_size_t)],
         "qevict_export_state": [P, P, ctypes.c_size_t, P],
@@ -100,7 +102,7 @@ def exported_symbols():
             "qevict_prefill_scores", "qevict_prefill_route", "qevict_decode_step", "qevict_route",
             "qevict_read_counters", "qevict_check", "qevict_destroy", "qevict_status_string",
             "qevict_prefill_scores_noalloc", "qevict_flush_scores", "qevict_get_tuple", "qevict_export_bytes",
-            "qevict_export_state", "qevict_import_state"]
+            "qevict_export_state", "qevict_import_state", "qevict_set_rope_table"]
 
 
 def _check(status: int, where: str):
@@ -120,6 +122,10 @@ def make_config(wl, **over) -> Config:
             setattr(c, name, float(over.get(name, getattr(wl, name, 0.0))))
         elif name in ("ranker", "no_promotion"):
             setattr(c, name, int(over.get(name, getattr(wl, name, 0))))
+        elif name == "rope":   # keys carry RoPE and are quantised before it when the workload has a base
+            c.rope = int(over.get("rope", 1 if float(getattr(wl, "rope_base", 0.0) or 0.0) > 0 else 0))
+        elif name == "reserved0":
+            c.reserved0 = 0
         else:
             setattr(c, name, int(over.get(name, getattr(wl, name))))
     return c
@@ -183,6 +189,13 @@ class Cache:
     def prefill_scores(self, q_prompt, k_prompt, s0_out, stream=None):
         _check(load().qevict_prefill_scores(self.handle, _ptr(q_prompt), _ptr(k_prompt), _ptr(s0_out),
                                             _stream(stream)), "qevict_prefill_scores")
+
+    def set_rope_table(self, table, stream=None):
+        """table: fp32 CUDA tensor [rows][64][2] of (cos, sin) per position and channel pair."""
+        if table.dtype != __import__("torch").float32 or not table.is_cuda or not table.is_contiguous():
+            raise QEvictError(EINVAL, "set_rope_table", "table must be a contiguous float32 CUDA tensor")
+        _check(load().qevict_set_rope_table(self.handle, _ptr(table), int(table.shape[0]), _stream(stream)),
+               "qevict_set_rope_table")
 
     def prefill_route(self, layer: int, k_prompt, v_prompt, s0=None, q_prompt=None, stream=None):
         _check(load().qevict_prefill_route(self.handle, layer, _ptr(k_prompt), _ptr(v_prompt), _ptr(s0),

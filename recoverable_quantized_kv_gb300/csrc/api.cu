@@ -36,6 +36,7 @@ struct qevict_cache {
   std::vector<int> prefilled;
   int routes_done;
   int last_decode_layer;        // layer of the last decode enqueued, -1 after any other call
+  int rope_set;                 // rope = 1: the RoPE table has been copied in
 };
 
 namespace {
@@ -63,6 +64,7 @@ qevict_status check_config(const qevict_config *c) {
   if (!((c->window == 32 && c->bits == 2) || (c->window == 64 && c->bits == 4))) return QEVICT_EINVAL;
   if (c->ranker < 0 || c->ranker > 3 || c->no_promotion < 0 || c->no_promotion > 1) return QEVICT_EINVAL;
   if (!(c->decay >= 0.f && c->decay <= 1.f) || !(c->pnorm == 0.f || c->pnorm >= 1.f)) return QEVICT_EINVAL;
+  if (c->rope < 0 || c->rope > 1 || c->reserved0 != 0) return QEVICT_EINVAL;
   if (c->n_sink < 1 || c->n_sink > 16 || c->n_recent < c->window || c->omega < 1 ||
       c->omega > 256)
     return QEVICT_EINVAL;
@@ -162,6 +164,8 @@ void make_plan(const qevict_config *c, const qevict_budget_info *b, Plan *p) {
   C.off_colsum = global(4LL * c->batch * c->h_q * c->prompt_len);
   const int npw = (c->prompt_len - c->n_sink + W - 1) / W;
   p->off_s0buf = global(4LL * c->batch * npw);
+  // rope = 1: max_len rows of the caller's table; the decode kernel reads rows 0..31 in any case
+  C.off_rope = L.off_rope = global(c->rope ? 512LL * std::max(c->max_len, 32) : 16);
   L.qblock = qb;
   L.arena_bytes = off;
   L.n_split = n_split;
@@ -199,6 +203,7 @@ void make_plan(const qevict_config *c, const qevict_budget_info *b, Plan *p) {
   C.no_promotion = c->no_promotion;
   C.decay = c->decay == 0.f ? 0.99f : c->decay;
   C.pnorm = c->pnorm == 0.f ? 3.0f : c->pnorm;
+  C.rope = c->rope;
 }
 
 qevict_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QEVICT_OK : QEVICT_ECUDA; }
@@ -244,6 +249,7 @@ qevict_status qevict_init_cache(const qevict_config *cfg, void *d_arena, size_t 
   c->prefilled.assign(cfg->n_layers, 0);
   c->routes_done = 0;
   c->last_decode_layer = -1;
+  c->rope_set = 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(d_arena, 0, (size_t)p.lay.arena_bytes, s);
   if (e == cudaSuccess) e = qv::launch_init(c->dev, s);
@@ -261,6 +267,17 @@ qevict_status qevict_get_layout(const qevict_cache *cache, qevict_layout *out) {
   return QEVICT_OK;
 }
 
+qevict_status qevict_set_rope_table(qevict_cache *cache, const float *d_table, int64_t rows, qevict_stream_t stream) {
+  if (!cache || !d_table || !cache->cfg.rope || rows < cache->cfg.max_len) return QEVICT_EINVAL;
+  for (int l = 0; l < cache->cfg.n_layers; ++l)
+    if (cache->prefilled[l]) return QEVICT_ESCHEDULE;
+  if (cudaMemcpyAsync(cache->dev.arena + cache->dev.off_rope, d_table, 512 * (size_t)cache->cfg.max_len,
+                      cudaMemcpyDeviceToDevice, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return QEVICT_ECUDA;
+  cache->rope_set = 1;
+  return QEVICT_OK;
+}
+
 qevict_status qevict_prefill_scores(const qevict_cache *cache, const void *q_prompt, const void *k_prompt,
                                     float *s0_out, qevict_stream_t stream) {
   if (!cache || !q_prompt || !k_prompt || !s0_out) return QEVICT_EINVAL;
@@ -273,7 +290,7 @@ qevict_status qevict_prefill_route(qevict_cache *cache, int32_t layer, const voi
                                    const float *s0, const void *q_prompt, qevict_stream_t stream) {
   if (!cache || layer < 0 || layer >= cache->cfg.n_layers || !k_prompt || !v_prompt) return QEVICT_EINVAL;
   if (!s0 && !q_prompt) return QEVICT_EINVAL;
-  if (cache->prefilled[layer]) return QEVICT_ESCHEDULE;
+  if (cache->prefilled[layer] || (cache->cfg.rope && !cache->rope_set)) return QEVICT_ESCHEDULE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const auto *kp = static_cast<const __nv_bfloat16 *>(k_prompt);
   const auto *vp = static_cast<const __nv_bfloat16 *>(v_prompt);
@@ -459,6 +476,8 @@ qevict_status qevict_import_state(qevict_cache *cache, const void *host_buf, siz
     cache->prefilled[l] = m[qv::M_T] > 0 ? 1 : 0;
     cache->t_host[l] = m[qv::M_T];
     if (m[qv::M_T] > 0) cache->routes_done = m[qv::M_NEVENT];
+    // a prefilled rope = 1 cache had its table set, and the table travels inside the arena
+    if (m[qv::M_T] > 0 && cache->cfg.rope) cache->rope_set = 1;
   }
   cache->last_decode_layer = -1;
   return QEVICT_OK;

@@ -38,11 +38,13 @@ struct CacheDev {
   int64_t off_flushctr;            // uint32 [L][B] score-flush arrivals
   int64_t off_rowstat;             // float [B][h_q][P] prefill row log2-sum-exp
   int64_t off_colsum;              // float [B][h_q][P] prefill column sums
+  int64_t off_rope;                // float [max_len][64][2] (cos, sin) of every position (rope = 1)
   // sizes
   int B, L, h_q, h_kv, G, n_sink, n_recent, W, bits, omega;
   int k_f, k_q, n_windows, ring_windows, n_split, max_items, prompt_len, max_len;
   int ranker, no_promotion;
   float decay, pnorm;
+  int rope;                        // 1: Quantized keys are kept before RoPE
 
   // Stable index of a window's mass record between two routing events: 1 + i for the i-th recent
   // window from the first unrouted one, then the Full table entries, then the Quantized ones.
@@ -53,6 +55,7 @@ struct CacheDev {
   __host__ __device__ T *at(int64_t off, int64_t st, int u) const {
     return reinterpret_cast<T *>(arena + off + st * (int64_t)u);
   }
+  __host__ __device__ const float *rope_tab() const { return reinterpret_cast<const float *>(arena + off_rope); }
   __host__ __device__ int *status() const { return reinterpret_cast<int *>(arena + off_status); }
 };
 

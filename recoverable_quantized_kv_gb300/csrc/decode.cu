@@ -13,6 +13,8 @@
 // Softmax is online per warp; per-window masses are kept as log2-sum-exp values, which the last CTA
 // of the (sequence, KV head) to finish (counted with one atomic, no waiting) normalises into the
 // window scores while it merges the splits.
+// With pre-RoPE Quantized keys (QEvict §4.3 "Cache Execution") the kernel variant ROPE rotates the
+// dequantised keys to their positions in registers before the key MMAs.
 #include "cache_dev.cuh"
 #include "common.cuh"
 
@@ -23,11 +25,15 @@ constexpr int DEC_CONSUMERS = DEC_WARPS - 1;
 constexpr int DEC_SLOTS = 36;          // CTA-wide ring of 4 KB slots filled by bulk copies
 constexpr int DEC_STAGE_BYTES = 4096;
 // per consumer warp: the key look-up table of the window in hand (INT2: bf16 bytes of the 4 values
-// of 128 channels; INT4: fp32 scale and offset of 128 channels), 8 k-steps x 4 lane classes x 32 B
+// of 128 channels; INT4: fp32 scale and offset of 128 channels), 8 k-steps x 4 lane classes x 32 B,
+// then (ROPE) the cos/sin rows of the window's first position of each 32-token half.  Both live in
+// the warp's own output region of the CTA merge, which the warp writes only after its last window.
 constexpr int DEC_TBL_BYTES = 1024;
-constexpr int DEC_TBL_OFF = DEC_SLOTS * DEC_STAGE_BYTES;
 // CTA merge: running max / sum / rescale per (warp, head), CTA max, and every warp's outputs
+constexpr int DEC_CO_OFF = (3 * DEC_CONSUMERS * 8 + 16) * 4;   // bytes before the outputs
 constexpr int DEC_MRG_FLOATS = 3 * DEC_CONSUMERS * 8 + 16 + DEC_CONSUMERS * 128 * 8;
+// ROPE: cos/sin of the in-window offsets 0..31, 16 KB shared by the consumer warps
+constexpr int DEC_REL_BYTES = 32 * 64 * 2 * 4;
 
 // Chunk stream geometry of one (window, bits) format.  A bf16 window streams its K block then its
 // V block in 4 KB chunks; a Quantized window streams its ledger record (codes, then parameters).
@@ -35,7 +41,7 @@ constexpr int DEC_MRG_FLOATS = 3 * DEC_CONSUMERS * 8 + 16 + DEC_CONSUMERS * 128 
 // DEC_CONSUMERS * MAX_CHUNKS chunks past the first one not yet issued.  Giving every slot PHASES
 // "full" barriers used in turn keeps every parity wait unambiguous: the chunk PHASES * DEC_SLOTS
 // earlier on the same barrier has always landed by then.
-template <int W, int BITS>
+template <int W, int BITS, bool ROPE>
 struct DecGeo {
   static constexpr int HALVES = W / 32;                        // 32-token halves of a window
   static constexpr int KCH = W / 16;                           // 4 KB chunks of one K (or V) block
@@ -44,11 +50,15 @@ struct DecGeo {
   static constexpr int MAX_CHUNKS = BF_CHUNKS > Q_CHUNKS ? BF_CHUNKS : Q_CHUNKS;
   static constexpr int PHASES = 1 + (DEC_CONSUMERS * MAX_CHUNKS + DEC_SLOTS - 1) / DEC_SLOTS;
   static constexpr int FULL = PHASES * DEC_SLOTS;
-  static constexpr int BAR_OFF = DEC_TBL_OFF + DEC_CONSUMERS * DEC_TBL_BYTES;
+  static constexpr int REL_OFF = DEC_SLOTS * DEC_STAGE_BYTES;
+  static constexpr int BAR_OFF = REL_OFF + (ROPE ? DEC_REL_BYTES : 0);
   static constexpr int MRG_OFF = BAR_OFF + (FULL + DEC_SLOTS) * 8;
   static constexpr int SMEM = MRG_OFF + DEC_MRG_FLOATS * 4;
   static_assert((PHASES - 1) * DEC_SLOTS >= DEC_CONSUMERS * MAX_CHUNKS, "too few full barriers per slot");
   static_assert(W == 32 || Geo<W, BITS>::CODE_BYTES == DEC_STAGE_BYTES, "INT4 code blocks fill one chunk each");
+  static_assert(DEC_TBL_BYTES + HALVES * 512 <= 128 * 8 * 4, "per-warp tables fit the warp's output region");
+  static_assert(SMEM <= 232448, "shared memory per CTA");
+  static_assert(MRG_OFF % 16 == 0 && DEC_CO_OFF % 16 == 0, "16-byte aligned per-warp tables");
 };
 
 // Work list of one (sequence, KV head): item 0 = the sink tokens, items 1..nL = recent windows
@@ -212,11 +222,35 @@ __device__ __forceinline__ uint32_t pack_half(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
-template <int W, int BITS>
+__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+__device__ __forceinline__ float bf_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+
+// cos/sin of the in-window offset tt for channels 16jj + 2tl + 8hh and + 1, from the offset table:
+// 16 B per (offset, k-step jj, channel half, lane class), the two halves swapped on odd offsets so
+// that the lanes of neighbouring token rows read different banks
+__device__ __forceinline__ float4 rel_cs(const uint8_t *rel, int tt, int jj, int hh, int tl) {
+  return *reinterpret_cast<const float4 *>(rel + ((((tt * 4 + jj) * 2 + (hh ^ (tt & 1))) * 4 + tl) * 16));
+}
+
+// RoPE of one token's channel pairs (i, i + 64) and (i + 1, i + 65) (QEvict §4.3: RoPE re-applied
+// after dequantisation): a0, a1 are the pre-RoPE values of channels i, i + 1 and b0, b1 of i + 64,
+// i + 65.  The angle of position p0 + tt comes by angle addition from the window's row cb (cos, sin of
+// p0 for i and i + 1) and the offset's row rt; the rotation x_i c - x_{i+64} s, x_{i+64} c + x_i s
+// rounds every product and sum on its own.  ka, kb: the bf16 pairs (i, i + 1) and (i + 64, i + 65).
+__device__ __forceinline__ void rope_rot(float a0, float a1, float b0, float b1, const float4 &cb, const float4 &rt,
+                                         uint32_t &ka, uint32_t &kb) {
+  const float c0 = __fmaf_rn(cb.x, rt.x, -__fmul_rn(cb.y, rt.y)), s0 = __fmaf_rn(cb.y, rt.x, __fmul_rn(cb.x, rt.y));
+  const float c1 = __fmaf_rn(cb.z, rt.z, -__fmul_rn(cb.w, rt.w)), s1 = __fmaf_rn(cb.w, rt.z, __fmul_rn(cb.z, rt.w));
+  ka = pack_bf16(__fsub_rn(__fmul_rn(a0, c0), __fmul_rn(b0, s0)), __fsub_rn(__fmul_rn(a1, c1), __fmul_rn(b1, s1)));
+  kb = pack_bf16(__fadd_rn(__fmul_rn(b0, c0), __fmul_rn(a0, s0)), __fadd_rn(__fmul_rn(b1, c1), __fmul_rn(a1, s1)));
+}
+
+template <int W, int BITS, bool ROPE>
 __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDev C, const DecodeIO io) {
   static_assert((W == 32 && BITS == 2) || (W == 64 && BITS == 4), "formats: W=32 INT2, W=64 INT4");
   using Gm = Geo<W, BITS>;
-  using Dg = DecGeo<W, BITS>;
+  using Dg = DecGeo<W, BITS, ROPE>;
   constexpr int NMT = 2;                 // 16-token groups of a 32-token half
   constexpr int HALVES = Dg::HALVES;
   constexpr int KCH = Dg::KCH, BFC = Dg::BF_CHUNKS, QCH = Dg::Q_CHUNKS;
@@ -279,7 +313,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   };
 
   uint8_t *slots = smem;
-  uint8_t *tbl = smem + DEC_TBL_OFF + (warp < DEC_CONSUMERS ? warp : 0) * DEC_TBL_BYTES;
+  uint8_t *tbl = smem + Dg::MRG_OFF + DEC_CO_OFF + (warp < DEC_CONSUMERS ? warp : 0) * (D * 8 * 4);
+  uint8_t *rel = smem + Dg::REL_OFF;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + Dg::BAR_OFF);   // [Dg::FULL]
   uint64_t *empty = full + Dg::FULL;                                    // [DEC_SLOTS]
   __shared__ int q_next;    // next queue position to hand to a consumer warp
@@ -404,6 +439,16 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
       qb[j][0] = gl < G ? ldg32(qh + 16 * j + 2 * tl) : 0u;
       qb[j][1] = gl < G ? ldg32(qh + 16 * j + 2 * tl + 8) : 0u;
     }
+  }
+  if constexpr (ROPE) {
+    // the offset table: rows 0..31 of the RoPE table, laid out as rel_cs reads it
+    const float *tab = C.rope_tab();
+    for (int k = threadIdx.x; k < DEC_REL_BYTES / 16; k += DEC_CONSUMERS * 32) {
+      const int t = k >> 5, jj = (k >> 3) & 3, t4 = k & 3, hh = ((k >> 2) & 1) ^ (t & 1);
+      *reinterpret_cast<float4 *>(rel + 16 * k) =
+          __ldg(reinterpret_cast<const float4 *>(tab + ((size_t)t * 64 + 16 * jj + 2 * t4 + 8 * hh) * 2));
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(DEC_CONSUMERS * 32) : "memory");   // consumer warps only
   }
   while (ok) {
     int pos = 0;
@@ -554,6 +599,11 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
       float s[NMT][4];
 #pragma unroll
       for (int mt = 0; mt < NMT; ++mt) s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
+      float4 csr;   // ROPE: this lane's 16 B of the RoPE row of the window's first position
+      if constexpr (ROPE) {
+        const int wq = __ldg(&qtab[it - 1 - nL - nF].x);
+        csr = __ldg(reinterpret_cast<const float4 *>(C.rope_tab() + (size_t)(C.n_sink + wq * W) * D) + lane);
+      }
       const uint8_t *ch = wait_chunk(c0);
       // key tables: channel d = 4*lane + k, values bf16(fp32(c*s + m)), c = 0..3, split in lo / hi bytes
       {
@@ -574,8 +624,37 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
           tw[base + 2] = __byte_perm(p01, p23, 0x7531);
         }
       }
+      if constexpr (ROPE) *reinterpret_cast<float4 *>(tbl + DEC_TBL_BYTES + 16 * lane) = csr;
       __syncwarp();
       const uint4 kcw0 = lds128(ch + lane * 16), kcw1 = lds128(ch + 512 + lane * 16);
+      if constexpr (ROPE) {
+        // k-steps jj and jj + 4 hold the RoPE partners (channels c and c + 64) in the same registers
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const uint4 TA0 = lds128(tbl + (jj * 4 + tl) * 32), TB0 = lds128(tbl + (jj * 4 + tl) * 32 + 16);
+          const uint4 TA1 = lds128(tbl + ((jj + 4) * 4 + tl) * 32), TB1 = lds128(tbl + ((jj + 4) * 4 + tl) * 32 + 16);
+          const uint8_t *csw = tbl + DEC_TBL_BYTES + (16 * jj + 2 * tl) * 8;
+          const float4 cb0 = *reinterpret_cast<const float4 *>(csw), cb1 = *reinterpret_cast<const float4 *>(csw + 64);
+#pragma unroll
+          for (int mt = 0; mt < NMT; ++mt) {
+            // k-step j sits in code word j / 2, low half for even j
+            const uint4 &kc = mt == 0 ? kcw0 : kcw1;
+            const uint32_t wa = word_of(kc, jj >> 1) >> (16 * (jj & 1));
+            const uint32_t wb = word_of(kc, 2 + (jj >> 1)) >> (16 * (jj & 1));
+            uint32_t ka[4], kb[4];
+            lut_k_regs((wa & 0x3333u) | 0x4040u, ((wa >> 2) & 0x3333u) | 0x4040u, TA0, TB0, ka[0], ka[1], ka[2], ka[3]);
+            lut_k_regs((wb & 0x3333u) | 0x4040u, ((wb >> 2) & 0x3333u) | 0x4040u, TA1, TB1, kb[0], kb[1], kb[2], kb[3]);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+              const int tt = 16 * mt + gl + 8 * (r & 1);
+              rope_rot(bf_lo(ka[r]), bf_hi(ka[r]), bf_lo(kb[r]), bf_hi(kb[r]), (r >> 1) ? cb1 : cb0,
+                       rel_cs(rel, tt, jj, r >> 1, tl), ka[r], kb[r]);
+            }
+            mma_bf16(s[mt], ka[0], ka[1], ka[2], ka[3], qb[jj][0], qb[jj][1]);
+            mma_bf16(s[mt], kb[0], kb[1], kb[2], kb[3], qb[jj + 4][0], qb[jj + 4][1]);
+          }
+        }
+      } else {
 #pragma unroll
       for (int jp = 0; jp < 4; ++jp) {
         // selectors of both fields of a code word at once: k-step 2jp in the low half, 2jp+1 high
@@ -598,6 +677,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
             mma_bf16(s[mt], a0, a1, a2, a3, qb[j][0], qb[j][1]);
           }
         }
+      }
       }
 #pragma unroll
       for (int mt = 0; mt < NMT; ++mt) {
@@ -639,6 +719,13 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
       add_half_mass();
     } else {
       // ---------------- Quantized window, W = 64: INT4 codes; chunks K codes | V codes | parameters
+      float4 csr[HALVES];   // ROPE: this lane's 16 B of the RoPE rows of each half's first position
+      if constexpr (ROPE) {
+        const int wq = __ldg(&qtab[it - 1 - nL - nF].x);
+#pragma unroll
+        for (int hv = 0; hv < HALVES; ++hv)
+          csr[hv] = __ldg(reinterpret_cast<const float4 *>(C.rope_tab() + (size_t)(C.n_sink + wq * W + 32 * hv) * D) + lane);
+      }
       const uint8_t *kch = wait_chunk(c0);
       const uint8_t *vch = wait_chunk(c0 + 1);
       const uint8_t *pch = wait_chunk(c0 + 2);
@@ -658,6 +745,11 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
           tf[base + 4] = (k & 1) ? h2f_hi(mw) : h2f_lo(mw);
         }
       }
+      if constexpr (ROPE) {
+#pragma unroll
+        for (int hv = 0; hv < HALVES; ++hv)
+          *reinterpret_cast<float4 *>(tbl + DEC_TBL_BYTES + hv * 512 + 16 * lane) = csr[hv];
+      }
       __syncwarp();
       const __half *vsp = reinterpret_cast<const __half *>(pch + (Gm::OFF_VS - 2 * Gm::CODE_BYTES));
       const __half *vmp = reinterpret_cast<const __half *>(pch + (Gm::OFF_VM - 2 * Gm::CODE_BYTES));
@@ -673,6 +765,34 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
           const int tg = 2 * hv + mt;
           const uint4 w03 = lds128(kch + (((2 * tg) * 32 + lane) * 4) * 4);
           const uint4 w47 = lds128(kch + (((2 * tg + 1) * 32 + lane) * 4) * 4);
+          if constexpr (ROPE) {
+            // pre-RoPE keys bf16(fp32(c * s + m)), rotated to their positions; k-steps jj and jj + 4
+            // hold the RoPE partners in the same registers
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const uint32_t wa = word_of(w03, jj), wb = word_of(w47, jj);
+              const uint32_t Ea = wa & 0x0F0F0F0Fu, Oa = (wa >> 4) & 0x0F0F0F0Fu;
+              const uint32_t Eb = wb & 0x0F0F0F0Fu, Ob = (wb >> 4) & 0x0F0F0F0Fu;
+              const float4 sa = *reinterpret_cast<const float4 *>(tbl + (jj * 4 + tl) * 32);
+              const float4 ma = *reinterpret_cast<const float4 *>(tbl + (jj * 4 + tl) * 32 + 16);
+              const float4 sb = *reinterpret_cast<const float4 *>(tbl + ((jj + 4) * 4 + tl) * 32);
+              const float4 mb = *reinterpret_cast<const float4 *>(tbl + ((jj + 4) * 4 + tl) * 32 + 16);
+              const uint8_t *csw = tbl + DEC_TBL_BYTES + hv * 512 + (16 * jj + 2 * tl) * 8;
+              const float4 cb0 = *reinterpret_cast<const float4 *>(csw), cb1 = *reinterpret_cast<const float4 *>(csw + 64);
+              uint32_t ka[4], kb[4];
+#pragma unroll
+              for (int r = 0; r < 4; ++r) {
+                const bool h8 = r >= 2;   // channels 2t + 8, 2t + 9
+                const float a0 = bf_round(__fmaf_rn(nib_f(Ea, r), h8 ? sa.z : sa.x, h8 ? ma.z : ma.x));
+                const float a1 = bf_round(__fmaf_rn(nib_f(Oa, r), h8 ? sa.w : sa.y, h8 ? ma.w : ma.y));
+                const float b0 = bf_round(__fmaf_rn(nib_f(Eb, r), h8 ? sb.z : sb.x, h8 ? mb.z : mb.x));
+                const float b1 = bf_round(__fmaf_rn(nib_f(Ob, r), h8 ? sb.w : sb.y, h8 ? mb.w : mb.y));
+                rope_rot(a0, a1, b0, b1, h8 ? cb1 : cb0, rel_cs(rel, 16 * mt + gl + 8 * (r & 1), jj, r >> 1, tl), ka[r], kb[r]);
+              }
+              mma_bf16(s[mt], ka[0], ka[1], ka[2], ka[3], qb[jj][0], qb[jj][1]);
+              mma_bf16(s[mt], kb[0], kb[1], kb[2], kb[3], qb[jj + 4][0], qb[jj + 4][1]);
+            }
+          } else {
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const uint32_t w = word_of(j < 4 ? w03 : w47, j & 3);
@@ -684,6 +804,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
             const uint32_t a2 = pack_bf16(__fmaf_rn(nib_f(E, 2), sc.z, mn.z), __fmaf_rn(nib_f(Od, 2), sc.w, mn.w));
             const uint32_t a3 = pack_bf16(__fmaf_rn(nib_f(E, 3), sc.z, mn.z), __fmaf_rn(nib_f(Od, 3), sc.w, mn.w));
             mma_bf16(s[mt], a0, a1, a2, a3, qb[j][0], qb[j][1]);
+          }
           }
         }
 #pragma unroll
@@ -857,10 +978,10 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
 
 int decode_warps() { return DEC_WARPS; }
 
-template <int W, int BITS>
+template <int W, int BITS, bool ROPE>
 static cudaError_t launch_decode_fmt(const CacheDev &C, const DecodeIO &io, cudaStream_t stream) {
-  using Dg = DecGeo<W, BITS>;
-  auto kern = decode_kernel<W, BITS>;
+  using Dg = DecGeo<W, BITS, ROPE>;
+  auto kern = decode_kernel<W, BITS, ROPE>;
   static bool attr_set[64] = {};   // per device: the dynamic shared memory opt-in of this kernel
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -885,8 +1006,10 @@ static cudaError_t launch_decode_fmt(const CacheDev &C, const DecodeIO &io, cuda
 }
 
 cudaError_t launch_decode(const CacheDev &C, const DecodeIO &io, cudaStream_t stream) {
-  if (C.W == 32 && C.bits == 2) return launch_decode_fmt<32, 2>(C, io, stream);
-  if (C.W == 64 && C.bits == 4) return launch_decode_fmt<64, 4>(C, io, stream);
+  if (C.W == 32 && C.bits == 2)
+    return C.rope ? launch_decode_fmt<32, 2, true>(C, io, stream) : launch_decode_fmt<32, 2, false>(C, io, stream);
+  if (C.W == 64 && C.bits == 4)
+    return C.rope ? launch_decode_fmt<64, 4, true>(C, io, stream) : launch_decode_fmt<64, 4, false>(C, io, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -15,6 +15,8 @@
 // move_kernel: one CTA per (task, KV head): promotion (ledger -> bf16 F slot) or a copy of an
 //   aged window into its F slot.  Runs after quant_kernel so sources are read before any freed F
 //   slot is rewritten.
+// With pre-RoPE keys (rope = 1, QEvict §4.3 "Cache Execution") quant_kernel first takes a window's
+// keys back to the pre-RoPE domain at its positions, and move_kernel rotates rebuilt keys forward.
 #include "cache_dev.cuh"
 #include "common.cuh"
 
@@ -450,6 +452,19 @@ __global__ void __launch_bounds__(MIG_THREADS) quant_kernel(const CacheDev C, co
     load_window<W>(C, pio, unit, b, g, tk.y, tk.z, xk, xv);
     for (int i = threadIdx.x; i < 2 * Gm::CODE_BYTES / 4; i += blockDim.x) cw[i] = 0u;
     __syncthreads();
+    if (C.rope) {
+      // keys back to the pre-RoPE domain at the window's positions (QEvict §4.3), pairs (i, i + 64):
+      // x_i c + x_{i+64} s and x_{i+64} c - x_i s, each product and sum rounded on its own
+      const float *cs = C.rope_tab() + (size_t)(C.n_sink + tk.x * W) * D;
+      for (int idx = tid; idx < W * (D / 2); idx += blockDim.x) {
+        const int tok = idx / (D / 2), i = idx % (D / 2);
+        const float c = cs[tok * D + 2 * i], sn = cs[tok * D + 2 * i + 1];
+        const float a = xk[tok][i], bb = xk[tok][i + D / 2];
+        xk[tok][i] = __fadd_rn(__fmul_rn(a, c), __fmul_rn(bb, sn));
+        xk[tok][i + D / 2] = __fsub_rn(__fmul_rn(bb, c), __fmul_rn(a, sn));
+      }
+      __syncthreads();
+    }
     uint8_t *blk = ledger + ((size_t)tk.w * C.h_kv + g) * Gm::QB;
     // scatter a code into its fragment-native position (shared-memory words, copied out below)
     auto put = [&](bool is_v, int tok, int dim, unsigned c) {
@@ -531,17 +546,37 @@ __global__ void __launch_bounds__(MIG_THREADS) move_kernel(const CacheDev C, con
       const __half *km = reinterpret_cast<const __half *>(led + Gm::OFF_KM);
       const __half *vsp = reinterpret_cast<const __half *>(led + Gm::OFF_VS);
       const __half *vmp = reinterpret_cast<const __half *>(led + Gm::OFF_VM);
-      for (int idx = tid; idx < 2 * W * D; idx += blockDim.x) {
-        const bool is_v = idx >= W * D;
-        const int e = is_v ? idx - W * D : idx, tok = e / D, dim = e % D;
+      auto dq = [&](bool is_v, int tok, int dim) -> float {
         int byte, shift;
         code_pos<BITS>(is_v, tok, dim, byte, shift);
         const float c = (float)((led[byte + (is_v ? Gm::OFF_VCODE : 0)] >> shift) & ((1u << BITS) - 1u));
         const float s = __half2float(is_v ? vsp[tok] : ks[dim]);
         const float m = __half2float(is_v ? vmp[tok] : km[dim]);
-        const __nv_bfloat16 x = __float2bfloat16_rn(__fmaf_rn(c, s, m));
-        if (is_v) dv[fnv_index(tok, dim)] = x;
-        else dk[fnk_index(tok, dim)] = x;
+        return __bfloat162float(__float2bfloat16_rn(__fmaf_rn(c, s, m)));
+      };
+      if (!C.rope) {
+        for (int idx = tid; idx < 2 * W * D; idx += blockDim.x) {
+          const bool is_v = idx >= W * D;
+          const int e = is_v ? idx - W * D : idx, tok = e / D, dim = e % D;
+          const __nv_bfloat16 x = __float2bfloat16_rn(dq(is_v, tok, dim));
+          if (is_v) dv[fnv_index(tok, dim)] = x;
+          else dk[fnk_index(tok, dim)] = x;
+        }
+      } else {
+        for (int idx = tid; idx < W * D; idx += blockDim.x) {
+          const int tok = idx / D, dim = idx % D;
+          dv[fnv_index(tok, dim)] = __float2bfloat16_rn(dq(true, tok, dim));
+        }
+        // pre-RoPE keys rotated back to the window's positions (QEvict §4.3), then bf16:
+        // x_i c - x_{i+64} s and x_{i+64} c + x_i s, each product and sum rounded on its own
+        const float *cs = C.rope_tab() + (size_t)(C.n_sink + tk.x * W) * D;
+        for (int idx = tid; idx < W * (D / 2); idx += blockDim.x) {
+          const int tok = idx / (D / 2), i = idx % (D / 2);
+          const float c = cs[tok * D + 2 * i], sn = cs[tok * D + 2 * i + 1];
+          const float a = dq(false, tok, i), bb = dq(false, tok, i + D / 2);
+          dk[fnk_index(tok, i)] = __float2bfloat16_rn(__fsub_rn(__fmul_rn(a, c), __fmul_rn(bb, sn)));
+          dk[fnk_index(tok, i + D / 2)] = __float2bfloat16_rn(__fadd_rn(__fmul_rn(bb, c), __fmul_rn(a, sn)));
+        }
       }
     } else if (src_kind == SRC_RING) {
       const int rs = tk.z % C.ring_windows;

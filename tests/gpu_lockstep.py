@@ -29,9 +29,12 @@ def close_rel(gpu, ref, what, rel=REL_TOL, floor_frac=1e-6, abs_small=1e-9):
 
 
 class Lockstep:
-    def __init__(self, wl, check_state=True, oracle_prefill_scores=True, layers=None, per_step=True, state_seqs=None):
+    def __init__(self, wl, check_state=True, oracle_prefill_scores=True, layers=None, per_step=True, state_seqs=None,
+                 churn=None):
         """per_step: flush the scores after every decode step and check that step's window masses;
-        otherwise scores absorb the steps' masses only inside route(), checked after routing."""
+        otherwise scores absorb the steps' masses only inside route(), checked after routing.
+        churn: a seed; before every routing event the scores are replaced by seeded random values
+        (cumulative ranker only), so that windows move between the tiers in both directions."""
         self.wl = wl
         self.cfg = binding.make_config(wl)
         self.cache = binding.Cache(self.cfg)
@@ -52,6 +55,13 @@ class Lockstep:
         # sequences whose full tier state / tables / window data are compared (outputs, masses, scores
         # and counters are compared for every sequence)
         self.state_seqs = list(range(self.B)) if state_seqs is None else state_seqs
+        self.churn = churn
+        # pre-RoPE Quantized keys: both sides get the same (cos, sin) table, a model input
+        if getattr(wl, "rope_base", 0.0) > 0:
+            table = synth.rope_table(wl.max_len, wl.rope_base)
+            for u in self.units.values():
+                u.set_rope_table(table)
+            self.cache.set_rope_table(torch.from_numpy(table).cuda())
 
     # ---- views of one unit's state
     def _u(self, l, b):
@@ -223,6 +233,16 @@ class Lockstep:
                     u = self.units[(l, b)]
                     ref = u.S if ranker == 0 else u.U
                     close_rel(tot, ref[:self.N], f"scores before event {self.step} layer {l} seq {b}")
+        if self.churn is not None:
+            assert ranker == 0
+            rng = np.random.default_rng([self.churn, self.step])
+            H = self.wl.h_kv
+            for l in range(self.L):
+                for b in range(self.B):
+                    forced = torch.zeros(H, self.N, dtype=torch.float32)
+                    forced[0] = torch.from_numpy((rng.random(self.N) * 10).astype(np.float32))
+                    self.cache.region("score", self._u(l, b), 4 * H * self.N).view(torch.float32).copy_(
+                        forced.view(-1).cuda())
         self.cache.route()   # absorbs the pending steps' masses, then ranks
         torch.cuda.synchronize()
         for l in range(self.L):

@@ -73,6 +73,44 @@ def test_alternative_rankers_and_no_promotion(lib, policy):
         assert ls.cache.counters()["promotions"] == 0
 
 
+@pytest.mark.parametrize("fmt", [dict(), dict(window=64, bits=4, prompt_len=3000), dict(h_q=16, h_kv=2, n_sink=16, batch=2, n_recent=64)])
+def test_rope_domain_keys(lib, fmt):
+    """QEvict §4.3 "Cache Execution": the keys carry RoPE; Quantized keys are stored before it and
+    rotated back to their positions after dequantisation, in attention and on promotion.  Codes,
+    parameters and promoted bf16 windows bit-exact, outputs and masses within tolerance; forced score
+    churn moves windows both ways."""
+    base = synth.workload("tiny_4k", prompt_len=1500, steps=32, n_plant=4, kappa=6.0, rope_base=10000.0)
+    ls = _run(base.replace(**fmt), 32, churn=7)
+    c = ls.cache.counters()
+    assert c["promotions"] > 0 and c["demotions"] > 0 and c["first_quant"] > 0
+
+
+def test_rope_table_rules(lib):
+    """The RoPE table is required before the first prefill of a rope cache, and refused for a cache
+    without RoPE, with too few rows, or after a prefill."""
+    wl = synth.workload("tiny_4k", prompt_len=600, steps=16, n_plant=2, budget_num=60, rope_base=10000.0)
+    table = torch.from_numpy(synth.rope_table(wl.max_len, wl.rope_base)).cuda()
+    p = synth.prompt_inputs(wl, 0, 0)
+    s0 = torch.rand(1, O.prompt_windows(O.Config.from_obj(wl)), device="cuda")
+    plain = binding.Cache(binding.make_config(wl, rope=0))
+    with pytest.raises(binding.QEvictError) as e:
+        plain.set_rope_table(table)
+    assert e.value.status == binding.EINVAL
+    c = binding.Cache(binding.make_config(wl))
+    with pytest.raises(binding.QEvictError) as e:
+        c.set_rope_table(table[:wl.max_len - 1].contiguous())
+    assert e.value.status == binding.EINVAL
+    with pytest.raises(binding.QEvictError) as e:
+        c.prefill_route(0, p["k"][None].cuda(), p["v"][None].cuda(), s0=s0)
+    assert e.value.status == binding.ESCHEDULE
+    c.set_rope_table(table)
+    c.prefill_route(0, p["k"][None].cuda(), p["v"][None].cuda(), s0=s0)
+    with pytest.raises(binding.QEvictError) as e:
+        c.set_rope_table(table)
+    assert e.value.status == binding.ESCHEDULE
+    c.check()
+
+
 def test_two_tier_and_quantized_only(lib):
     """q = 0: Full/Evicted only (two-tier window eviction); q = 1: K_f = 0 (quantised retention)."""
     base = synth.workload("tiny_4k", prompt_len=1200, steps=16, n_plant=4)
@@ -126,6 +164,8 @@ def test_full_size_llama_shape(lib):
     ("drift_16k", dict(n_layers=1, steps=24), 24, True),
     # the 131K point in the INT4 / 64-token-window format
     ("long_131k", dict(n_layers=1, batch=1, steps=8, window=64, bits=4), 8, False),
+    # pre-RoPE Quantized keys at positions up to 131K (RoPE base 500000)
+    ("long_131k", dict(n_layers=1, batch=1, steps=8, rope_base=500000.0), 8, False),
 ])
 def test_full_size_workloads(lib, name, over, steps, check_state):
     """The other workloads at their full per-layer shapes (one layer each), in lockstep: outputs,
