@@ -45,6 +45,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample-steps", type=int, default=8)
+    ap.add_argument("--rope-base", type=float, default=0.0,
+                    help="keys carry RoPE with this base and Quantized keys are kept before it (GPU arm only)")
     ap.add_argument("--layers", type=int, default=None,
                     help="run the workload with fewer layers (a smaller case for profiler captures; "
                          "the JSON line then reports that layer count)")
@@ -270,14 +272,18 @@ def run_gpu(args, rank, world):
     binding.load()
     dev = torch.device("cuda", torch.cuda.current_device())
     wl = synth.workload(args.workload) if args.layers is None else synth.workload(args.workload, n_layers=args.layers)
+    if args.rope_base > 0:
+        wl = wl.replace(rope_base=args.rope_base)
     K, Wm = args.steps, args.warmup
     Om = wl.omega
     K_kern = 2 * Om
     K_e2e = 0 if args.no_e2e else K
-    total = Wm + K_kern + Om + K + K_e2e
+    total = Wm + (Om - 1) + K_kern + Om + K + K_e2e   # (Om - 1): steps that realign to a routing event
     steps_cap = max(wl.steps, int(math.ceil(total / Om) * Om) + Om)
     cfg = binding.make_config(wl, max_len=wl.prompt_len + steps_cap)
     cache = binding.Cache(cfg, device=dev)
+    if wl.rope_base > 0:
+        cache.set_rope_table(torch.from_numpy(synth.rope_table(cfg.max_len, wl.rope_base)).to(dev))
     bud = cache.bud
     L, B = wl.n_layers, wl.batch
     stream = torch.cuda.Stream(device=dev)      # graphs cannot be captured on the legacy default stream
@@ -356,8 +362,10 @@ def run_gpu(args, rank, world):
             ms.append(cache.arena[off:off + 64].view(torch.int32).cpu().numpy().copy())
         return ms
 
-    # ---- warm-up (untimed)
+    # ---- warm-up (untimed), then up to the next routing event so that every later phase starts on one
     for _ in range(Wm):
+        one_step(state["step"])
+    while state["step"] % Om:
         one_step(state["step"])
     torch.cuda.synchronize()
 
@@ -485,7 +493,7 @@ def run_gpu(args, rank, world):
                    "prompt_len": wl.prompt_len, "decode_steps_cached": steps_cap, "window": wl.window,
                    "bits": wl.bits, "omega": Om, "budget": f"{wl.budget_num}/{wl.budget_den}",
                    "q": f"{wl.q_num}/{wl.q_den}", "k_f": bud.k_f, "k_q": bud.k_q,
-                   "parallelism": f"replicas x{world}",
+                   "parallelism": f"replicas x{world}", "rope_base": wl.rope_base,
                    "l2": "inputs larger than L2: each step streams every layer's cache (%.0f MB)" %
                          (bytes_per_step / 1e6)},
         "hbm_gbs_step": bytes_per_step / (ms_step / 1e3) / 1e9,
