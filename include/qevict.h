@@ -287,6 +287,60 @@ qevict_status qevict_export_bytes(const qevict_cache *cache, size_t *bytes);
 qevict_status qevict_export_state(const qevict_cache *cache, void *host_buf, size_t bytes, qevict_stream_t stream);
 qevict_status qevict_import_state(qevict_cache *cache, const void *host_buf, size_t bytes, qevict_stream_t stream);
 
+/* Routing diagnostics against a FullKV run, QEvict App. I and App. K.  Two caches decode the same
+ * inputs: `policy`, the cache evaluated (cumulative ranker, ranker = 0), and `fullkv`, a cache of the
+ * same shapes whose budget keeps every window Full (its k_f >= n_windows), so its per-step window
+ * masses are the FullKV attention A_tau(w).  Windows play the role of the pages' token positions.
+ * At every routing event the diagnostics record, per (layer, sequence):
+ *   FMM_H   App. I.2 Eq. (13): over the next `horizon` decode steps, the FullKV attention of each query
+ *           head on the windows the policy holds Evicted, over that on every state that existed at
+ *           the event (sinks and windows whose first position was cached); averaged over the
+ *           (head, event) pairs whose horizon was fully decoded;
+ *   churn   Eq. (14): Jaccard distance of the windows retained (Full or Quantized) at consecutive
+ *           events;
+ *   mu(z)   Eq. (15): shares of the FullKV window scores per policy tier (Full, Quantized, Evicted,
+ *           Local) over the windows that exist, at the last event;
+ *   QSA, R_Q  Eq. (16)-(17): cosine and sum ratio of the policy's and the FullKV window scores over
+ *           the policy's Quantized windows, at events after the prefill;
+ *   Global LIR(m)  Eq. (18): inactive episodes (runs of events outside the selected set that start
+ *           when a window leaves it) that reach m events, and those that later return; for the
+ *           policy's Full tier and for the FullKV top-k_f selection (ties to the older window);
+ *   P_ab(Delta)  Eq. (19): counts of event pairs Delta = 1..8 apart with the window in (1) or out
+ *           (0) of the policy's Full tier, counted from the event the window was first routed.
+ * The diagnostics own no device memory: `d_buf` (256-byte aligned, qevict_diag_bytes long) holds
+ * their state.  Errors: QEVICT_EINVAL for mismatched caches, a policy ranker other than 0, a FullKV
+ * cache that can evict, horizon not a multiple of omega or above 8 * omega, lir_m < 0;
+ * QEVICT_ESCHEDULE unless both caches are prefilled with no decode step yet (init) or both are due
+ * for a routing event (qevict_diag_route). */
+typedef struct qevict_diag qevict_diag;
+typedef struct {
+  int32_t horizon;   /* FMM horizon H in decode steps; 0 = 32 */
+  int32_t lir_m;     /* Global LIR eligibility threshold m; 0 = 3 */
+} qevict_diag_config;
+typedef struct {
+  int64_t events;                /* routing events recorded, the prefill's included */
+  double fmm;                    /* mean FMM_H over its terms */
+  int64_t fmm_terms;             /* (layer, sequence, query head, event) terms with a complete horizon */
+  double churn;                  /* mean over consecutive event pairs of every unit */
+  int64_t churn_terms;
+  double qsa, r_q;               /* means over the events after the prefill with Quantized windows */
+  int64_t qsa_terms;
+  double tier_mass[4];           /* Full, Quantized, Evicted, Local shares at the last event, mean over units */
+  int64_t lir_eligible, lir_rescued;                 /* policy Full tier */
+  int64_t lir_oracle_eligible, lir_oracle_rescued;   /* FullKV top-k_f selection */
+  int64_t lag[8][2][2];          /* lag[Delta-1][a][b] */
+} qevict_diag_report;
+qevict_status qevict_diag_bytes(const qevict_cache *policy, const qevict_diag_config *dc, size_t *bytes);
+/* Records the prefill routing as the first event (enqueued on `stream`). */
+qevict_status qevict_diag_init(qevict_cache *policy, qevict_cache *fullkv, const qevict_diag_config *dc, void *d_buf,
+                               size_t bytes, qevict_stream_t stream, qevict_diag **out);
+/* A routing event of both caches in place of two qevict_route calls: reads the FullKV masses of the
+ * steps since the previous event, routes the policy, routes the FullKV cache, records the event. */
+qevict_status qevict_diag_route(qevict_diag *diag, qevict_stream_t stream);
+/* Synchronises `stream` and sums the per-unit records into `out` (host memory). */
+qevict_status qevict_diag_read(qevict_diag *diag, qevict_diag_report *out, qevict_stream_t stream);
+qevict_status qevict_diag_destroy(qevict_diag *diag);
+
 /* Frees the host handle (the arena stays the caller's). */
 qevict_status qevict_destroy(qevict_cache *cache);
 

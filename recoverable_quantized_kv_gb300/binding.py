@@ -54,6 +54,19 @@ class Tuple(ctypes.Structure):
                                                "l_slot", "f_table", "q_table", "meta")]
 
 
+class DiagConfig(ctypes.Structure):
+    _fields_ = [("horizon", ctypes.c_int32), ("lir_m", ctypes.c_int32)]
+
+
+class DiagReport(ctypes.Structure):
+    _fields_ = [("events", ctypes.c_int64), ("fmm", ctypes.c_double), ("fmm_terms", ctypes.c_int64),
+                ("churn", ctypes.c_double), ("churn_terms", ctypes.c_int64), ("qsa", ctypes.c_double),
+                ("r_q", ctypes.c_double), ("qsa_terms", ctypes.c_int64), ("tier_mass", ctypes.c_double * 4),
+                ("lir_eligible", ctypes.c_int64), ("lir_rescued", ctypes.c_int64),
+                ("lir_oracle_eligible", ctypes.c_int64), ("lir_oracle_rescued", ctypes.c_int64),
+                ("lag", ctypes.c_int64 * 32)]
+
+
 _lib = None
 
 
@@ -77,6 +90,11 @@ def load() -> ctypes.CDLL:
         "qevict_route": [P, P],
         "qevict_flush_scores": [P, P],
         "qevict_set_rope_table": [P, P, I64, P],
+        "qevict_diag_bytes": [P, ctypes.POINTER(DiagConfig), ctypes.POINTER(ctypes.c_size_t)],
+        "qevict_diag_init": [P, P, ctypes.POINTER(DiagConfig), P, ctypes.c_size_t, P, ctypes.POINTER(P)],
+        "qevict_diag_route": [P, P],
+        "qevict_diag_read": [P, ctypes.POINTER(DiagReport), P],
+        "qevict_diag_destroy": [P],
         "qevict_get_tuple": [P, I32, I32, ctypes.POINTER(Tuple)],
         "qevict_export_bytes": [P, ctypes.POINTER(ctypes.c_size_t)],
         "qevict_export_state": [P, P, ctypes.c_size_t, P],
@@ -102,7 +120,8 @@ def exported_symbols():
             "qevict_prefill_scores", "qevict_prefill_route", "qevict_decode_step", "qevict_route",
             "qevict_read_counters", "qevict_check", "qevict_destroy", "qevict_status_string",
             "qevict_prefill_scores_noalloc", "qevict_flush_scores", "qevict_get_tuple", "qevict_export_bytes",
-            "qevict_export_state", "qevict_import_state", "qevict_set_rope_table"]
+            "qevict_export_state", "qevict_import_state", "qevict_set_rope_table", "qevict_diag_bytes",
+            "qevict_diag_init", "qevict_diag_route", "qevict_diag_read", "qevict_diag_destroy"]
 
 
 def _check(status: int, where: str):
@@ -248,3 +267,45 @@ class Cache:
 
     def unit(self, layer: int, seq: int) -> int:
         return layer * self.cfg.batch + seq
+
+
+class Diagnostics:
+    """Routing diagnostics of a policy cache against a FullKV cache fed the same inputs (QEvict App. I).
+    Create after both caches are prefilled; call route() in place of both caches' route()."""
+
+    def __init__(self, policy: "Cache", fullkv: "Cache", horizon: int = 0, lir_m: int = 0, stream=None):
+        import torch
+        lib = load()
+        self.policy, self.fullkv = policy, fullkv
+        self.dc = DiagConfig(horizon, lir_m)
+        n = ctypes.c_size_t()
+        _check(lib.qevict_diag_bytes(policy.handle, ctypes.byref(self.dc), ctypes.byref(n)), "qevict_diag_bytes")
+        self.buf = torch.empty(n.value, dtype=torch.uint8, device=policy.arena.device)
+        h = ctypes.c_void_p()
+        _check(lib.qevict_diag_init(policy.handle, fullkv.handle, ctypes.byref(self.dc), self.buf.data_ptr(),
+                                    self.buf.numel(), _stream(stream), ctypes.byref(h)), "qevict_diag_init")
+        self.handle = h
+
+    def route(self, stream=None):
+        _check(load().qevict_diag_route(self.handle, _stream(stream)), "qevict_diag_route")
+
+    def report(self, stream=None) -> dict:
+        r = DiagReport()
+        _check(load().qevict_diag_read(self.handle, ctypes.byref(r), _stream(stream)), "qevict_diag_read")
+        import numpy as np
+        return {"events": r.events, "fmm": r.fmm, "fmm_terms": r.fmm_terms, "churn": r.churn,
+                "churn_terms": r.churn_terms, "qsa": r.qsa, "r_q": r.r_q, "qsa_terms": r.qsa_terms,
+                "tier_mass": np.array(list(r.tier_mass)), "lir_eligible": r.lir_eligible,
+                "lir_rescued": r.lir_rescued, "lir_oracle_eligible": r.lir_oracle_eligible,
+                "lir_oracle_rescued": r.lir_oracle_rescued, "lag": np.array(list(r.lag)).reshape(8, 2, 2)}
+
+    def close(self):
+        if self.handle:
+            load().qevict_diag_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
-SOURCES = ["api.cu", "decode.cu", "route.cu", "scores.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "decode.cu", "route.cu", "scores.cu", "noalloc.cu", "diag.cu"]
 LIB = os.path.join(HERE, "libqevict.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]

@@ -10,6 +10,7 @@
 
 #include "cache_dev.cuh"
 #include "common.cuh"
+#include "diag_dev.cuh"
 #include "qevict.h"
 
 namespace qv {
@@ -24,6 +25,8 @@ cudaError_t launch_decode(const CacheDev &C, const DecodeIO &io, cudaStream_t s)
 cudaError_t launch_flush(const CacheDev &C, cudaStream_t s);
 int route_max_windows();
 int decode_warps();
+cudaError_t launch_diag_collect(const CacheDev &R, const DiagDev &Dg, cudaStream_t s);
+cudaError_t launch_diag_event(const CacheDev &P, const CacheDev &R, const DiagDev &Dg, int e, cudaStream_t s);
 }  // namespace qv
 
 struct qevict_cache {
@@ -333,11 +336,16 @@ qevict_status qevict_decode_step(qevict_cache *cache, int32_t layer, const void 
   return QEVICT_OK;
 }
 
-qevict_status qevict_route(qevict_cache *cache, qevict_stream_t stream) {
-  if (!cache) return QEVICT_EINVAL;
+static qevict_status route_due(const qevict_cache *cache) {
   const int due = cache->cfg.prompt_len + (cache->routes_done + 1) * cache->cfg.omega;
   for (int l = 0; l < cache->cfg.n_layers; ++l)
     if (!cache->prefilled[l] || cache->t_host[l] != due) return QEVICT_ESCHEDULE;
+  return QEVICT_OK;
+}
+
+qevict_status qevict_route(qevict_cache *cache, qevict_stream_t stream) {
+  if (!cache) return QEVICT_EINVAL;
+  if (route_due(cache) != QEVICT_OK) return QEVICT_ESCHEDULE;
   cudaError_t e = qv::launch_flush(cache->dev, reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaSuccess)
     e = qv::launch_route(cache->dev, 0, cache->cfg.batch * cache->cfg.n_layers, nullptr, nullptr, 0, 8,
@@ -480,6 +488,166 @@ qevict_status qevict_import_state(qevict_cache *cache, const void *host_buf, siz
     if (m[qv::M_T] > 0 && cache->cfg.rope) cache->rope_set = 1;
   }
   cache->last_decode_layer = -1;
+  return QEVICT_OK;
+}
+
+// ----------------------------------------------------------------------------- routing diagnostics
+
+struct qevict_diag {
+  qevict_cache *policy, *fullkv;
+  qv::DiagDev dev;
+  int events;
+};
+
+namespace {
+
+qevict_status diag_check(const qevict_cache *P, const qevict_cache *R, const qevict_diag_config *dc, int *horizon,
+                         int *lir_m) {
+  if (!P || !R || P == R || !dc) return QEVICT_EINVAL;
+  const qevict_config &a = P->cfg, &b = R->cfg;
+  if (a.batch != b.batch || a.n_layers != b.n_layers || a.h_q != b.h_q || a.h_kv != b.h_kv || a.d_head != b.d_head ||
+      a.n_sink != b.n_sink || a.n_recent != b.n_recent || a.window != b.window || a.bits != b.bits ||
+      a.omega != b.omega || a.prompt_len != b.prompt_len || a.max_len != b.max_len || a.rope != b.rope)
+    return QEVICT_EINVAL;
+  if (a.ranker != 0 || R->bud.k_f < R->bud.n_windows) return QEVICT_EINVAL;
+  const int H = dc->horizon ? dc->horizon : 32, m = dc->lir_m ? dc->lir_m : 3;
+  if (H < a.omega || H % a.omega || H / a.omega > qv::DG_MAX_OPEN || a.omega > qv::DG_MAX_OMEGA || m < 1 ||
+      dc->horizon < 0 || dc->lir_m < 0)
+    return QEVICT_EINVAL;
+  *horizon = H;
+  *lir_m = m;
+  return QEVICT_OK;
+}
+
+qv::DiagDev diag_plan(const qevict_cache *P, int horizon, int lir_m, int64_t *bytes) {
+  qv::DiagDev d = {};
+  d.U = P->cfg.batch * P->cfg.n_layers;
+  d.N = P->bud.n_windows;
+  d.Hq = P->cfg.h_q;
+  d.n_open = horizon / P->cfg.omega;
+  d.horizon = horizon;
+  d.lir_m = lir_m;
+  int64_t off = 0;
+  auto take = [&](int64_t n) {
+    const int64_t o = off;
+    off += align256(std::max<int64_t>(n, 16));
+    return o;
+  };
+  const int64_t UN = (int64_t)d.U * d.N;
+  d.off_evict = take(4 * UN);   // the three -1 regions first: one memset covers them
+  d.off_since = take(4 * UN);
+  d.off_evT = take(4LL * d.U * qv::DG_MAX_OPEN);
+  d.off_evId = take(4LL * d.U * qv::DG_MAX_OPEN);
+  d.off_runpol = take(4 * UN);
+  d.off_runorc = take(4 * UN);
+  d.off_xpol = take(4 * UN);
+  d.off_xorc = take(4 * UN);
+  d.off_ret = take(UN);
+  d.off_fnum = take(8LL * d.U * d.Hq * qv::DG_MAX_OPEN);
+  d.off_fden = take(8LL * d.U * d.Hq * qv::DG_MAX_OPEN);
+  d.off_acc = take(8LL * d.U * qv::DA_N);
+  *bytes = off;
+  return d;
+}
+
+}  // namespace
+
+qevict_status qevict_diag_bytes(const qevict_cache *policy, const qevict_diag_config *dc, size_t *bytes) {
+  if (!policy || !dc || !bytes || dc->horizon < 0 || dc->lir_m < 0) return QEVICT_EINVAL;
+  const int H = dc->horizon ? dc->horizon : 32, om = policy->cfg.omega;
+  if (H < om || H % om || H / om > qv::DG_MAX_OPEN) return QEVICT_EINVAL;
+  int64_t b = 0;
+  diag_plan(policy, H, 3, &b);
+  *bytes = (size_t)b;
+  return QEVICT_OK;
+}
+
+qevict_status qevict_diag_init(qevict_cache *policy, qevict_cache *fullkv, const qevict_diag_config *dc, void *d_buf,
+                               size_t bytes, qevict_stream_t stream, qevict_diag **out) {
+  if (!out || !d_buf || ((uintptr_t)d_buf & 255)) return QEVICT_EINVAL;
+  int H = 0, m = 0;
+  qevict_status st = diag_check(policy, fullkv, dc, &H, &m);
+  if (st != QEVICT_OK) return st;
+  for (const qevict_cache *c : {policy, fullkv}) {
+    if (c->routes_done != 0) return QEVICT_ESCHEDULE;
+    for (int l = 0; l < c->cfg.n_layers; ++l)
+      if (!c->prefilled[l] || c->t_host[l] != c->cfg.prompt_len) return QEVICT_ESCHEDULE;
+  }
+  int64_t need = 0;
+  qv::DiagDev d = diag_plan(policy, H, m, &need);
+  if ((int64_t)bytes < need) return QEVICT_ENOMEM;
+  d.base = static_cast<uint8_t *>(d_buf);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(d_buf, 0, (size_t)need, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(d.base + d.off_evict, 0xFF, (size_t)(d.off_evId - d.off_evict), s);
+  if (e == cudaSuccess) e = qv::launch_diag_event(policy->dev, fullkv->dev, d, 0, s);
+  if (e != cudaSuccess) return QEVICT_ECUDA;
+  qevict_diag *dg = new (std::nothrow) qevict_diag();
+  if (!dg) return QEVICT_ENOMEM;
+  dg->policy = policy;
+  dg->fullkv = fullkv;
+  dg->dev = d;
+  dg->events = 1;
+  *out = dg;
+  return QEVICT_OK;
+}
+
+qevict_status qevict_diag_route(qevict_diag *diag, qevict_stream_t stream) {
+  if (!diag) return QEVICT_EINVAL;
+  if (route_due(diag->policy) != QEVICT_OK || route_due(diag->fullkv) != QEVICT_OK) return QEVICT_ESCHEDULE;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (qv::launch_diag_collect(diag->fullkv->dev, diag->dev, s) != cudaSuccess) return QEVICT_ECUDA;
+  qevict_status st = qevict_route(diag->policy, stream);
+  if (st == QEVICT_OK) st = qevict_route(diag->fullkv, stream);
+  if (st != QEVICT_OK) return st;
+  if (qv::launch_diag_event(diag->policy->dev, diag->fullkv->dev, diag->dev, diag->events, s) != cudaSuccess)
+    return QEVICT_ECUDA;
+  diag->events += 1;
+  return QEVICT_OK;
+}
+
+qevict_status qevict_diag_read(qevict_diag *diag, qevict_diag_report *out, qevict_stream_t stream) {
+  if (!diag || !out) return QEVICT_EINVAL;
+  const qv::DiagDev &d = diag->dev;
+  std::vector<double> acc((size_t)d.U * qv::DA_N);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(acc.data(), d.base + d.off_acc, acc.size() * sizeof(double), cudaMemcpyDeviceToHost, s) !=
+      cudaSuccess)
+    return QEVICT_ECUDA;
+  qevict_status st = read_status(diag->policy, s);
+  if (st == QEVICT_OK) st = read_status(diag->fullkv, s);
+  if (st == QEVICT_ECUDA) return st;
+  std::memset(out, 0, sizeof(*out));
+  double fs = 0, fc = 0, cs = 0, cc = 0, qs = 0, rs = 0, qc = 0;
+  for (int u = 0; u < d.U; ++u) {
+    const double *a = acc.data() + (size_t)u * qv::DA_N;
+    fs += a[qv::DA_FMM_SUM];
+    fc += a[qv::DA_FMM_CNT];
+    cs += a[qv::DA_CHURN_SUM];
+    cc += a[qv::DA_CHURN_CNT];
+    qs += a[qv::DA_QSA_SUM];
+    rs += a[qv::DA_RQ_SUM];
+    qc += a[qv::DA_QSA_CNT];
+    for (int z = 0; z < 4; ++z) out->tier_mass[z] += a[qv::DA_MU + z] / d.U;
+    out->lir_eligible += (int64_t)a[qv::DA_LIR + 0];
+    out->lir_rescued += (int64_t)a[qv::DA_LIR + 1];
+    out->lir_oracle_eligible += (int64_t)a[qv::DA_LIR + 2];
+    out->lir_oracle_rescued += (int64_t)a[qv::DA_LIR + 3];
+    for (int k = 0; k < qv::DG_MAX_LAG * 4; ++k) (&out->lag[0][0][0])[k] += (int64_t)a[qv::DA_LAG + k];
+    if (u == 0) out->events = (int64_t)a[qv::DA_EVENTS];
+  }
+  out->fmm = fc > 0 ? fs / fc : 0.0;
+  out->fmm_terms = (int64_t)fc;
+  out->churn = cc > 0 ? cs / cc : 0.0;
+  out->churn_terms = (int64_t)cc;
+  out->qsa = qc > 0 ? qs / qc : 0.0;
+  out->r_q = qc > 0 ? rs / qc : 0.0;
+  out->qsa_terms = (int64_t)qc;
+  return st;
+}
+
+qevict_status qevict_diag_destroy(qevict_diag *diag) {
+  delete diag;
   return QEVICT_OK;
 }
 

@@ -56,6 +56,8 @@ class Lockstep:
         # and counters are compared for every sequence)
         self.state_seqs = list(range(self.B)) if state_seqs is None else state_seqs
         self.churn = churn
+        self.route_hook = None   # replaces the cache's own routing call (e.g. a diagnostics route)
+        self.s0 = {}             # per layer: the prompt scores the prefill routed on
         # pre-RoPE Quantized keys: both sides get the same (cos, sin) table, a model input
         if getattr(wl, "rope_base", 0.0) > 0:
             table = synth.rope_table(wl.max_len, wl.rope_base)
@@ -94,6 +96,7 @@ class Lockstep:
                 else:   # at full size: every query's mass lands on windows or sinks, sinks take a little
                     assert 0 < wl.prompt_len - s0h[b].sum() < 0.01 * wl.prompt_len
             self.cache.prefill_route(l, k, v, s0=s0)
+            self.s0[l] = s0.clone()
             for b in range(self.B):
                 self.units[(l, b)].prefill_route(ins[b]["k"].float().numpy(), ins[b]["v"].float().numpy(), s0h[b])
             del q, k, v
@@ -243,7 +246,7 @@ class Lockstep:
                     forced[0] = torch.from_numpy((rng.random(self.N) * 10).astype(np.float32))
                     self.cache.region("score", self._u(l, b), 4 * H * self.N).view(torch.float32).copy_(
                         forced.view(-1).cuda())
-        self.cache.route()   # absorbs the pending steps' masses, then ranks
+        (self.route_hook or self.cache.route)()   # absorbs the pending steps' masses, then ranks
         torch.cuda.synchronize()
         for l in range(self.L):
             for b in range(self.B):
