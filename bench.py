@@ -45,6 +45,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample-steps", type=int, default=8)
+    ap.add_argument("--diag", type=int, default=0,
+                    help="also run N routing events with the routing diagnostics against a FullKV cache")
     ap.add_argument("--rope-base", type=float, default=0.0,
                     help="keys carry RoPE with this base and Quantized keys are kept before it (GPU arm only)")
     ap.add_argument("--layers", type=int, default=None,
@@ -515,7 +517,73 @@ def run_gpu(args, rank, world):
     }
     if e2e:
         result["e2e"] = e2e
+    if args.diag:
+        del cache
+        torch.cuda.empty_cache()
+        result["diagnostics"] = run_diag(wl, dev, stream, args.diag)
     return result
+
+
+def run_diag(wl, dev, stream, n_events):
+    """Routing diagnostics (QEvict App. I) of the policy against a FullKV cache fed the same inputs:
+    n_events routing events, each timed through qevict_diag_route, then one more event of plain
+    qevict_route calls on both caches for the cost without diagnostics."""
+    import torch
+    from recoverable_quantized_kv_gb300 import binding, synth
+    Om, L, B = wl.omega, wl.n_layers, wl.batch
+    steps = (n_events + 1) * Om
+    max_len = wl.prompt_len + steps
+    pol = binding.Cache(binding.make_config(wl, max_len=max_len), device=dev)
+    fwl = wl.replace(budget_num=1000, q_num=0)
+    full = binding.Cache(binding.make_config(fwl, max_len=max_len), device=dev)
+    for c in (pol, full):
+        if wl.rope_base > 0:
+            c.set_rope_table(torch.from_numpy(synth.rope_table(max_len, wl.rope_base)).to(dev))
+    for layer in range(L):
+        ins = [synth.prompt_inputs(wl, b, layer, device=dev) for b in range(B)]
+        q = torch.stack([x["q"] for x in ins])
+        k = torch.stack([x["k"] for x in ins])
+        v = torch.stack([x["v"] for x in ins])
+        pol.prefill_route(layer, k, v, s0=None, q_prompt=q, stream=stream)
+        full.prefill_route(layer, k, v, s0=None, q_prompt=q, stream=stream)
+        del ins, q, k, v
+    diag = binding.Diagnostics(pol, full, stream=stream)
+    dec = [[synth.decode_inputs(wl, b, layer, steps=steps, device=dev) for b in range(B)] for layer in range(L)]
+    out = torch.empty(B, wl.h_q, D, dtype=torch.bfloat16, device=dev)
+    diag_ms, plain_ms = [], []
+    for s in range(steps):
+        for layer in range(L):
+            q = torch.stack([d["q"][s] for d in dec[layer]])
+            k = torch.stack([d["k"][s] for d in dec[layer]])
+            v = torch.stack([d["v"][s] for d in dec[layer]])
+            pol.decode_step(layer, q, k, v, out, stream)
+            full.decode_step(layer, q, k, v, out, stream)
+        if (s + 1) % Om == 0:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            if s + 1 < steps:
+                diag.route(stream)
+            else:
+                pol.route(stream)
+                full.route(stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            (diag_ms if s + 1 < steps else plain_ms).append(e0.elapsed_time(e1))
+    rep = diag.report(stream)
+    lag = rep["lag"]
+
+    def p(a, b, d):
+        n = lag[d - 1, a].sum()
+        return float(lag[d - 1, a, b] / n) if n else None
+    return {"events": rep["events"], "fmm_h32": rep["fmm"], "fmm_terms": rep["fmm_terms"], "churn": rep["churn"],
+            "qsa": rep["qsa"], "r_q": rep["r_q"], "tier_mass_full_quant_evict_local": rep["tier_mass"].tolist(),
+            "lir3_policy": [rep["lir_eligible"], rep["lir_rescued"]],
+            "lir3_fullkv_topk": [rep["lir_oracle_eligible"], rep["lir_oracle_rescued"]],
+            "p01": [p(0, 1, 1), p(0, 1, 8)], "p10": [p(1, 0, 1), p(1, 0, 8)],
+            "route_ms_per_event_with_diag": statistics.mean(diag_ms), "route_ms_plain_pair": plain_ms[0],
+            "note": "policy and FullKV caches decode the same synthetic inputs; route_ms covers both caches' "
+                    "routing events (all layers); p01/p10 at Delta = 1 and 8"}
 
 
 def _bus_id(torch, dev):

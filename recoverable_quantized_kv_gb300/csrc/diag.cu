@@ -28,7 +28,10 @@ __device__ __forceinline__ float warp_sum_f(float v) {
   return v;
 }
 
-// One CTA per (KV head g, sequence, layer) of R.
+// One CTA per (KV head g, sequence, layer) of R.  Only two kinds of window enter the sums: those the
+// policy has evicted by an open event (FMM numerator) and those that did not exist yet at an open event
+// (left out of its denominator, which is then the step count minus their attention: every step's
+// attention sums to one over the sinks and the windows).
 __global__ void __launch_bounds__(DG_COLLECT_THREADS) diag_collect_kernel(const CacheDev R, const DiagDev Dg) {
   const int g = blockIdx.x, b = blockIdx.y, layer = blockIdx.z;
   const int unit = layer * R.B + b, bg = b * R.h_kv + g;
@@ -36,12 +39,17 @@ __global__ void __launch_bounds__(DG_COLLECT_THREADS) diag_collect_kernel(const 
   __shared__ int s_meta[8];
   __shared__ float st[DG_MAX_OMEGA * 16];                  // merged max and 1/L of each pending step
   __shared__ int s_evT[DG_MAX_OPEN], s_evId[DG_MAX_OPEN];
-  __shared__ float acc_tot[8], acc_ex[8][DG_MAX_OPEN], acc_ev[8][DG_MAX_OPEN];
+  __shared__ unsigned s_inh[DG_MAX_OMEGA];                 // per step: the open events it counts for
+  __shared__ float acc_ev[8][DG_MAX_OPEN], acc_nx[8][DG_MAX_OPEN];
   const int *meta = R.at<const int>(R.off_meta, R.st_meta, unit);
   if (threadIdx.x < 8) s_meta[threadIdx.x] = meta[threadIdx.x];
-  if (threadIdx.x < NO) {
-    s_evT[threadIdx.x] = Dg.ev_T(unit)[threadIdx.x];
-    s_evId[threadIdx.x] = Dg.ev_id(unit)[threadIdx.x];
+  if (threadIdx.x < DG_MAX_OPEN) {
+    s_evT[threadIdx.x] = threadIdx.x < NO ? Dg.ev_T(unit)[threadIdx.x] : -1;
+    s_evId[threadIdx.x] = threadIdx.x < NO ? Dg.ev_id(unit)[threadIdx.x] : -1;
+  }
+  if (threadIdx.x < 8 * DG_MAX_OPEN) {
+    (&acc_ev[0][0])[threadIdx.x] = 0.f;
+    (&acc_nx[0][0])[threadIdx.x] = 0.f;
   }
   __syncthreads();
   const int T = s_meta[M_T], F = s_meta[M_FLUSHT], j0 = s_meta[M_NROUTE];
@@ -54,109 +62,130 @@ __global__ void __launch_bounds__(DG_COLLECT_THREADS) diag_collect_kernel(const 
   const float *ms = reinterpret_cast<const float *>(R.arena + R.off_mstat + R.st_mstat_layer * layer) +
                     (size_t)bg * R.omega * 16;
   for (int i = threadIdx.x; i < nk * 16; i += blockDim.x) st[i] = ms[i];
+  for (int k = threadIdx.x; k < nk; k += blockDim.x) {
+    const int Tk = F + k + 1;   // tokens cached after step k; its query sits at position Tk - 1
+    unsigned m = 0;
+    for (int j = 0; j < NO; ++j)
+      if (s_evT[j] >= 0 && Tk > s_evT[j] && Tk - s_evT[j] <= Dg.horizon) m |= 1u << j;
+    s_inh[k] = m;
+  }
+  __syncthreads();
   const float *mu = reinterpret_cast<const float *>(R.arena + R.off_mu + R.st_mu_layer * layer) +
                     (size_t)bg * R.omega * R.max_items * 8;
   const int2 *ftab = R.at<const int2>(R.off_ftab, R.st_ftab, unit);
   const int2 *qtab = R.at<const int2>(R.off_qtab, R.st_qtab, unit);
   const int *evict = Dg.evict(unit);
   const int LOC = R.loc_items(), KFC = R.kf_cap();
-  const int lane = threadIdx.x & 31;
-  for (int k = 0; k < nk; ++k) {
-    const int Tk = F + k + 1;   // tokens cached after step k; its query sits at position Tk - 1
-    if (threadIdx.x < 8 * (1 + 2 * DG_MAX_OPEN)) {
-      const int h = threadIdx.x & 7, j = threadIdx.x >> 3;
-      if (j == 0) acc_tot[h] = 0.f;
-      else if (j <= DG_MAX_OPEN) acc_ex[h][j - 1] = 0.f;
-      else acc_ev[h][j - 1 - DG_MAX_OPEN] = 0.f;
-    }
-    __syncthreads();
-    // per thread: its items' masses for every head, split by open event
-    float tot[8], ex[8][DG_MAX_OPEN], ev[8][DG_MAX_OPEN];
+  float ev[8][DG_MAX_OPEN], nx[8][DG_MAX_OPEN];
 #pragma unroll
-    for (int h = 0; h < 8; ++h) {
-      tot[h] = 0.f;
+  for (int h = 0; h < 8; ++h)
 #pragma unroll
-      for (int j = 0; j < DG_MAX_OPEN; ++j) ex[h][j] = ev[h][j] = 0.f;
+    for (int j = 0; j < DG_MAX_OPEN; ++j) ev[h][j] = nx[h][j] = 0.f;
+  for (int idx = 1 + threadIdx.x; idx < R.max_items; idx += blockDim.x) {
+    int w, k0 = 0;
+    if (idx <= LOC) {   // recent window j0 + idx - 1, present from the step that caches its first position
+      w = j0 + idx - 1;
+      if (w >= R.n_windows) continue;
+      k0 = max(0, R.n_sink + w * R.W - F);
+    } else if (idx <= LOC + KFC) {
+      const int f = idx - 1 - LOC;
+      if (f >= nF) continue;
+      w = ftab[f].x;
+    } else {
+      const int q = idx - 1 - LOC - KFC;
+      if (q >= nQ) continue;
+      w = qtab[q].x;
     }
-    for (int idx = 1 + threadIdx.x; idx < R.max_items; idx += blockDim.x) {
-      int w;
-      if (idx <= LOC) {   // recent window j0 + idx - 1, present once its first position is cached
-        w = j0 + idx - 1;
-        if (w >= R.n_windows || R.n_sink + w * R.W > F + k) continue;
-      } else if (idx <= LOC + KFC) {
-        const int f = idx - 1 - LOC;
-        if (f >= nF) continue;
-        w = ftab[f].x;
-      } else {
-        const int q = idx - 1 - LOC - KFC;
-        if (q >= nQ) continue;
-        w = qtab[q].x;
-      }
+    const int ew = evict[w];
+    unsigned evb = 0, nxb = 0;
+    for (int j = 0; j < NO; ++j) {
+      if (s_evT[j] < 0) continue;
+      if (ew >= 0 && ew <= s_evId[j]) evb |= 1u << j;                 // evicted by event j
+      if (R.n_sink + w * R.W >= s_evT[j]) nxb |= 1u << j;             // did not exist at event j
+    }
+    if (!(evb | nxb)) continue;
+    for (int k = k0; k < nk; ++k) {
+      const unsigned me = evb & s_inh[k], mn = nxb & s_inh[k];
+      if (!(me | mn)) continue;
       const float *m = mu + ((size_t)k * R.max_items + idx) * 8;
       const float *Mk = st + k * 16;
-      const int ew = evict[w];
 #pragma unroll
       for (int h = 0; h < 8; ++h) {
         if (h >= G) continue;
         const float a = exp2f(m[h] - Mk[h]) * Mk[8 + h];
-        tot[h] += a;
 #pragma unroll
         for (int j = 0; j < DG_MAX_OPEN; ++j) {
-          if (j >= NO || s_evT[j] < 0) continue;
-          if (R.n_sink + w * R.W < s_evT[j]) ex[h][j] += a;                  // existed at event j
-          if (ew >= 0 && ew <= s_evId[j]) ev[h][j] += a;                     // evicted by then
+          if (me >> j & 1u) ev[h][j] += a;
+          if (mn >> j & 1u) nx[h][j] += a;
         }
       }
     }
+  }
+  const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int h = 0; h < 8; ++h) {
-      if (h >= G) continue;
-      const float t = warp_sum_f(tot[h]);
-      if (lane == 0) atomicAdd(&acc_tot[h], t);
+  for (int h = 0; h < 8; ++h) {
+    if (h >= G) continue;
 #pragma unroll
-      for (int j = 0; j < DG_MAX_OPEN; ++j) {
-        if (j >= NO) continue;
-        const float x = warp_sum_f(ex[h][j]), y = warp_sum_f(ev[h][j]);
-        if (lane == 0) {
-          atomicAdd(&acc_ex[h][j], x);
-          atomicAdd(&acc_ev[h][j], y);
-        }
+    for (int j = 0; j < DG_MAX_OPEN; ++j) {
+      if (j >= NO) continue;
+      const float x = warp_sum_f(ev[h][j]), y = warp_sum_f(nx[h][j]);
+      if (lane == 0) {
+        atomicAdd(&acc_ev[h][j], x);
+        atomicAdd(&acc_nx[h][j], y);
       }
     }
-    __syncthreads();
-    // the sinks hold the rest of the step's attention; the step counts for an event inside its horizon
-    if (threadIdx.x < G * NO) {
-      const int h = threadIdx.x % G, j = threadIdx.x / G;
-      if (s_evT[j] >= 0 && Tk > s_evT[j] && Tk - s_evT[j] <= Dg.horizon) {
-        const size_t o = ((size_t)unit * R.h_q + (size_t)g * G + h) * DG_MAX_OPEN + j;
-        Dg.fnum()[o] += (double)acc_ev[h][j];
-        Dg.fden()[o] += (double)(1.f - acc_tot[h]) + (double)acc_ex[h][j];
-      }
+  }
+  __syncthreads();
+  if (threadIdx.x < G * NO) {
+    const int h = threadIdx.x % G, j = threadIdx.x / G;
+    int steps = 0;
+    for (int k = 0; k < nk; ++k) steps += (s_inh[k] >> j) & 1u;
+    if (steps) {
+      const size_t o = ((size_t)unit * R.h_q + (size_t)g * G + h) * DG_MAX_OPEN + j;
+      Dg.fnum()[o] += (double)acc_ev[h][j];
+      Dg.fden()[o] += (double)steps - (double)acc_nx[h][j];
     }
-    __syncthreads();
   }
 }
 
-__device__ double block_sum_d(double v, double *wsum) {
+__device__ int block_sum_i(int v, int *ws) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
   __syncthreads();
-  if (lane == 0) wsum[warp] = v;
+  if (lane == 0) ws[warp] = v;
   __syncthreads();
-  double t = 0.0;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += wsum[w];
+  if (warp == 0) {
+    int t = lane < (int)(blockDim.x >> 5) ? ws[lane] : 0;
+#pragma unroll
+    for (int off = 16; off; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+    if (lane == 0) ws[32] = t;
+  }
   __syncthreads();
-  return t;
+  return ws[32];
 }
 
-// One CTA per (sequence, layer) unit; runs after both caches routed at event e.
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// One CTA per (sequence, layer) unit; runs after both caches routed at event e.  Double-precision sums
+// stay in one warp: this GPU's FP64 rate is low.
 __global__ void __launch_bounds__(DG_EVENT_THREADS, 1) diag_event_kernel(const CacheDev P, const CacheDev R,
                                                                          const DiagDev Dg, int e) {
-  extern __shared__ float s_full[];   // [n_windows] FullKV scores (the oracle selection ranks them)
-  __shared__ double wsum[32];
+  extern __shared__ __align__(16) uint8_t dsm[];
+  const int N = P.n_windows;
+  float *s_full = reinterpret_cast<float *>(dsm);        // [N] FullKV window scores
+  float *s_pol = s_full + N;                             // [N] policy window scores
+  uint8_t *s_tier = reinterpret_cast<uint8_t *>(s_pol + N);   // [N] policy tier (Local for unrouted)
+  __shared__ int ws[33];
+  __shared__ unsigned hist[256];
+  __shared__ unsigned long long s_prefix;
+  __shared__ int s_want;
   __shared__ int s_lag[DG_MAX_LAG * 4], s_lir[4];
-  const int unit = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
+  const int unit = blockIdx.x, tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, warp = tid >> 5;
   const int *pm = P.at<const int>(P.off_meta, P.st_meta, unit);
   const int *rm = R.at<const int>(R.off_meta, R.st_meta, unit);
   const int T = pm[M_T], n_route = pm[M_NROUTE];
@@ -164,110 +193,176 @@ __global__ void __launch_bounds__(DG_EVENT_THREADS, 1) diag_event_kernel(const C
     if (tid == 0) atomicOr(P.status(), QV_ERR_STATE);
     return;
   }
-  const int N = P.n_windows, NO = Dg.n_open, Hq = P.h_q;
+  const int NO = Dg.n_open, Hq = P.h_q;
   double *acc = Dg.acc(unit);
   int *evT = Dg.ev_T(unit), *evId = Dg.ev_id(unit);
   double *fnum = Dg.fnum() + (size_t)unit * Hq * DG_MAX_OPEN, *fden = Dg.fden() + (size_t)unit * Hq * DG_MAX_OPEN;
 
-  // 1. events whose horizon is complete: FMM of every head (Eq. (13)); then open this event
-  if (tid == 0) {
+  // 1. events whose horizon is complete: FMM of every head (Eq. (13)), one warp; then open this event
+  if (warp == 0) {
+    double fs = 0.0, fc = 0.0;
     for (int j = 0; j < NO; ++j) {
       if (evT[j] < 0 || T - evT[j] < Dg.horizon) continue;
-      for (int h = 0; h < Hq; ++h) {
+      for (int h = lane; h < Hq; h += 32) {
         const double den = fden[h * DG_MAX_OPEN + j];
         if (den > 0.0) {
-          acc[DA_FMM_SUM] += fnum[h * DG_MAX_OPEN + j] / den;
-          acc[DA_FMM_CNT] += 1.0;
+          fs += fnum[h * DG_MAX_OPEN + j] / den;
+          fc += 1.0;
         }
       }
-      evT[j] = -1;
     }
-    int slot = -1;
-    for (int j = 0; j < NO && slot < 0; ++j)
-      if (evT[j] < 0) slot = j;
-    if (slot < 0) {
-      atomicOr(P.status(), QV_ERR_STATE);
-    } else {
-      evT[slot] = T;
-      evId[slot] = e;
-      for (int h = 0; h < Hq; ++h) fnum[h * DG_MAX_OPEN + slot] = fden[h * DG_MAX_OPEN + slot] = 0.0;
+    fs = warp_sum_d(fs);
+    fc = warp_sum_d(fc);
+    __syncwarp();
+    if (lane == 0) {
+      acc[DA_FMM_SUM] += fs;
+      acc[DA_FMM_CNT] += fc;
+      int slot = -1;
+      for (int j = 0; j < NO; ++j) {
+        if (evT[j] >= 0 && T - evT[j] >= Dg.horizon) evT[j] = -1;
+        if (evT[j] < 0 && slot < 0) slot = j;
+      }
+      if (slot < 0) {
+        atomicOr(P.status(), QV_ERR_STATE);
+      } else {
+        evT[slot] = T;
+        evId[slot] = e;
+        for (int h = 0; h < Hq; ++h) fnum[h * DG_MAX_OPEN + slot] = fden[h * DG_MAX_OPEN + slot] = 0.0;
+      }
     }
   }
   if (tid < DG_MAX_LAG * 4) s_lag[tid] = 0;
   if (tid < 4) s_lir[tid] = 0;
 
-  // 2. per window: evictions, retained sets, scores, tier masses
+  // 2. per window: evictions, the retained set, both runs' scores (sums of the KV-head partials, head order)
   const uint8_t *state = P.at<const uint8_t>(P.off_state, P.st_state, unit);
   const float *sp = P.at<const float>(P.off_score, P.st_score, unit);
   const float *sr = R.at<const float>(R.off_score, R.st_score, unit);
   int *evict = Dg.evict(unit);
   uint8_t *ret = Dg.ret(unit);
-  double inter = 0, uni = 0, dot = 0, nq = 0, nf = 0, sq = 0, sf = 0, mz[4] = {0, 0, 0, 0};
+  int inter = 0, uni = 0;
   for (int w = tid; w < N; w += nt) {
     const bool routed = w < n_route;
     const int tier = routed ? (state[w] & 3) : TIER_LOCAL;
     if (routed && tier == TIER_EVICT && evict[w] < 0) evict[w] = e;
     const int now = routed && (tier == TIER_FULL || tier == TIER_QUANT);
     const int prev = ret[w];
-    inter += (double)(prev & now);
-    uni += (double)(prev | now);
+    inter += prev & now;
+    uni += prev | now;
     ret[w] = (uint8_t)now;
-    float a = sr[w], c = sp[w];   // window scores: the sum of the KV-head partials in head order
+    float a = sr[w], c = sp[w];
     for (int g = 1; g < P.h_kv; ++g) {
       a += sr[(size_t)g * N + w];
       c += sp[(size_t)g * N + w];
     }
     s_full[w] = a;
-    if (tier == TIER_QUANT) {
-      dot += (double)c * a;
-      nq += (double)c * c;
-      nf += (double)a * a;
-      sq += c;
-      sf += a;
-    }
-    if (P.n_sink + w * P.W < T) mz[tier] += a;
+    s_pol[w] = c;
+    s_tier[w] = (uint8_t)tier;
   }
-  inter = block_sum_d(inter, wsum);
-  uni = block_sum_d(uni, wsum);
-  dot = block_sum_d(dot, wsum);
-  nq = block_sum_d(nq, wsum);
-  nf = block_sum_d(nf, wsum);
-  sq = block_sum_d(sq, wsum);
-  sf = block_sum_d(sf, wsum);
+  inter = block_sum_i(inter, ws);   // its barriers also publish the shared arrays
+  uni = block_sum_i(uni, ws);
+
+  // 3. one warp: QSA / R_Q over the Quantized windows (Eq. (16)-(17)), tier shares over the windows that
+  //    exist (Eq. (15)), churn (Eq. (14))
+  if (warp == 0) {
+    double dot = 0, nq = 0, nf = 0, sq = 0, sf = 0, mz[4] = {0, 0, 0, 0};
+    for (int w = lane; w < N; w += 32) {
+      const double a = s_full[w], c = s_pol[w];
+      const int tier = s_tier[w];
+      if (tier == TIER_QUANT) {
+        dot += c * a;
+        nq += c * c;
+        nf += a * a;
+        sq += c;
+        sf += a;
+      }
+      if (P.n_sink + w * P.W < T) mz[tier] += a;
+    }
+    dot = warp_sum_d(dot);
+    nq = warp_sum_d(nq);
+    nf = warp_sum_d(nf);
+    sq = warp_sum_d(sq);
+    sf = warp_sum_d(sf);
 #pragma unroll
-  for (int z = 0; z < 4; ++z) mz[z] = block_sum_d(mz[z], wsum);   // also orders s_full before step 3
-  if (tid == 0) {
-    if (e >= 1 && uni > 0) {
-      acc[DA_CHURN_SUM] += 1.0 - inter / uni;
-      acc[DA_CHURN_CNT] += 1.0;
+    for (int z = 0; z < 4; ++z) mz[z] = warp_sum_d(mz[z]);
+    if (lane == 0) {
+      if (e >= 1 && uni > 0) {
+        acc[DA_CHURN_SUM] += 1.0 - (double)inter / (double)uni;
+        acc[DA_CHURN_CNT] += 1.0;
+      }
+      if (e >= 1 && nq > 0 && nf > 0) {   // a non-empty Quantized tier
+        acc[DA_QSA_SUM] += dot / sqrt(nq * nf);
+        acc[DA_RQ_SUM] += sq / sf;
+        acc[DA_QSA_CNT] += 1.0;
+      }
+      const double tot = mz[0] + mz[1] + mz[2] + mz[3];
+      // shares in the order Full, Quantized, Evicted, Local
+      acc[DA_MU + 0] = tot > 0 ? mz[TIER_FULL] / tot : 0.0;
+      acc[DA_MU + 1] = tot > 0 ? mz[TIER_QUANT] / tot : 0.0;
+      acc[DA_MU + 2] = tot > 0 ? mz[TIER_EVICT] / tot : 0.0;
+      acc[DA_MU + 3] = tot > 0 ? mz[TIER_LOCAL] / tot : 0.0;
+      acc[DA_EVENTS] = e + 1;
     }
-    if (e >= 1 && nq > 0 && nf > 0) {   // a non-empty Quantized tier
-      acc[DA_QSA_SUM] += dot / sqrt(nq * nf);
-      acc[DA_RQ_SUM] += sq / sf;
-      acc[DA_QSA_CNT] += 1.0;
-    }
-    const double tot = mz[0] + mz[1] + mz[2] + mz[3];
-    // shares in the order Full, Quantized, Evicted, Local
-    acc[DA_MU + 0] = tot > 0 ? mz[TIER_FULL] / tot : 0.0;
-    acc[DA_MU + 1] = tot > 0 ? mz[TIER_QUANT] / tot : 0.0;
-    acc[DA_MU + 2] = tot > 0 ? mz[TIER_EVICT] / tot : 0.0;
-    acc[DA_MU + 3] = tot > 0 ? mz[TIER_LOCAL] / tot : 0.0;
-    acc[DA_EVENTS] = e + 1;
   }
 
-  // 3. selections X of the policy's Full tier and of the FullKV top-K_f: history, LIR episodes, lags
+  // 4. the FullKV top-K_f selection: radix select of the K_f-th smallest key (score descending, window
+  //    id ascending) among the routed windows, 8 bits per pass
+  auto key_of = [&](int w) -> unsigned long long {
+    return ((unsigned long long)(~__float_as_uint(s_full[w])) << 32) | (unsigned)w;
+  };
+  const bool all_in = n_route <= P.k_f;
+  if (tid == 0) {
+    s_prefix = 0ull;
+    s_want = P.k_f;   // 1-based rank of the last selected key
+  }
+  unsigned long long mask = 0ull;
+  for (int shift = 56; shift >= 0 && !all_in; shift -= 8) {
+    for (int i = tid; i < 256; i += nt) hist[i] = 0u;
+    __syncthreads();
+    const unsigned long long prefix = s_prefix;
+    for (int w = tid; w < n_route; w += nt) {
+      const unsigned long long k = key_of(w);
+      if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l holds bins 8l .. 8l+7; find the bin where the running count reaches the wanted rank
+      unsigned c[8], sum = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        c[i] = hist[8 * lane + i];
+        sum += c[i];
+      }
+      unsigned incl = sum;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const unsigned y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      const unsigned want = (unsigned)s_want;
+      unsigned before = incl - sum;
+      if (before < want && want <= incl) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (before < want && want <= before + c[i]) {
+            s_prefix = prefix | ((unsigned long long)(8 * lane + i) << shift);
+            s_want = (int)(want - before);
+          }
+          before += c[i];
+        }
+      }
+    }
+    mask |= 255ull << shift;
+    __syncthreads();
+  }
+  const unsigned long long kth = s_prefix;
+
+  // 5. selections X of the policy's Full tier and of the FullKV top-K_f: history, LIR episodes, lags
   uint32_t *xp = Dg.xpol(unit), *xo = Dg.xorc(unit);
   int *rp = Dg.runpol(unit), *ro = Dg.runorc(unit), *since = Dg.since(unit);
   const int m = Dg.lir_m;
   for (int w = tid; w < n_route; w += nt) {
-    const int tier = state[w] & 3;
-    const float a = s_full[w];
-    int rank = 0;
-    for (int v = 0; v < n_route; ++v) {
-      const float b = s_full[v];
-      rank += (b > a || (b == a && v < w)) ? 1 : 0;
-    }
-    const uint32_t Xp = tier == TIER_FULL ? 1u : 0u, Xo = rank < P.k_f ? 1u : 0u;
+    const uint32_t Xp = s_tier[w] == TIER_FULL ? 1u : 0u, Xo = (all_in || key_of(w) <= kth) ? 1u : 0u;
     if (since[w] < 0) {
       since[w] = e;
       xp[w] = xo[w] = 0u;
@@ -305,14 +400,14 @@ cudaError_t launch_diag_collect(const CacheDev &R, const DiagDev &Dg, cudaStream
 }
 
 cudaError_t launch_diag_event(const CacheDev &P, const CacheDev &R, const DiagDev &Dg, int e, cudaStream_t s) {
-  const size_t smem = (size_t)P.n_windows * sizeof(float);
+  const size_t smem = (size_t)P.n_windows * 9;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev]) {
-    err = cudaFuncSetAttribute(diag_event_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 8192 * 4);
+    err = cudaFuncSetAttribute(diag_event_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 8192 * 9);
     if (err != cudaSuccess) return err;
     attr_set[dev] = true;
   }
