@@ -182,6 +182,7 @@ qevict_status qevict_set_rope_table(qevict_cache *cache, const float *d_table, i
  * prompt) S0[j] = (1/h_q) sum_h sum_{tau < P} sum_{i in w_j, i <= tau} a_tau^h(i), dense causal
  * attention of every prompt query.  q_prompt [batch][P][h_q][d], k_prompt [batch][P][h_kv][d];
  * s0_out [batch][ceil((P - n_sink) / window)] fp32.  Prompts are per layer: call once per layer.
+ * q_prompt and k_prompt must be 16-byte aligned (TMA tensor maps), else QEVICT_EINVAL.
  * Scratch: a region of the arena reserved for it (no allocation); reads the inputs twice. */
 qevict_status qevict_prefill_scores(const qevict_cache *cache, const void *q_prompt, const void *k_prompt,
                                     float *s0_out, qevict_stream_t stream);
@@ -244,7 +245,7 @@ qevict_status qevict_check(qevict_cache *cache, qevict_stream_t stream);
  * input and output buffers.  Its scratch is a fixed 8 MiB array inside the library image, held on
  * every GPU that loads the library until the process exits; nothing is allocated per call.
  *   q_prompt [batch][prompt_len][h_q][128], k_prompt [batch][prompt_len][h_kv][128] bf16 (device);
- *   s0_out [batch][ceil((prompt_len - n_sink) / window)] fp32 (device).
+ *   s0_out [batch][ceil((prompt_len - n_sink) / window)] fp32 (device).  q_prompt, k_prompt 16-byte aligned.
  * Errors: QEVICT_EINVAL for bad sizes or NULL pointers; QEVICT_ENOMEM when
  * 2 * batch * h_q * prompt_len > QEVICT_NOALLOC_SCRATCH_FLOATS (nothing is enqueued then).
  * The first call on a device looks up the scratch address with that device current; make that first

@@ -283,7 +283,8 @@ qevict_status qevict_set_rope_table(qevict_cache *cache, const float *d_table, i
 
 qevict_status qevict_prefill_scores(const qevict_cache *cache, const void *q_prompt, const void *k_prompt,
                                     float *s0_out, qevict_stream_t stream) {
-  if (!cache || !q_prompt || !k_prompt || !s0_out) return QEVICT_EINVAL;
+  if (!cache || !q_prompt || !k_prompt || !s0_out || (((uintptr_t)q_prompt | (uintptr_t)k_prompt) & 15))
+    return QEVICT_EINVAL;
   return cuda_status(qv::launch_prefill_scores(cache->dev, static_cast<const __nv_bfloat16 *>(q_prompt),
                                                static_cast<const __nv_bfloat16 *>(k_prompt), s0_out,
                                                reinterpret_cast<cudaStream_t>(stream)));
@@ -292,7 +293,7 @@ qevict_status qevict_prefill_scores(const qevict_cache *cache, const void *q_pro
 qevict_status qevict_prefill_route(qevict_cache *cache, int32_t layer, const void *k_prompt, const void *v_prompt,
                                    const float *s0, const void *q_prompt, qevict_stream_t stream) {
   if (!cache || layer < 0 || layer >= cache->cfg.n_layers || !k_prompt || !v_prompt) return QEVICT_EINVAL;
-  if (!s0 && !q_prompt) return QEVICT_EINVAL;
+  if (!s0 && (!q_prompt || (((uintptr_t)q_prompt | (uintptr_t)k_prompt) & 15))) return QEVICT_EINVAL;
   if (cache->prefilled[layer] || (cache->cfg.rope && !cache->rope_set)) return QEVICT_ESCHEDULE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const auto *kp = static_cast<const __nv_bfloat16 *>(k_prompt);

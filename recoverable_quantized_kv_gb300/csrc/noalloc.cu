@@ -29,17 +29,19 @@ namespace {
 
 constexpr long long kScratchFloats = QEVICT_NOALLOC_SCRATCH_FLOATS;
 static __device__ __align__(256) float g_noalloc_scratch[kScratchFloats];
+static __device__ int g_noalloc_status;   // the scoring kernels' bounded waits record timeouts here
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 float *g_scratch_addr[kMaxDevices] = {};   // device address of g_noalloc_scratch, per device
+int *g_status_addr[kMaxDevices] = {};      // device address of g_noalloc_status, per device
 
 }  // namespace
 
 extern "C" qevict_status qevict_prefill_scores_noalloc(int32_t batch, int32_t prompt_len, int32_t h_q, int32_t h_kv,
                                                        int32_t n_sink, int32_t window, const void *q_prompt,
                                                        const void *k_prompt, float *s0_out, qevict_stream_t stream) {
-  if (!q_prompt || !k_prompt || !s0_out || batch < 1 || h_kv < 1 || h_q < h_kv || h_q % h_kv || window < 1 ||
+  if (!q_prompt || !k_prompt || !s0_out || (((uintptr_t)q_prompt | (uintptr_t)k_prompt) & 15) || batch < 1 || h_kv < 1 || h_q < h_kv || h_q % h_kv || window < 1 ||
       n_sink < 0 || prompt_len <= n_sink)
     return QEVICT_EINVAL;
   const int G = h_q / h_kv;
@@ -50,19 +52,25 @@ extern "C" qevict_status qevict_prefill_scores_noalloc(int32_t batch, int32_t pr
   if (cudaGetDevice(&dev) != cudaSuccess) return QEVICT_ECUDA;
   if (dev < 0 || dev >= kMaxDevices) return QEVICT_EINVAL;
   float *scratch;
+  int *status;
   {
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_scratch_addr[dev]) {
       void *p = nullptr;
       if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return QEVICT_ECUDA;
+      void *st = nullptr;
+      if (cudaGetSymbolAddress(&st, g_noalloc_status) != cudaSuccess || !st) return QEVICT_ECUDA;
       g_scratch_addr[dev] = static_cast<float *>(p);
+      g_status_addr[dev] = static_cast<int *>(st);
     }
     scratch = g_scratch_addr[dev];
+    status = g_status_addr[dev];
   }
   qv::CacheDev C = {};
   C.arena = reinterpret_cast<uint8_t *>(scratch);
   C.off_rowstat = 0;
   C.off_colsum = per_array * (long long)sizeof(float);
+  C.off_status = reinterpret_cast<uint8_t *>(status) - C.arena;   // a word of its own, outside the scratch
   C.B = batch;
   C.h_q = h_q;
   C.h_kv = h_kv;

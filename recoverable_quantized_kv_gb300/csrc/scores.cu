@@ -8,194 +8,239 @@
 //   pass 1: row log2-sum-exp of the scaled logits of every query, online;
 //   pass 2: column sum of 2^(logit - rowLSE) of every key over the queries at or after it;
 //   pass 3: per-window sums over the heads in a fixed order (deterministic).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "cache_dev.cuh"
 #include "common.cuh"
 
 namespace qv {
 
-// Both passes are flash-attention-shaped contractions on the tensor cores (mma.m16n8k16, bf16 in,
-// fp32 accumulate).  A CTA of 4 warps owns 64 rows (queries in pass 1, keys in pass 2), each warp
-// 16 of them with its A fragments in registers; the other operand streams through shared memory in
-// 64-row tiles (double-buffered with cp.async, rows padded to 136 elements so ldmatrix is free of
-// bank conflicts), and every row's reduction stays inside its 4 owning lanes.
-constexpr int SC_WARPS = 4;
-constexpr int SC_TILE = 64;            // rows per CTA and rows per streamed tile
-constexpr int SC_LD = D + 8;           // padded shared-memory row, elements
+// Both passes run on the 5th-generation tensor cores: a CTA owns 128 rows (queries in pass 1, keys in
+// pass 2) of one (sequence, head) and streams the other operand in 128-row tiles.  A producer thread
+// loads tiles with TMA (tensor maps over the [B][P][heads][128] prompt tensors, 128-byte swizzle, rows
+// past the prompt zero-filled) into a two-stage ring; one thread issues tcgen05.mma (M = N = 128, K = 16
+// per instruction, bf16 in, fp32 out) into one of two TMEM accumulators; four epilogue warps read their
+// 32 TMEM lanes each with tcgen05.ld, so every thread owns one row and reduces it without shuffles.
+// Every wait is bounded; the TMEM columns are released on every path.
+constexpr int TC_ROWS = 128;                         // rows per CTA and per streamed tile
+constexpr int TC_STAGES = 2;
+constexpr int TC_THREADS = 192;                      // warps 0-3 epilogue, 4 TMA producer, 5 MMA issuer
+constexpr int TC_TILE_BYTES = TC_ROWS * D * 2;       // 32 KB: two 128-byte-swizzled blocks of 64 dims
+constexpr int TC_KBLOCK = TC_TILE_BYTES / 2;
+constexpr int TC_TMEM_COLS = 2 * TC_ROWS;            // two fp32 accumulators of 128 columns
+constexpr int TC_OFF_RS = TC_TILE_BYTES * (1 + TC_STAGES);     // pass 2: row statistics of two tiles
+constexpr int TC_OFF_BAR = TC_OFF_RS + 2 * TC_ROWS * 4;
+constexpr int TC_NBAR = 2 * TC_STAGES + 4 + 2;       // full, empty, tfull[2], tempty[2], afull, fin
+constexpr int TC_SMEM = 1024 + TC_OFF_BAR + TC_NBAR * 8 + 16;
 
-__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc, bool valid) {
-  const int n = valid ? 16 : 0;        // zero-fill rows past the prompt
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem_dst)), "l"(gsrc), "r"(n) : "memory");
+// tcgen05 shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+// instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both K-major, M = N = 128
+constexpr uint32_t TC_IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(TC_ROWS >> 3) << 17) |
+                              ((uint32_t)(TC_ROWS >> 4) << 24);
 
-__device__ __forceinline__ void ldsm_x4(const void *p, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(smem_u32(p)));
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, int x, int y, int z, int w,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+      : "memory");
 }
-
-// Stage rows [r0, r0 + 64) of a [B][P][heads][D] bf16 tensor (head hh of sequence b) into a
-// padded shared tile; rows at or past P are zero-filled.
-__device__ __forceinline__ void stage_tile(__nv_bfloat16 *dst, const __nv_bfloat16 *src, int b, int P, int heads,
-                                           int hh, int r0) {
-  for (int idx = threadIdx.x; idx < SC_TILE * (D / 8); idx += SC_WARPS * 32) {
-    const int r = idx / (D / 8), c = (idx % (D / 8)) * 8;
-    const int row = r0 + r;
-    const bool valid = row < P;
-    const __nv_bfloat16 *g = src + (((size_t)b * P + (valid ? row : 0)) * heads + hh) * D + c;
-    cp_async16(dst + r * SC_LD + c, g, valid);
-  }
-  cp_async_commit();
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
 }
-
-// A fragments of 16 rows [r0, r0 + 16) x 128 dims straight from global (zero rows past P).
-__device__ __forceinline__ void load_a_frags(uint32_t (&a)[8][4], const __nv_bfloat16 *src, int b, int P, int heads,
-                                             int hh, int r0) {
-  const int lane = threadIdx.x & 31, gl = lane >> 2, tl = lane & 3;
-  const int ra = r0 + gl, rb = r0 + gl + 8;
-  const uint32_t *pa = reinterpret_cast<const uint32_t *>(src + (((size_t)b * P + min(ra, P - 1)) * heads + hh) * D);
-  const uint32_t *pb = reinterpret_cast<const uint32_t *>(src + (((size_t)b * P + min(rb, P - 1)) * heads + hh) * D);
+__device__ __forceinline__ void tc_mma(uint32_t tmem, uint64_t da, uint64_t db, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem),
+      "l"(da), "l"(db), "r"(TC_IDESC), "r"(accumulate)
+      : "memory");
+}
+// 32 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld32(uint32_t addr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(addr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    a[j][0] = ra < P ? __ldg(pa + 8 * j + tl) : 0u;
-    a[j][1] = rb < P ? __ldg(pb + 8 * j + tl) : 0u;
-    a[j][2] = ra < P ? __ldg(pa + 8 * j + tl + 4) : 0u;
-    a[j][3] = rb < P ? __ldg(pb + 8 * j + tl + 4) : 0u;
-  }
+  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
 }
 
-// S[16 x 64] = A (16 rows x 128) . B^T, B = the 64 staged rows; s[n][*] covers tile columns 8n..8n+7.
-__device__ __forceinline__ void tile_mma(float (&s)[8][4], const uint32_t (&a)[8][4], const __nv_bfloat16 *tile) {
-  const int lane = threadIdx.x & 31;
-  // ldmatrix x4 row addresses: matrices (n, dims 16j..+7), (n, 16j+8..), (n+1, 16j..), (n+1, 16j+8..)
-  const int mrow = (lane & 7) + ((lane >> 4) << 3), mcol = ((lane >> 3) & 1) * 8;
-#pragma unroll
-  for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-#pragma unroll
-    for (int n = 0; n < 8; n += 2) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(tile + (8 * n + mrow) * SC_LD + 16 * j + mcol, b0, b1, b2, b3);
-      mma_bf16(s[n], a[j][0], a[j][1], a[j][2], a[j][3], b0, b1);
-      mma_bf16(s[n + 1], a[j][0], a[j][1], a[j][2], a[j][3], b2, b3);
-    }
-  }
-}
-
-// Pass 1: rowstat[b][h][tau] = log2 sum_{i <= tau} 2^(q_tau . k_i * scale_log2).
-__global__ void __launch_bounds__(SC_WARPS * 32) rowstat_kernel(const CacheDev C, const __nv_bfloat16 *q,
-                                                                const __nv_bfloat16 *k, float scale_log2) {
-  __shared__ __align__(128) __nv_bfloat16 kt[2][SC_TILE * SC_LD];
-  const int P = C.prompt_len;
+// COL = false, pass 1: rowstat[b][h][tau] = log2 sum_{i <= tau} 2^(q_tau . k_i * scale_log2).
+// COL = true,  pass 2: colsum[b][h][i] = sum_{tau >= i} 2^(q_tau . k_i * scale_log2 - rowstat[tau]).
+template <bool COL>
+__global__ void __launch_bounds__(TC_THREADS) tc_score_kernel(const __grid_constant__ CUtensorMap tq,
+                                                              const __grid_constant__ CUtensorMap tk,
+                                                              const CacheDev C, int *status, float scale_log2) {
+  extern __shared__ uint8_t tc_smem_raw[];
+  uint8_t *sm = tc_smem_raw + ((1024 - (smem_u32(tc_smem_raw) & 1023)) & 1023);   // swizzle atoms: 1024-aligned
+  uint8_t *sA = sm;
+  float *rsb = reinterpret_cast<float *>(sm + TC_OFF_RS);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + TC_OFF_BAR);
+  uint64_t *full = bars, *empty = bars + TC_STAGES, *tfull = bars + 2 * TC_STAGES, *tempty = tfull + 2;
+  uint64_t *afull = tempty + 2, *fin = afull + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + TC_NBAR);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int P = C.prompt_len, nrt = (P + TC_ROWS - 1) / TC_ROWS;
   const int h = blockIdx.y, b = blockIdx.z, g = h / C.G;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gl = lane >> 2, tl = lane & 3;
-  const int q0 = blockIdx.x * SC_TILE, r0 = q0 + 16 * warp;
-  uint32_t qa[8][4];
-  load_a_frags(qa, q, b, P, C.h_q, h, r0);
-  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};   // rows gl, gl+8; l is this lane's partial sum
-  const int ntiles = q0 / SC_TILE + 1;   // key tiles up to the diagonal
-  stage_tile(kt[0], k, b, P, C.h_kv, g, 0);
-  for (int t = 0; t < ntiles; ++t) {
-    if (t + 1 < ntiles) {
-      stage_tile(kt[(t + 1) & 1], k, b, P, C.h_kv, g, (t + 1) * SC_TILE);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    float s[8][4];
-    tile_mma(s, qa, kt[t & 1]);
-    const int k0 = t * SC_TILE;
-    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int n = 0; n < 8; ++n)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int row = r0 + gl + ((c >> 1) << 3), key = k0 + 8 * n + 2 * tl + (c & 1);
-        const float v = (key <= row && key < P) ? s[n][c] * scale_log2 : -INFINITY;
-        s[n][c] = v;
-        mx[c >> 1] = fmaxf(mx[c >> 1], v);
-      }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-      const float mn = fmaxf(m[r], mx[r]);
-      if (mn != -INFINITY) {
-        l[r] *= exp2f(m[r] - mn);
-        m[r] = mn;
-      }
-    }
-#pragma unroll
-    for (int n = 0; n < 8; ++n)
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        if (s[n][c] != -INFINITY) l[c >> 1] += exp2f(s[n][c] - m[c >> 1]);
-    __syncthreads();   // the tile is consumed before the next stage overwrites it
-  }
-#pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
-    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
-    const int row = r0 + gl + 8 * r;
-    if (tl == 0 && row < P)
-      reinterpret_cast<float *>(C.arena + C.off_rowstat)[((size_t)b * C.h_q + h) * P + row] = m[r] + __log2f(l[r]);
-  }
-}
+  const int rt = COL ? (int)blockIdx.x : nrt - 1 - (int)blockIdx.x;   // pass 1: the longest rows first
+  const int r0 = rt * TC_ROWS;
+  const int t_begin = COL ? rt : 0, nb = COL ? nrt - rt : rt + 1;
 
-// Pass 2: colsum[b][h][i] = sum_{tau >= i} 2^(q_tau . k_i * scale_log2 - rowstat[tau]).  Keys are
-// the rows here (S^T = K Q^T), so a key's sum over queries stays in its 4 lanes.
-__global__ void __launch_bounds__(SC_WARPS * 32) colsum_kernel(const CacheDev C, const __nv_bfloat16 *q,
-                                                               const __nv_bfloat16 *k, float scale_log2) {
-  __shared__ __align__(128) __nv_bfloat16 qt[2][SC_TILE * SC_LD];
-  __shared__ float rs[2][SC_TILE];
-  const int P = C.prompt_len;
-  const int h = blockIdx.y, b = blockIdx.z, g = h / C.G;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gl = lane >> 2, tl = lane & 3;
-  const int i0 = blockIdx.x * SC_TILE, r0 = i0 + 16 * warp;
-  const float *rowstat = reinterpret_cast<const float *>(C.arena + C.off_rowstat) + ((size_t)b * C.h_q + h) * P;
-  uint32_t ka[8][4];
-  load_a_frags(ka, k, b, P, C.h_kv, g, r0);
-  float col[2] = {0.f, 0.f};   // keys gl, gl+8: this lane's partial sums
-  const int t0 = i0 / SC_TILE, ntiles = (P + SC_TILE - 1) / SC_TILE;
-  auto stage = [&](int t, int buf) {
-    if (threadIdx.x < SC_TILE) {
-      const int row = t * SC_TILE + threadIdx.x;
-      rs[buf][threadIdx.x] = row < P ? rowstat[row] : 0.f;
-    }
-    stage_tile(qt[buf], q, b, P, C.h_q, h, t * SC_TILE);
-  };
-  stage(t0, 0);
-  for (int t = t0; t < ntiles; ++t) {
-    const int buf = (t - t0) & 1;
-    if (t + 1 < ntiles) {
-      stage(t + 1, buf ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-    float s[8][4];
-    tile_mma(s, ka, qt[buf]);
-    const int qq0 = t * SC_TILE;
-#pragma unroll
-    for (int n = 0; n < 8; ++n)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int key = r0 + gl + ((c >> 1) << 3), qc = 8 * n + 2 * tl + (c & 1), query = qq0 + qc;
-        if (query >= key && query < P) col[c >> 1] += exp2f(s[n][c] * scale_log2 - rs[buf][qc]);
-      }
-    __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < TC_NBAR; ++i) mbar_init(&bars[i], (&bars[i] >= tempty && &bars[i] < tempty + 2) ? 128 : 1);
+    fence_mbar_init();
   }
+  if (warp == 5) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TC_TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // A: pass 1 the 128 queries of head h, pass 2 the 128 keys of KV head g; B tiles the other operand
+  const CUtensorMap *mapA = COL ? &tk : &tq, *mapB = COL ? &tq : &tk;
+  const int headA = COL ? g : h, headB = COL ? h : g;
+
+  if (warp == 4) {
+    if (lane == 0) {   // ---- TMA producer
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(mapA)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(mapB)) : "memory");
+      mbar_arrive_expect_tx(afull, TC_TILE_BYTES);
+      tma_load_4d(sA, mapA, 0, headA, r0, b, afull);
+      tma_load_4d(sA + TC_KBLOCK, mapA, 64, headA, r0, b, afull);
+      int issued = 0;
+      for (int i = 0; i < nb; ++i) {
+        const int s = i % TC_STAGES;
+        if (!mbar_wait(&empty[s], ((i / TC_STAGES) & 1) ^ 1, status)) break;
+        uint8_t *dst = sm + TC_TILE_BYTES * (1 + s);
+        mbar_arrive_expect_tx(&full[s], TC_TILE_BYTES);
+        tma_load_4d(dst, mapB, 0, headB, (t_begin + i) * TC_ROWS, b, &full[s]);
+        tma_load_4d(dst + TC_KBLOCK, mapB, 64, headB, (t_begin + i) * TC_ROWS, b, &full[s]);
+        issued = i + 1;
+      }
+      // copies still in flight land before the CTA leaves (normally all were consumed already)
+      for (int i = max(0, issued - TC_STAGES); i < issued; ++i)
+        mbar_wait(&full[i % TC_STAGES], (i / TC_STAGES) & 1, status);
+      mbar_wait(afull, 0, status);
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {   // ---- MMA issuer
+      bool ok = mbar_wait(afull, 0, status);
+      const uint32_t a0 = smem_u32(sA);
+      for (int i = 0; ok && i < nb; ++i) {
+        const int s = i % TC_STAGES, buf = i & 1;
+        if (!mbar_wait(&full[s], (i / TC_STAGES) & 1, status)) break;
+        if (!mbar_wait(&tempty[buf], ((i >> 1) & 1) ^ 1, status)) break;
+        tc_fence_after();
+        const uint32_t b0 = smem_u32(sm + TC_TILE_BYTES * (1 + s));
 #pragma unroll
-  for (int r = 0; r < 2; ++r) {
-    col[r] += __shfl_xor_sync(0xffffffffu, col[r], 1);
-    col[r] += __shfl_xor_sync(0xffffffffu, col[r], 2);
-    const int key = r0 + gl + 8 * r;
-    if (tl == 0 && key < P) reinterpret_cast<float *>(C.arena + C.off_colsum)[((size_t)b * C.h_q + h) * P + key] = col[r];
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * TC_KBLOCK + (kk & 3) * 32;   // 16 dims = 32 B inside a 128-B row
+          tc_mma(tmem + buf * TC_ROWS, umma_desc(a0 + off), umma_desc(b0 + off), kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&empty[s]);
+        tc_commit(&tfull[buf]);
+      }
+      tc_commit(fin);   // every MMA issued above has completed once this arrives
+      mbar_wait(fin, 0, status);
+    }
+  } else {
+    // ---- epilogue: thread = TMEM lane = row r0 + row
+    const int row = 32 * warp + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+    bool ok = true;
+    if (!COL) {
+      const int qrow = r0 + row;
+      float m = -INFINITY, l = 0.f;
+      for (int i = 0; i < nb; ++i) {
+        const int buf = i & 1;
+        if (ok) ok = mbar_wait(&tfull[buf], (i >> 1) & 1, status);
+        tc_fence_after();
+        const bool diag = i == rt;   // key tile i meets the query tile on the diagonal
+#pragma unroll 1
+        for (int c0 = 0; c0 < TC_ROWS; c0 += 32) {
+          float v[32];
+          tmem_ld32(lane_addr + buf * TC_ROWS + c0, v);
+          float mx = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (diag && c0 + j > row) v[j] = -INFINITY;   // causal: keys after the query
+            mx = fmaxf(mx, v[j]);
+          }
+          const float mn = fmaxf(m, mx * scale_log2);
+          if (mn != -INFINITY) {   // the chunk holds a key at or before the query
+            float acc = l * exp2f(m - mn);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc += exp2f(fmaf(v[j], scale_log2, -mn));
+            l = acc;
+            m = mn;
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[buf]);
+      }
+      if (qrow < P) reinterpret_cast<float *>(C.arena + C.off_rowstat)[((size_t)b * C.h_q + h) * P + qrow] = m + __log2f(l);
+    } else {
+      const int key = r0 + row;
+      const float *rowstat = reinterpret_cast<const float *>(C.arena + C.off_rowstat) + ((size_t)b * C.h_q + h) * P;
+      float col = 0.f;
+      int tau = t_begin * TC_ROWS + row;
+      float nxt = tau < P ? rowstat[tau] : 0.f;   // the row statistic of query tau, one tile ahead
+      for (int i = 0; i < nb; ++i) {
+        const int t = t_begin + i, buf = i & 1;
+        rsb[buf * TC_ROWS + row] = nxt;
+        tau += TC_ROWS;
+        if (i + 1 < nb) nxt = tau < P ? rowstat[tau] : 0.f;
+        asm volatile("bar.sync 1, 128;" ::: "memory");   // the tile's row statistics, epilogue warps only
+        if (ok) ok = mbar_wait(&tfull[buf], (i >> 1) & 1, status);
+        tc_fence_after();
+        const bool diag = t == rt, tail = (t + 1) * TC_ROWS > P;
+        const float *rs = rsb + buf * TC_ROWS;
+#pragma unroll 1
+        for (int c0 = 0; c0 < TC_ROWS; c0 += 32) {
+          float v[32];
+          tmem_ld32(lane_addr + buf * TC_ROWS + c0, v);
+          if (!diag && !tail) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) col += exp2f(fmaf(v[j], scale_log2, -rs[c0 + j]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int c = c0 + j;
+              const bool valid = (!diag || c >= row) && t * TC_ROWS + c < P;   // causal, inside the prompt
+              col += valid ? exp2f(fmaf(v[j], scale_log2, -rs[c])) : 0.f;
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[buf]);
+      }
+      if (key < P) reinterpret_cast<float *>(C.arena + C.off_colsum)[((size_t)b * C.h_q + h) * P + key] = col;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_TMEM_COLS) : "memory");
   }
 }
 
@@ -213,13 +258,56 @@ __global__ void window_sum_kernel(const CacheDev C, float *s0) {
   s0[(size_t)b * npw + j] = s / (float)C.h_q;
 }
 
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// [B][P][heads][128] bf16 as a 4-D tensor map; a box is 64 dims x 1 head x 128 rows, 128-byte swizzled
+bool prompt_map(CUtensorMap *map, const __nv_bfloat16 *base, int B, int P, int heads) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)P, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2, (cuuint64_t)P * heads * D * 2};
+  const cuuint32_t box[4] = {64, 1, (cuuint32_t)TC_ROWS, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<__nv_bfloat16 *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
 cudaError_t launch_prefill_scores(const CacheDev &C, const __nv_bfloat16 *q, const __nv_bfloat16 *k, float *s0,
                                   cudaStream_t stream) {
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
   const int P = C.prompt_len;
-  dim3 grid((P + SC_TILE - 1) / SC_TILE, C.h_q, C.B);
-  rowstat_kernel<<<grid, SC_WARPS * 32, 0, stream>>>(C, q, k, scale_log2);
-  colsum_kernel<<<grid, SC_WARPS * 32, 0, stream>>>(C, q, k, scale_log2);
+  if (((uintptr_t)q | (uintptr_t)k) & 15) return cudaErrorInvalidValue;   // tensor maps: 16-byte aligned bases
+  CUtensorMap tq, tk;
+  if (!prompt_map(&tq, q, C.B, P, C.h_q) || !prompt_map(&tk, k, C.B, P, C.h_kv)) return cudaErrorInvalidValue;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    e = cudaFuncSetAttribute(tc_score_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(tc_score_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  int *status = C.status();
+  dim3 grid((P + TC_ROWS - 1) / TC_ROWS, C.h_q, C.B);
+  tc_score_kernel<false><<<grid, TC_THREADS, TC_SMEM, stream>>>(tq, tk, C, status, scale_log2);
+  tc_score_kernel<true><<<grid, TC_THREADS, TC_SMEM, stream>>>(tq, tk, C, status, scale_log2);
   const int npw = (P - C.n_sink + C.W - 1) / C.W;
   window_sum_kernel<<<dim3((npw + 127) / 128, C.B), 128, 0, stream>>>(C, s0);
   return cudaGetLastError();
