@@ -323,7 +323,8 @@ def run_gpu(args, rank, world):
     tpeak, tpeak_kind = measured_tensor_peak()
     prefill_scores = {"ms_per_layer": pre_ms, "tflops": pre_tf, "peak_tflops": tpeak, "frac": pre_tf / tpeak,
                       "flops_per_layer": pre_flops,
-                      "note": "causal FLOPs of both passes (row log-sum-exp, column sums), mma.m16n8k16 bf16; "
+                      "note": "causal FLOPs of both passes (row log-sum-exp, column sums), tcgen05.mma M=N=128 bf16 "
+                              "with TMA tensor-map loads; "
                               f"peak = {tpeak_kind} dense bf16 burst"}
     del pq, pk, ps0
 

@@ -20,17 +20,21 @@ namespace qv {
 // pass 2) of one (sequence, head) and streams the other operand in 128-row tiles.  A producer thread
 // loads tiles with TMA (tensor maps over the [B][P][heads][128] prompt tensors, 128-byte swizzle, rows
 // past the prompt zero-filled) into a two-stage ring; one thread issues tcgen05.mma (M = N = 128, K = 16
-// per instruction, bf16 in, fp32 out) into one of two TMEM accumulators; four epilogue warps read their
-// 32 TMEM lanes each with tcgen05.ld, so every thread owns one row and reduces it without shuffles.
+// per instruction, bf16 in, fp32 out) into one of two TMEM accumulators; eight epilogue warps read
+// TMEM with tcgen05.ld: warp w takes the 32 lanes (rows) 32 (w % 4) .. and the 64 columns 64 (w / 4) ..,
+// so every thread reduces half a row without shuffles and the two halves meet once at the end.
 // Every wait is bounded; the TMEM columns are released on every path.
 constexpr int TC_ROWS = 128;                         // rows per CTA and per streamed tile
 constexpr int TC_STAGES = 2;
-constexpr int TC_THREADS = 192;                      // warps 0-3 epilogue, 4 TMA producer, 5 MMA issuer
+constexpr int TC_EPI = 8;                            // epilogue warps
+constexpr int TC_THREADS = (TC_EPI + 2) * 32;        // + 1 TMA producer warp + 1 MMA issuer warp
+constexpr int TC_PRODUCER = TC_EPI, TC_ISSUER = TC_EPI + 1;
 constexpr int TC_TILE_BYTES = TC_ROWS * D * 2;       // 32 KB: two 128-byte-swizzled blocks of 64 dims
 constexpr int TC_KBLOCK = TC_TILE_BYTES / 2;
 constexpr int TC_TMEM_COLS = 2 * TC_ROWS;            // two fp32 accumulators of 128 columns
 constexpr int TC_OFF_RS = TC_TILE_BYTES * (1 + TC_STAGES);     // pass 2: row statistics of two tiles
-constexpr int TC_OFF_BAR = TC_OFF_RS + 2 * TC_ROWS * 4;
+constexpr int TC_OFF_HALF = TC_OFF_RS + 2 * TC_ROWS * 4;       // the second column half's partials
+constexpr int TC_OFF_BAR = TC_OFF_HALF + 2 * TC_ROWS * 4;
 constexpr int TC_NBAR = 2 * TC_STAGES + 4 + 2;       // full, empty, tfull[2], tempty[2], afull, fin
 constexpr int TC_SMEM = 1024 + TC_OFF_BAR + TC_NBAR * 8 + 16;
 
@@ -64,6 +68,12 @@ __device__ __forceinline__ void tc_mma(uint32_t tmem, uint64_t da, uint64_t db, 
       "l"(da), "l"(db), "r"(TC_IDESC), "r"(accumulate)
       : "memory");
 }
+__device__ __forceinline__ float ex2(float x) {   // 2^x on the special-function unit, subnormal results as 0
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // 32 consecutive fp32 columns of this thread's TMEM lane
 __device__ __forceinline__ void tmem_ld32(uint32_t addr, float (&v)[32]) {
   uint32_t r[32];
@@ -102,10 +112,11 @@ __global__ void __launch_bounds__(TC_THREADS) tc_score_kernel(const __grid_const
   const int t_begin = COL ? rt : 0, nb = COL ? nrt - rt : rt + 1;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < TC_NBAR; ++i) mbar_init(&bars[i], (&bars[i] >= tempty && &bars[i] < tempty + 2) ? 128 : 1);
+    for (int i = 0; i < TC_NBAR; ++i)
+      mbar_init(&bars[i], (&bars[i] >= tempty && &bars[i] < tempty + 2) ? TC_EPI * 32 : 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == TC_ISSUER) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(TC_TMEM_COLS)
                  : "memory");
@@ -119,7 +130,7 @@ __global__ void __launch_bounds__(TC_THREADS) tc_score_kernel(const __grid_const
   const CUtensorMap *mapA = COL ? &tk : &tq, *mapB = COL ? &tq : &tk;
   const int headA = COL ? g : h, headB = COL ? h : g;
 
-  if (warp == 4) {
+  if (warp == TC_PRODUCER) {
     if (lane == 0) {   // ---- TMA producer
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(mapA)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(mapB)) : "memory");
@@ -141,7 +152,7 @@ __global__ void __launch_bounds__(TC_THREADS) tc_score_kernel(const __grid_const
         mbar_wait(&full[i % TC_STAGES], (i / TC_STAGES) & 1, status);
       mbar_wait(afull, 0, status);
     }
-  } else if (warp == 5) {
+  } else if (warp == TC_ISSUER) {
     if (lane == 0) {   // ---- MMA issuer
       bool ok = mbar_wait(afull, 0, status);
       const uint32_t a0 = smem_u32(sA);
@@ -163,9 +174,10 @@ __global__ void __launch_bounds__(TC_THREADS) tc_score_kernel(const __grid_const
       mbar_wait(fin, 0, status);
     }
   } else {
-    // ---- epilogue: thread = TMEM lane = row r0 + row
-    const int row = 32 * warp + lane;
-    const uint32_t lane_addr = tmem + ((uint32_t)(32 * warp) << 16);
+    // ---- epilogue: thread = TMEM lane = row r0 + row, columns half * 64 .. + 63 of every tile
+    const int row = 32 * (warp & 3) + lane, half = warp >> 2, cbeg = 64 * half;
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + cbeg;
+    float *hp = reinterpret_cast<float *>(sm + TC_OFF_HALF);
     bool ok = true;
     if (!COL) {
       const int qrow = r0 + row;
@@ -176,20 +188,25 @@ __global__ void __launch_bounds__(TC_THREADS) tc_score_kernel(const __grid_const
         tc_fence_after();
         const bool diag = i == rt;   // key tile i meets the query tile on the diagonal
 #pragma unroll 1
-        for (int c0 = 0; c0 < TC_ROWS; c0 += 32) {
+        for (int c0 = 0; c0 < 64; c0 += 32) {
           float v[32];
           tmem_ld32(lane_addr + buf * TC_ROWS + c0, v);
           float mx = -INFINITY;
+          if (diag) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (diag && c0 + j > row) v[j] = -INFINITY;   // causal: keys after the query
-            mx = fmaxf(mx, v[j]);
+            for (int j = 0; j < 32; ++j) {
+              if (cbeg + c0 + j > row) v[j] = -INFINITY;   // causal: keys after the query
+              mx = fmaxf(mx, v[j]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) mx = fmaxf(mx, v[j]);
           }
           const float mn = fmaxf(m, mx * scale_log2);
           if (mn != -INFINITY) {   // the chunk holds a key at or before the query
-            float acc = l * exp2f(m - mn);
+            float acc = l * ex2(m - mn);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc += exp2f(fmaf(v[j], scale_log2, -mn));
+            for (int j = 0; j < 32; ++j) acc += ex2(fmaf(v[j], scale_log2, -mn));
             l = acc;
             m = mn;
           }
@@ -197,48 +214,61 @@ __global__ void __launch_bounds__(TC_THREADS) tc_score_kernel(const __grid_const
         tc_fence_before();
         mbar_arrive(&tempty[buf]);
       }
-      if (qrow < P) reinterpret_cast<float *>(C.arena + C.off_rowstat)[((size_t)b * C.h_q + h) * P + qrow] = m + __log2f(l);
+      // the two column halves of a row meet: (m, l) pairs merge by log-sum-exp
+      if (half) {
+        hp[row] = m;
+        hp[TC_ROWS + row] = l;
+      }
+      asm volatile("bar.sync 1, %0;" ::"r"(TC_EPI * 32) : "memory");
+      if (!half) {
+        const float m2 = hp[row], l2 = hp[TC_ROWS + row], mm = fmaxf(m, m2);
+        const float ls = (m == -INFINITY ? 0.f : l * exp2f(m - mm)) + (m2 == -INFINITY ? 0.f : l2 * exp2f(m2 - mm));
+        if (qrow < P) reinterpret_cast<float *>(C.arena + C.off_rowstat)[((size_t)b * C.h_q + h) * P + qrow] = mm + __log2f(ls);
+      }
     } else {
       const int key = r0 + row;
       const float *rowstat = reinterpret_cast<const float *>(C.arena + C.off_rowstat) + ((size_t)b * C.h_q + h) * P;
       float col = 0.f;
       int tau = t_begin * TC_ROWS + row;
-      float nxt = tau < P ? rowstat[tau] : 0.f;   // the row statistic of query tau, one tile ahead
+      float nxt = (!half && tau < P) ? rowstat[tau] : 0.f;   // the row statistic of query tau, one tile ahead
       for (int i = 0; i < nb; ++i) {
         const int t = t_begin + i, buf = i & 1;
-        rsb[buf * TC_ROWS + row] = nxt;
+        if (!half) rsb[buf * TC_ROWS + row] = nxt;
         tau += TC_ROWS;
-        if (i + 1 < nb) nxt = tau < P ? rowstat[tau] : 0.f;
-        asm volatile("bar.sync 1, 128;" ::: "memory");   // the tile's row statistics, epilogue warps only
+        if (!half && i + 1 < nb) nxt = tau < P ? rowstat[tau] : 0.f;
+        asm volatile("bar.sync 1, %0;" ::"r"(TC_EPI * 32) : "memory");   // the tile's row statistics
         if (ok) ok = mbar_wait(&tfull[buf], (i >> 1) & 1, status);
         tc_fence_after();
         const bool diag = t == rt, tail = (t + 1) * TC_ROWS > P;
-        const float *rs = rsb + buf * TC_ROWS;
+        const float *rs = rsb + buf * TC_ROWS + cbeg;
 #pragma unroll 1
-        for (int c0 = 0; c0 < TC_ROWS; c0 += 32) {
+        for (int c0 = 0; c0 < 64; c0 += 32) {
           float v[32];
           tmem_ld32(lane_addr + buf * TC_ROWS + c0, v);
           if (!diag && !tail) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) col += exp2f(fmaf(v[j], scale_log2, -rs[c0 + j]));
+            for (int j = 0; j < 32; ++j) col += ex2(fmaf(v[j], scale_log2, -rs[c0 + j]));
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-              const int c = c0 + j;
+              const int c = cbeg + c0 + j;
               const bool valid = (!diag || c >= row) && t * TC_ROWS + c < P;   // causal, inside the prompt
-              col += valid ? exp2f(fmaf(v[j], scale_log2, -rs[c])) : 0.f;
+              col += valid ? ex2(fmaf(v[j], scale_log2, -rs[c0 + j])) : 0.f;
             }
           }
         }
         tc_fence_before();
         mbar_arrive(&tempty[buf]);
       }
-      if (key < P) reinterpret_cast<float *>(C.arena + C.off_colsum)[((size_t)b * C.h_q + h) * P + key] = col;
+      if (half) hp[row] = col;
+      asm volatile("bar.sync 1, %0;" ::"r"(TC_EPI * 32) : "memory");
+      if (!half && key < P)
+        reinterpret_cast<float *>(C.arena + C.off_colsum)[((size_t)b * C.h_q + h) * P + key] = col + hp[row];
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == TC_ISSUER) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TC_TMEM_COLS) : "memory");
   }
