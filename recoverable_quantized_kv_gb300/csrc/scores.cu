@@ -16,27 +16,32 @@
 
 namespace qv {
 
-// Both passes run on the 5th-generation tensor cores: a CTA owns 128 rows (queries in pass 1, keys in
-// pass 2) of one (sequence, head) and streams the other operand in 128-row tiles.  A producer thread
-// loads tiles with TMA (tensor maps over the [B][P][heads][128] prompt tensors, 128-byte swizzle, rows
-// past the prompt zero-filled) into a two-stage ring; one thread issues tcgen05.mma (M = N = 128, K = 16
-// per instruction, bf16 in, fp32 out) into one of two TMEM accumulators; eight epilogue warps read
-// TMEM with tcgen05.ld: warp w takes the 32 lanes (rows) 32 (w % 4) .. and the 64 columns 64 (w / 4) ..,
-// so every thread reduces half a row without shuffles and the two halves meet once at the end.
-// Every wait is bounded; the TMEM columns are released on every path.
-constexpr int TC_ROWS = 128;                         // rows per CTA and per streamed tile
-constexpr int TC_STAGES = 2;
-constexpr int TC_EPI = 8;                            // epilogue warps
+// Both passes run on the 5th-generation tensor cores.  A CTA (one per SM) owns two row tiles of 128 rows
+// (queries in pass 1, keys in pass 2) of one (sequence, head); both multiply every streamed 128-row tile
+// of the other operand, so each tile is read once for 256 rows.  A producer thread loads tiles with TMA
+// (tensor maps over the [B][P][heads][128] prompt tensors, 128-byte swizzle, rows past the prompt
+// zero-filled) into a four-stage ring; one thread issues tcgen05.mma (M = N = 128, K = 16 per
+// instruction, bf16 in, fp32 out) into two TMEM accumulators per row tile (all 512 columns); sixteen
+// epilogue warps read TMEM with tcgen05.ld: eight per row tile, warp w taking the 32 lanes (rows)
+// 32 (w % 4) .. and the 64 columns 64 ((w / 4) % 2) .., so every thread reduces half a row without
+// shuffles and the two halves meet once at the end.  Every wait is bounded; the TMEM columns are
+// released on every path.
+constexpr int TC_ROWS = 128;                         // rows per row tile and per streamed tile
+constexpr int TC_RT = 2;                             // row tiles per CTA
+constexpr int TC_STAGES = 4;
+constexpr int TC_EPI = 8 * TC_RT;                    // epilogue warps
 constexpr int TC_THREADS = (TC_EPI + 2) * 32;        // + 1 TMA producer warp + 1 MMA issuer warp
 constexpr int TC_PRODUCER = TC_EPI, TC_ISSUER = TC_EPI + 1;
 constexpr int TC_TILE_BYTES = TC_ROWS * D * 2;       // 32 KB: two 128-byte-swizzled blocks of 64 dims
 constexpr int TC_KBLOCK = TC_TILE_BYTES / 2;
-constexpr int TC_TMEM_COLS = 2 * TC_ROWS;            // two fp32 accumulators of 128 columns
-constexpr int TC_OFF_RS = TC_TILE_BYTES * (1 + TC_STAGES);     // pass 2: row statistics of two tiles
-constexpr int TC_OFF_HALF = TC_OFF_RS + 2 * TC_ROWS * 4;       // the second column half's partials
-constexpr int TC_OFF_BAR = TC_OFF_HALF + 2 * TC_ROWS * 4;
-constexpr int TC_NBAR = 2 * TC_STAGES + 4 + 2;       // full, empty, tfull[2], tempty[2], afull, fin
+constexpr int TC_TMEM_COLS = TC_RT * 2 * TC_ROWS;    // two fp32 accumulators of 128 columns per row tile
+constexpr int TC_OFF_B = TC_RT * TC_TILE_BYTES;
+constexpr int TC_OFF_RS = TC_OFF_B + TC_STAGES * TC_TILE_BYTES;   // [RT][2][128] negated row statistics
+constexpr int TC_OFF_HALF = TC_OFF_RS + TC_RT * 2 * TC_ROWS * 4;  // [RT][2][128] second-half partials
+constexpr int TC_OFF_BAR = TC_OFF_HALF + TC_RT * 2 * TC_ROWS * 4;
+constexpr int TC_NBAR = 2 * TC_STAGES + 4 * TC_RT + 2;            // full, empty, tfull, tempty, afull, fin
 constexpr int TC_SMEM = 1024 + TC_OFF_BAR + TC_NBAR * 8 + 16;
+static_assert(TC_TMEM_COLS <= 512 && TC_SMEM <= 232448, "one CTA per SM");
 
 // tcgen05 shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart
 __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
@@ -74,6 +79,25 @@ __device__ __forceinline__ float ex2(float x) {   // 2^x on the special-function
   return y;
 }
 
+// Packed fp32 pairs (two lanes of work per instruction) and the three-input maximum.
+__device__ __forceinline__ void fma2(float &dx, float &dy, float ax, float ay, float bx, float by, float cx, float cy) {
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
+      " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+      : "=f"(dx), "=f"(dy)
+      : "f"(ax), "f"(ay), "f"(bx), "f"(by), "f"(cx), "f"(cy));
+}
+__device__ __forceinline__ void add2(float &ax, float &ay, float bx, float by) {
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%0, %1};\n mov.b64 rb, {%2, %3};\n add.rn.f32x2 rd, ra, rb;\n"
+      " mov.b64 {%0, %1}, rd;\n}"
+      : "+f"(ax), "+f"(ay)
+      : "f"(bx), "f"(by));
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // 32 consecutive fp32 columns of this thread's TMEM lane
 __device__ __forceinline__ void tmem_ld32(uint32_t addr, float (&v)[32]) {
   uint32_t r[32];
@@ -93,27 +117,35 @@ __device__ __forceinline__ void tmem_ld32(uint32_t addr, float (&v)[32]) {
 // COL = false, pass 1: rowstat[b][h][tau] = log2 sum_{i <= tau} 2^(q_tau . k_i * scale_log2).
 // COL = true,  pass 2: colsum[b][h][i] = sum_{tau >= i} 2^(q_tau . k_i * scale_log2 - rowstat[tau]).
 template <bool COL>
-__global__ void __launch_bounds__(TC_THREADS) tc_score_kernel(const __grid_constant__ CUtensorMap tq,
-                                                              const __grid_constant__ CUtensorMap tk,
-                                                              const CacheDev C, int *status, float scale_log2) {
+__global__ void __launch_bounds__(TC_THREADS, 1) tc_score_kernel(const __grid_constant__ CUtensorMap tq,
+                                                                 const __grid_constant__ CUtensorMap tk,
+                                                                 const CacheDev C, int *status, float scale_log2) {
   extern __shared__ uint8_t tc_smem_raw[];
   uint8_t *sm = tc_smem_raw + ((1024 - (smem_u32(tc_smem_raw) & 1023)) & 1023);   // swizzle atoms: 1024-aligned
-  uint8_t *sA = sm;
-  float *rsb = reinterpret_cast<float *>(sm + TC_OFF_RS);
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + TC_OFF_BAR);
-  uint64_t *full = bars, *empty = bars + TC_STAGES, *tfull = bars + 2 * TC_STAGES, *tempty = tfull + 2;
-  uint64_t *afull = tempty + 2, *fin = afull + 1;
+  uint64_t *full = bars, *empty = bars + TC_STAGES;
+  uint64_t *tfull = bars + 2 * TC_STAGES, *tempty = tfull + 2 * TC_RT;   // [RT][2] each
+  uint64_t *afull = tempty + 2 * TC_RT, *fin = afull + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + TC_NBAR);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int P = C.prompt_len, nrt = (P + TC_ROWS - 1) / TC_ROWS;
+  const int P = C.prompt_len, nrt = (P + TC_ROWS - 1) / TC_ROWS, npair = (nrt + TC_RT - 1) / TC_RT;
   const int h = blockIdx.y, b = blockIdx.z, g = h / C.G;
-  const int rt = COL ? (int)blockIdx.x : nrt - 1 - (int)blockIdx.x;   // pass 1: the longest rows first
-  const int r0 = rt * TC_ROWS;
-  const int t_begin = COL ? rt : 0, nb = COL ? nrt - rt : rt + 1;
+  const int pr = COL ? (int)blockIdx.x : npair - 1 - (int)blockIdx.x;   // pass 1: the longest rows first
+  // tile range [lo[r], hi[r]] of row tile rt = TC_RT pr + r (empty past the prompt)
+  int lo[TC_RT], hi[TC_RT];
+#pragma unroll
+  for (int r = 0; r < TC_RT; ++r) {
+    const int rt = TC_RT * pr + r;
+    lo[r] = COL ? rt : 0;
+    hi[r] = rt < nrt ? (COL ? nrt - 1 : rt) : -1;
+  }
+  const int t_lo = COL ? TC_RT * pr : 0, t_hi = COL ? nrt - 1 : min(TC_RT * pr + TC_RT - 1, nrt - 1);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < TC_NBAR; ++i)
-      mbar_init(&bars[i], (&bars[i] >= tempty && &bars[i] < tempty + 2) ? TC_EPI * 32 : 1);
+    for (int i = 0; i < TC_NBAR; ++i) {
+      const bool te = &bars[i] >= tempty && &bars[i] < tempty + 2 * TC_RT;
+      mbar_init(&bars[i], te ? 8 * 32 : 1);
+    }
     fence_mbar_init();
   }
   if (warp == TC_ISSUER) {
@@ -126,7 +158,7 @@ __global__ void __launch_bounds__(TC_THREADS) tc_score_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // A: pass 1 the 128 queries of head h, pass 2 the 128 keys of KV head g; B tiles the other operand
+  // A: pass 1 the queries of head h, pass 2 the keys of KV head g; the streamed tiles the other operand
   const CUtensorMap *mapA = COL ? &tk : &tq, *mapB = COL ? &tq : &tk;
   const int headA = COL ? g : h, headB = COL ? h : g;
 
@@ -134,17 +166,20 @@ __global__ void __launch_bounds__(TC_THREADS) tc_score_kernel(const __grid_const
     if (lane == 0) {   // ---- TMA producer
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(mapA)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(mapB)) : "memory");
-      mbar_arrive_expect_tx(afull, TC_TILE_BYTES);
-      tma_load_4d(sA, mapA, 0, headA, r0, b, afull);
-      tma_load_4d(sA + TC_KBLOCK, mapA, 64, headA, r0, b, afull);
+      mbar_arrive_expect_tx(afull, TC_RT * TC_TILE_BYTES);
+      for (int r = 0; r < TC_RT; ++r) {
+        uint8_t *dst = sm + r * TC_TILE_BYTES;
+        tma_load_4d(dst, mapA, 0, headA, (TC_RT * pr + r) * TC_ROWS, b, afull);
+        tma_load_4d(dst + TC_KBLOCK, mapA, 64, headA, (TC_RT * pr + r) * TC_ROWS, b, afull);
+      }
       int issued = 0;
-      for (int i = 0; i < nb; ++i) {
+      for (int i = 0; i <= t_hi - t_lo; ++i) {
         const int s = i % TC_STAGES;
         if (!mbar_wait(&empty[s], ((i / TC_STAGES) & 1) ^ 1, status)) break;
-        uint8_t *dst = sm + TC_TILE_BYTES * (1 + s);
+        uint8_t *dst = sm + TC_OFF_B + TC_TILE_BYTES * s;
         mbar_arrive_expect_tx(&full[s], TC_TILE_BYTES);
-        tma_load_4d(dst, mapB, 0, headB, (t_begin + i) * TC_ROWS, b, &full[s]);
-        tma_load_4d(dst + TC_KBLOCK, mapB, 64, headB, (t_begin + i) * TC_ROWS, b, &full[s]);
+        tma_load_4d(dst, mapB, 0, headB, (t_lo + i) * TC_ROWS, b, &full[s]);
+        tma_load_4d(dst + TC_KBLOCK, mapB, 64, headB, (t_lo + i) * TC_ROWS, b, &full[s]);
         issued = i + 1;
       }
       // copies still in flight land before the CTA leaves (normally all were consumed already)
@@ -155,72 +190,94 @@ __global__ void __launch_bounds__(TC_THREADS) tc_score_kernel(const __grid_const
   } else if (warp == TC_ISSUER) {
     if (lane == 0) {   // ---- MMA issuer
       bool ok = mbar_wait(afull, 0, status);
-      const uint32_t a0 = smem_u32(sA);
-      for (int i = 0; ok && i < nb; ++i) {
-        const int s = i % TC_STAGES, buf = i & 1;
-        if (!mbar_wait(&full[s], (i / TC_STAGES) & 1, status)) break;
-        if (!mbar_wait(&tempty[buf], ((i >> 1) & 1) ^ 1, status)) break;
-        tc_fence_after();
-        const uint32_t b0 = smem_u32(sm + TC_TILE_BYTES * (1 + s));
+      int cnt[TC_RT];
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * TC_KBLOCK + (kk & 3) * 32;   // 16 dims = 32 B inside a 128-B row
-          tc_mma(tmem + buf * TC_ROWS, umma_desc(a0 + off), umma_desc(b0 + off), kk > 0 ? 1u : 0u);
+      for (int r = 0; r < TC_RT; ++r) cnt[r] = 0;
+      for (int i = 0; ok && i <= t_hi - t_lo; ++i) {
+        const int s = i % TC_STAGES, t = t_lo + i;
+        if (!mbar_wait(&full[s], (i / TC_STAGES) & 1, status)) break;
+        const uint32_t b0 = smem_u32(sm + TC_OFF_B + TC_TILE_BYTES * s);
+#pragma unroll
+        for (int r = 0; r < TC_RT; ++r) {
+          if (t < lo[r] || t > hi[r]) continue;
+          const int buf = cnt[r] & 1;
+          if (!mbar_wait(&tempty[2 * r + buf], ((cnt[r] >> 1) & 1) ^ 1, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sm + r * TC_TILE_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * TC_KBLOCK + (kk & 3) * 32;   // 16 dims = 32 B inside a 128-B row
+            tc_mma(tmem + (2 * r + buf) * TC_ROWS, umma_desc(a0 + off), umma_desc(b0 + off), kk > 0 ? 1u : 0u);
+          }
+          tc_commit(&tfull[2 * r + buf]);
+          ++cnt[r];
         }
         tc_commit(&empty[s]);
-        tc_commit(&tfull[buf]);
       }
       tc_commit(fin);   // every MMA issued above has completed once this arrives
       mbar_wait(fin, 0, status);
     }
   } else {
-    // ---- epilogue: thread = TMEM lane = row r0 + row, columns half * 64 .. + 63 of every tile
-    const int row = 32 * (warp & 3) + lane, half = warp >> 2, cbeg = 64 * half;
-    const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + cbeg;
-    float *hp = reinterpret_cast<float *>(sm + TC_OFF_HALF);
+    // ---- epilogue: group r = warp / 8; thread = TMEM lane = row of row tile rt, columns half * 64 .. + 63
+    const int r = warp >> 3, wq = warp & 3, half = (warp >> 2) & 1, cbeg = 64 * half;
+    const int rt = TC_RT * pr + r, r0 = rt * TC_ROWS, row = 32 * wq + lane;
+    const int nt = hi[r] - lo[r] + 1;   // tiles of this row tile (0 past the prompt)
+    const uint32_t lane_addr = tmem + ((uint32_t)(32 * wq) << 16) + 2 * r * TC_ROWS + cbeg;
+    float *hp = reinterpret_cast<float *>(sm + TC_OFF_HALF) + r * 2 * TC_ROWS;
+    float *rsb = reinterpret_cast<float *>(sm + TC_OFF_RS) + r * 2 * TC_ROWS;
+    const int barid = 1 + r;
     bool ok = true;
     if (!COL) {
       const int qrow = r0 + row;
       float m = -INFINITY, l = 0.f;
-      for (int i = 0; i < nb; ++i) {
-        const int buf = i & 1;
-        if (ok) ok = mbar_wait(&tfull[buf], (i >> 1) & 1, status);
+      for (int i = 0; i < nt; ++i) {
+        const int buf = i & 1, t = lo[r] + i;
+        if (ok) ok = mbar_wait(&tfull[2 * r + buf], (i >> 1) & 1, status);
         tc_fence_after();
-        const bool diag = i == rt;   // key tile i meets the query tile on the diagonal
+        const bool diag = t == rt;   // key tile t meets the query tile on the diagonal
 #pragma unroll 1
         for (int c0 = 0; c0 < 64; c0 += 32) {
           float v[32];
           tmem_ld32(lane_addr + buf * TC_ROWS + c0, v);
-          float mx = -INFINITY;
           if (diag) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < 32; ++j)
               if (cbeg + c0 + j > row) v[j] = -INFINITY;   // causal: keys after the query
-              mx = fmaxf(mx, v[j]);
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) mx = fmaxf(mx, v[j]);
           }
-          const float mn = fmaxf(m, mx * scale_log2);
-          if (mn != -INFINITY) {   // the chunk holds a key at or before the query
-            float acc = l * ex2(m - mn);
+          float mx0 = v[0], mx1 = v[1];   // two chains of three-input maxima
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc += ex2(fmaf(v[j], scale_log2, -mn));
-            l = acc;
+          for (int j = 2; j < 32; j += 4) {
+            mx0 = max3(mx0, v[j], v[j + 1]);
+            mx1 = max3(mx1, v[j + 2], v[j + 3]);
+          }
+          const float mn = fmaxf(m, fmaxf(mx0, mx1) * scale_log2);
+          if (mn != -INFINITY) {   // the chunk holds a key at or before the query
+            float a0 = l * ex2(m - mn), a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {   // 2^(s scale - mn) two at a time, four accumulators
+              float x0, x1, x2, x3;
+              fma2(x0, x1, v[j], v[j + 1], scale_log2, scale_log2, -mn, -mn);
+              fma2(x2, x3, v[j + 2], v[j + 3], scale_log2, scale_log2, -mn, -mn);
+              add2(a0, a1, ex2(x0), ex2(x1));
+              add2(a2, a3, ex2(x2), ex2(x3));
+            }
+            l = (a0 + a1) + (a2 + a3);
             m = mn;
           }
         }
         tc_fence_before();
-        mbar_arrive(&tempty[buf]);
+        mbar_arrive(&tempty[2 * r + buf]);
       }
       // the two column halves of a row meet: (m, l) pairs merge by log-sum-exp
       if (half) {
         hp[row] = m;
         hp[TC_ROWS + row] = l;
       }
-      asm volatile("bar.sync 1, %0;" ::"r"(TC_EPI * 32) : "memory");
-      if (!half) {
+      asm volatile("bar.sync %0, %1;" ::"r"(barid), "r"(8 * 32) : "memory");
+      if (!half && nt > 0) {
         const float m2 = hp[row], l2 = hp[TC_ROWS + row], mm = fmaxf(m, m2);
         const float ls = (m == -INFINITY ? 0.f : l * exp2f(m - mm)) + (m2 == -INFINITY ? 0.f : l2 * exp2f(m2 - mm));
         if (qrow < P) reinterpret_cast<float *>(C.arena + C.off_rowstat)[((size_t)b * C.h_q + h) * P + qrow] = mm + __log2f(ls);
@@ -229,15 +286,15 @@ __global__ void __launch_bounds__(TC_THREADS) tc_score_kernel(const __grid_const
       const int key = r0 + row;
       const float *rowstat = reinterpret_cast<const float *>(C.arena + C.off_rowstat) + ((size_t)b * C.h_q + h) * P;
       float col = 0.f;
-      int tau = t_begin * TC_ROWS + row;
-      float nxt = (!half && tau < P) ? rowstat[tau] : 0.f;   // the row statistic of query tau, one tile ahead
-      for (int i = 0; i < nb; ++i) {
-        const int t = t_begin + i, buf = i & 1;
-        if (!half) rsb[buf * TC_ROWS + row] = nxt;
+      int tau = lo[r] * TC_ROWS + row;
+      float nxt = (!half && nt > 0 && tau < P) ? rowstat[tau] : 0.f;   // the statistic of query tau, a tile ahead
+      for (int i = 0; i < nt; ++i) {
+        const int t = lo[r] + i, buf = i & 1;
+        if (!half) rsb[buf * TC_ROWS + row] = -nxt;   // negated: the FMA adds it
         tau += TC_ROWS;
-        if (!half && i + 1 < nb) nxt = tau < P ? rowstat[tau] : 0.f;
-        asm volatile("bar.sync 1, %0;" ::"r"(TC_EPI * 32) : "memory");   // the tile's row statistics
-        if (ok) ok = mbar_wait(&tfull[buf], (i >> 1) & 1, status);
+        if (!half && i + 1 < nt) nxt = tau < P ? rowstat[tau] : 0.f;
+        asm volatile("bar.sync %0, %1;" ::"r"(barid), "r"(8 * 32) : "memory");   // the tile's row statistics
+        if (ok) ok = mbar_wait(&tfull[2 * r + buf], (i >> 1) & 1, status);
         tc_fence_after();
         const bool diag = t == rt, tail = (t + 1) * TC_ROWS > P;
         const float *rs = rsb + buf * TC_ROWS + cbeg;
@@ -246,23 +303,32 @@ __global__ void __launch_bounds__(TC_THREADS) tc_score_kernel(const __grid_const
           float v[32];
           tmem_ld32(lane_addr + buf * TC_ROWS + c0, v);
           if (!diag && !tail) {
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) col += ex2(fmaf(v[j], scale_log2, -rs[c0 + j]));
+            for (int j = 0; j < 32; j += 4) {
+              const float4 q4 = *reinterpret_cast<const float4 *>(rs + c0 + j);
+              float x0, x1, x2, x3;
+              fma2(x0, x1, v[j], v[j + 1], scale_log2, scale_log2, q4.x, q4.y);
+              fma2(x2, x3, v[j + 2], v[j + 3], scale_log2, scale_log2, q4.z, q4.w);
+              add2(a0, a1, ex2(x0), ex2(x1));
+              add2(a2, a3, ex2(x2), ex2(x3));
+            }
+            col += (a0 + a1) + (a2 + a3);
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const int c = cbeg + c0 + j;
               const bool valid = (!diag || c >= row) && t * TC_ROWS + c < P;   // causal, inside the prompt
-              col += valid ? ex2(fmaf(v[j], scale_log2, -rs[c0 + j])) : 0.f;
+              col += valid ? ex2(fmaf(v[j], scale_log2, rs[c0 + j])) : 0.f;
             }
           }
         }
         tc_fence_before();
-        mbar_arrive(&tempty[buf]);
+        mbar_arrive(&tempty[2 * r + buf]);
       }
       if (half) hp[row] = col;
-      asm volatile("bar.sync 1, %0;" ::"r"(TC_EPI * 32) : "memory");
-      if (!half && key < P)
+      asm volatile("bar.sync %0, %1;" ::"r"(barid), "r"(8 * 32) : "memory");
+      if (!half && nt > 0 && key < P)
         reinterpret_cast<float *>(C.arena + C.off_colsum)[((size_t)b * C.h_q + h) * P + key] = col + hp[row];
     }
   }
@@ -335,7 +401,8 @@ cudaError_t launch_prefill_scores(const CacheDev &C, const __nv_bfloat16 *q, con
     attr_set[dev] = true;
   }
   int *status = C.status();
-  dim3 grid((P + TC_ROWS - 1) / TC_ROWS, C.h_q, C.B);
+  const int nrt = (P + TC_ROWS - 1) / TC_ROWS;
+  dim3 grid((nrt + TC_RT - 1) / TC_RT, C.h_q, C.B);
   tc_score_kernel<false><<<grid, TC_THREADS, TC_SMEM, stream>>>(tq, tk, C, status, scale_log2);
   tc_score_kernel<true><<<grid, TC_THREADS, TC_SMEM, stream>>>(tq, tk, C, status, scale_log2);
   const int npw = (P - C.n_sink + C.W - 1) / C.W;
