@@ -98,20 +98,26 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return d;
 }
 
-// 32 consecutive fp32 columns of this thread's TMEM lane
-__device__ __forceinline__ void tmem_ld32(uint32_t addr, float (&v)[32]) {
-  uint32_t r[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(addr));
+// 64 consecutive fp32 columns of this thread's TMEM lane: two 32-column loads, one wait
+__device__ __forceinline__ void tmem_ld64(uint32_t addr, float (&v)[64]) {
+  uint32_t r[64];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[32 * h + 0]), "=r"(r[32 * h + 1]), "=r"(r[32 * h + 2]), "=r"(r[32 * h + 3]), "=r"(r[32 * h + 4]),
+          "=r"(r[32 * h + 5]), "=r"(r[32 * h + 6]), "=r"(r[32 * h + 7]), "=r"(r[32 * h + 8]), "=r"(r[32 * h + 9]),
+          "=r"(r[32 * h + 10]), "=r"(r[32 * h + 11]), "=r"(r[32 * h + 12]), "=r"(r[32 * h + 13]),
+          "=r"(r[32 * h + 14]), "=r"(r[32 * h + 15]), "=r"(r[32 * h + 16]), "=r"(r[32 * h + 17]),
+          "=r"(r[32 * h + 18]), "=r"(r[32 * h + 19]), "=r"(r[32 * h + 20]), "=r"(r[32 * h + 21]),
+          "=r"(r[32 * h + 22]), "=r"(r[32 * h + 23]), "=r"(r[32 * h + 24]), "=r"(r[32 * h + 25]),
+          "=r"(r[32 * h + 26]), "=r"(r[32 * h + 27]), "=r"(r[32 * h + 28]), "=r"(r[32 * h + 29]),
+          "=r"(r[32 * h + 30]), "=r"(r[32 * h + 31])
+        : "r"(addr + 32 * h));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+  for (int j = 0; j < 64; ++j) v[j] = __uint_as_float(r[j]);
 }
 
 // COL = false, pass 1: rowstat[b][h][tau] = log2 sum_{i <= tau} 2^(q_tau . k_i * scale_log2).
@@ -238,35 +244,33 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_score_kernel(const __grid_co
         if (ok) ok = mbar_wait(&tfull[2 * r + buf], (i >> 1) & 1, status);
         tc_fence_after();
         const bool diag = t == rt;   // key tile t meets the query tile on the diagonal
-#pragma unroll 1
-        for (int c0 = 0; c0 < 64; c0 += 32) {
-          float v[32];
-          tmem_ld32(lane_addr + buf * TC_ROWS + c0, v);
-          if (diag) {
+        float v[64];
+        tmem_ld64(lane_addr + buf * TC_ROWS, v);
+        if (diag) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (cbeg + c0 + j > row) v[j] = -INFINITY;   // causal: keys after the query
-          }
-          float mx0 = v[0], mx1 = v[1];   // two chains of three-input maxima
+          for (int j = 0; j < 64; ++j)
+            if (cbeg + j > row) v[j] = -INFINITY;   // causal: keys after the query
+        }
+        float mx0 = v[0], mx1 = v[1];   // two chains of three-input maxima
 #pragma unroll
-          for (int j = 2; j < 32; j += 4) {
-            mx0 = max3(mx0, v[j], v[j + 1]);
-            mx1 = max3(mx1, v[j + 2], v[j + 3]);
-          }
-          const float mn = fmaxf(m, fmaxf(mx0, mx1) * scale_log2);
-          if (mn != -INFINITY) {   // the chunk holds a key at or before the query
-            float a0 = l * ex2(m - mn), a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        for (int j = 2; j < 62; j += 4) {
+          mx0 = max3(mx0, v[j], v[j + 1]);
+          mx1 = max3(mx1, v[j + 2], v[j + 3]);
+        }
+        mx0 = max3(mx0, v[62], v[63]);
+        const float mn = fmaxf(m, fmaxf(mx0, mx1) * scale_log2);
+        if (mn != -INFINITY) {   // the tile holds a key at or before the query
+          float a0 = l * ex2(m - mn), a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {   // 2^(s scale - mn) two at a time, four accumulators
-              float x0, x1, x2, x3;
-              fma2(x0, x1, v[j], v[j + 1], scale_log2, scale_log2, -mn, -mn);
-              fma2(x2, x3, v[j + 2], v[j + 3], scale_log2, scale_log2, -mn, -mn);
-              add2(a0, a1, ex2(x0), ex2(x1));
-              add2(a2, a3, ex2(x2), ex2(x3));
-            }
-            l = (a0 + a1) + (a2 + a3);
-            m = mn;
+          for (int j = 0; j < 64; j += 4) {   // 2^(s scale - mn) two at a time, four accumulators
+            float x0, x1, x2, x3;
+            fma2(x0, x1, v[j], v[j + 1], scale_log2, scale_log2, -mn, -mn);
+            fma2(x2, x3, v[j + 2], v[j + 3], scale_log2, scale_log2, -mn, -mn);
+            add2(a0, a1, ex2(x0), ex2(x1));
+            add2(a2, a3, ex2(x2), ex2(x3));
           }
+          l = (a0 + a1) + (a2 + a3);
+          m = mn;
         }
         tc_fence_before();
         mbar_arrive(&tempty[2 * r + buf]);
@@ -298,29 +302,26 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_score_kernel(const __grid_co
         tc_fence_after();
         const bool diag = t == rt, tail = (t + 1) * TC_ROWS > P;
         const float *rs = rsb + buf * TC_ROWS + cbeg;
-#pragma unroll 1
-        for (int c0 = 0; c0 < 64; c0 += 32) {
-          float v[32];
-          tmem_ld32(lane_addr + buf * TC_ROWS + c0, v);
-          if (!diag && !tail) {
-            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        float v[64];
+        tmem_ld64(lane_addr + buf * TC_ROWS, v);
+        if (!diag && !tail) {
+          float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-              const float4 q4 = *reinterpret_cast<const float4 *>(rs + c0 + j);
-              float x0, x1, x2, x3;
-              fma2(x0, x1, v[j], v[j + 1], scale_log2, scale_log2, q4.x, q4.y);
-              fma2(x2, x3, v[j + 2], v[j + 3], scale_log2, scale_log2, q4.z, q4.w);
-              add2(a0, a1, ex2(x0), ex2(x1));
-              add2(a2, a3, ex2(x2), ex2(x3));
-            }
-            col += (a0 + a1) + (a2 + a3);
-          } else {
+          for (int j = 0; j < 64; j += 4) {
+            const float4 q4 = *reinterpret_cast<const float4 *>(rs + j);
+            float x0, x1, x2, x3;
+            fma2(x0, x1, v[j], v[j + 1], scale_log2, scale_log2, q4.x, q4.y);
+            fma2(x2, x3, v[j + 2], v[j + 3], scale_log2, scale_log2, q4.z, q4.w);
+            add2(a0, a1, ex2(x0), ex2(x1));
+            add2(a2, a3, ex2(x2), ex2(x3));
+          }
+          col += (a0 + a1) + (a2 + a3);
+        } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int c = cbeg + c0 + j;
-              const bool valid = (!diag || c >= row) && t * TC_ROWS + c < P;   // causal, inside the prompt
-              col += valid ? ex2(fmaf(v[j], scale_log2, rs[c0 + j])) : 0.f;
-            }
+          for (int j = 0; j < 64; ++j) {
+            const int c = cbeg + j;
+            const bool valid = (!diag || c >= row) && t * TC_ROWS + c < P;   // causal, inside the prompt
+            col += valid ? ex2(fmaf(v[j], scale_log2, rs[j])) : 0.f;
           }
         }
         tc_fence_before();
