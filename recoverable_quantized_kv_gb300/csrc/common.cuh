@@ -158,27 +158,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *s
   }
 }
 
-__device__ __forceinline__ int ld_volatile_shared(const int *p) {
-  int v;
-  asm volatile("ld.volatile.shared.s32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_volatile_shared(int *p, int v) {
-  asm volatile("st.volatile.shared.s32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
-}
-// Bounded wait until a shared counter written by another warp of the CTA exceeds `c`.
-__device__ __forceinline__ bool wait_shared_gt(const int *p, int c, int *status) {
-  if (ld_volatile_shared(p) > c) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 0;; ++it) {
-    if (ld_volatile_shared(p) > c) return true;
-    if ((it & 255u) == 255u && globaltimer_ns() - t0 > 200000000ull) {
-      atomicOr(status, QV_ERR_TIMEOUT);
-      return false;
-    }
-  }
-}
-
 // 1-D bulk copy global -> shared (TMA), completion counted on `bar` in bytes.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
@@ -194,11 +173,6 @@ __device__ __forceinline__ uint4 lds128(const void *p) {
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "r"(smem_u32(p)));
-  return v;
-}
-__device__ __forceinline__ uint32_t lds32(const void *p) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)));
   return v;
 }
 
@@ -228,7 +202,6 @@ __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v 
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
 // Exact float of a small non-negative integer code (c < 2^23) without the conversion pipe.
-__device__ __forceinline__ float code_f(uint32_t c) { return __uint_as_float(0x4B000000u | c) - 8388608.0f; }
 
 __device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
 

@@ -61,29 +61,6 @@ struct DecGeo {
   static_assert(MRG_OFF % 16 == 0 && DEC_CO_OFF % 16 == 0, "16-byte aligned per-warp tables");
 };
 
-// Work list of one (sequence, KV head): item 0 = the sink tokens, items 1..nL = recent windows
-// j0 .. j0+nL-1, then the F-table entries, then the Q-table entries.  Item costs are the bytes
-// streamed, and split / warp ranges are byte-balanced prefixes of this list.
-struct Items {
-  int nL, nF, nQ, j0;
-  long long cs, cw, cq;
-  __device__ int total() const { return 1 + nL + nF + nQ; }
-  __device__ long long total_cost() const { return cs + (long long)(nL + nF) * cw + (long long)nQ * cq; }
-  __device__ int first_at(long long target) const {   // first item whose start cost >= target
-    if (target <= 0) return 0;
-    if (target <= cs) return 1;
-    long long r = target - cs;
-    const long long nb = nL + nF;
-    if (r <= nb * cw) return 1 + (int)((r + cw - 1) / cw);
-    r -= nb * cw;
-    const int i = 1 + nL + nF + (int)((r + cq - 1) / cq);
-    return i < total() ? i : total();
-  }
-  __device__ int bound(int part, int nparts) const {
-    return part >= nparts ? total() : first_at(total_cost() * part / nparts);
-  }
-};
-
 __device__ __forceinline__ uint32_t ldg32(const void *p) { return __ldg(reinterpret_cast<const uint32_t *>(p)); }
 __device__ __forceinline__ uint32_t ldg16(const void *p) { return __ldg(reinterpret_cast<const unsigned short *>(p)); }
 
@@ -155,14 +132,6 @@ __device__ __forceinline__ void p_to_b(const float (&p)[NMT][4], uint32_t (&pb)[
 
 __device__ __forceinline__ float h2f_lo(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFF))); }
 __device__ __forceinline__ float h2f_hi(uint32_t v) { return __half2float(__ushort_as_half((unsigned short)(v >> 16))); }
-
-// x_hat = bf16(fp32(code * s + m)) for the two halves of an INT2 field element pair.
-__device__ __forceinline__ uint32_t dq_pair(uint32_t field, int sh_lo, int sh_hi, float s_lo, float m_lo, float s_hi,
-                                            float m_hi) {
-  const float lo = __fmaf_rn(code_f((field >> sh_lo) & 3u), s_lo, m_lo);
-  const float hi = __fmaf_rn(code_f((field >> sh_hi) & 3u), s_hi, m_hi);
-  return pack_bf16(lo, hi);
-}
 
 __device__ __forceinline__ uint32_t word_of(const uint4 &v, int k) {
   return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
