@@ -94,10 +94,11 @@ def _compare(got, want):
     assert np.allclose(got["tier_mass"], want["tier_mass"], rtol=1e-6, atol=1e-9)
 
 
-@pytest.mark.parametrize("variant", [dict(), dict(no_promotion=1), dict(batch=2, h_q=8, h_kv=2)])
+@pytest.mark.parametrize("variant", [dict(), dict(no_promotion=1), dict(batch=2, h_q=8, h_kv=2),
+                                     dict(window=64, bits=4, prompt_len=3000), dict(rope_base=10000.0)])
 def test_diagnostics_match_the_oracle(lib, variant):
-    wl = synth.workload("tiny_4k", prompt_len=1500, steps=64, n_plant=4, kappa=6.0, budget_num=35, q_num=40,
-                        **variant)
+    wl = synth.workload("tiny_4k", prompt_len=1500, steps=64, n_plant=4, kappa=6.0, budget_num=35, q_num=40)
+    wl = wl.replace(**variant)
     got, want = _run(wl, 64, churn=5)
     _compare(got, want)
     assert got["fmm_terms"] > 0 and got["lir_eligible"] > 0
