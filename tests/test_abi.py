@@ -77,3 +77,14 @@ def test_documented_layouts_are_bijections():
             key = byte * 8 + shift
             assert len(np.unique(key)) == W * 128 and byte.max() < W * 128 * bits // 8
             assert np.all(shift % bits == 0)
+
+
+def test_router_capacity(cpu_lib):
+    """A unit holds at most 8192 windows (the router sorts them in one CTA): max_len one token past that
+    capacity is rejected, at it accepted."""
+    wl = synth.workload("tiny_4k")
+    cap = wl.n_sink + 8192 * wl.window
+    assert binding.budget(binding.make_config(wl, max_len=cap)).n_windows == 8192
+    with pytest.raises(binding.QEvictError) as e:
+        binding.budget(binding.make_config(wl, max_len=cap + 1))
+    assert e.value.status == binding.EINVAL

@@ -111,6 +111,20 @@ def test_rope_table_rules(lib):
     c.check()
 
 
+def test_minimal_prompt_until_the_cache_is_full(lib):
+    """A prompt of n_sink + 1 tokens (no historical window at prefill) decoded until T = max_len: every
+    window the cache ever routes ages out of the recent region during decode, and one more step is
+    refused."""
+    wl = synth.workload("tiny_4k", prompt_len=5, steps=240, n_plant=0, budget_num=4000)
+    ls = _run(wl, 240)
+    assert ls.bud.k_q > 0 and ls.cache.counters()["aged_quant"] > 0
+    q = torch.zeros(1, wl.h_q, 128, dtype=torch.bfloat16, device="cuda")
+    kv = torch.zeros(1, wl.h_kv, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(binding.QEvictError) as e:
+        ls.cache.decode_step(0, q, kv, kv, torch.empty_like(q))
+    assert e.value.status == binding.ESCHEDULE
+
+
 def test_two_tier_and_quantized_only(lib):
     """q = 0: Full/Evicted only (two-tier window eviction); q = 1: K_f = 0 (quantised retention)."""
     base = synth.workload("tiny_4k", prompt_len=1200, steps=16, n_plant=4)
