@@ -47,6 +47,7 @@ def parse_args():
     ap.add_argument("--cpu-sample-steps", type=int, default=8)
     ap.add_argument("--diag", type=int, default=0,
                     help="also run N routing events with the routing diagnostics against a FullKV cache")
+    ap.add_argument("--int4", action="store_true", help="the INT4 / 64-token-window format of the workload")
     ap.add_argument("--rope-base", type=float, default=0.0,
                     help="keys carry RoPE with this base and Quantized keys are kept before it (GPU arm only)")
     ap.add_argument("--layers", type=int, default=None,
@@ -276,6 +277,8 @@ def run_gpu(args, rank, world):
     wl = synth.workload(args.workload) if args.layers is None else synth.workload(args.workload, n_layers=args.layers)
     if args.rope_base > 0:
         wl = wl.replace(rope_base=args.rope_base)
+    if args.int4:
+        wl = wl.replace(window=64, bits=4)
     K, Wm = args.steps, args.warmup
     Om = wl.omega
     K_kern = 2 * Om

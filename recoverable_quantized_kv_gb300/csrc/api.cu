@@ -142,10 +142,11 @@ void make_plan(const qevict_config *c, const qevict_budget_info *b, Plan *p) {
   qv::CacheDev &C = p->dev;
   region(16LL * N, C.off_qtask, C.st_qtask);
   region(16LL * N, C.off_mtask, C.st_mtask);
-  // decode split-K partitions: about one CTA per SM for the whole batch
+  // decode split-K partitions: at most one CTA per SM for the whole batch (a decode CTA fills an SM, so a
+  // grid above the SM count would run a second, nearly empty wave)
   const int sms = device_sm_count();
   const int max_items = 1 + (R + 1) + kf_cap + kq_cap;
-  int n_split = (sms + c->batch * c->h_kv - 1) / (c->batch * c->h_kv);
+  int n_split = sms / (c->batch * c->h_kv);
   n_split = std::max(1, std::min(n_split, std::max(1, max_items / 4)));
   auto global = [&](int64_t bytes) {
     const int64_t o = off;
