@@ -195,7 +195,8 @@ __device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v <<
 __device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 __device__ __forceinline__ float bf_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
 
-// cos/sin of the in-window offset tt for channels 16jj + 2tl + 8hh and + 1, from the offset table:
+// cos/sin of the in-window offset tt for channels 16jj + 2tl + 8hh and + 1, as (cos, cos, sin, sin) of the
+// two channels, from the offset table:
 // 16 B per (offset, k-step jj, channel half, lane class), the two halves swapped on odd offsets so
 // that the lanes of neighbouring token rows read different banks
 __device__ __forceinline__ float4 rel_cs(const uint8_t *rel, int tt, int jj, int hh, int tl) {
@@ -204,16 +205,30 @@ __device__ __forceinline__ float4 rel_cs(const uint8_t *rel, int tt, int jj, int
 
 // RoPE of one token's channel pairs (i, i + 64) and (i + 1, i + 65) (QEvict §4.3: RoPE re-applied
 // after dequantisation): a0, a1 are the pre-RoPE values of channels i, i + 1 and b0, b1 of i + 64,
-// i + 65.  The angle of position p0 + tt comes by angle addition from the window's row cb (cos, sin of
-// p0 for i and i + 1) and the offset's row rt; the rotation x_i c - x_{i+64} s, x_{i+64} c + x_i s
-// rounds every product and sum on its own.  ka, kb: the bf16 pairs (i, i + 1) and (i + 64, i + 65).
-__device__ __forceinline__ void rope_rot(float a0, float a1, float b0, float b1, const float4 &cb, const float4 &rt,
-                                         uint32_t &ka, uint32_t &kb) {
-  const float c0 = __fmaf_rn(cb.x, rt.x, -__fmul_rn(cb.y, rt.y)), s0 = __fmaf_rn(cb.y, rt.x, __fmul_rn(cb.x, rt.y));
-  const float c1 = __fmaf_rn(cb.z, rt.z, -__fmul_rn(cb.w, rt.w)), s1 = __fmaf_rn(cb.w, rt.z, __fmul_rn(cb.z, rt.w));
-  ka = pack_bf16(__fsub_rn(__fmul_rn(a0, c0), __fmul_rn(b0, s0)), __fsub_rn(__fmul_rn(a1, c1), __fmul_rn(b1, s1)));
-  kb = pack_bf16(__fadd_rn(__fmul_rn(b0, c0), __fmul_rn(a0, s0)), __fadd_rn(__fmul_rn(b1, c1), __fmul_rn(a1, s1)));
+// i + 65.  The angle of position p0 + tt comes by angle addition from the window's row cb and the
+// offset's row rt, both (cos, cos, sin, sin) of the two channels (ncb: the window row's sines negated);
+// the rotation x_i c - x_{i+64} s, x_{i+64} c + x_i s rounds every product and sum on its own, two
+// channels per packed instruction.  ka, kb: the bf16 pairs (i, i + 1) and (i + 64, i + 65).
+__device__ __forceinline__ void rope_rot(float a0, float a1, float b0, float b1, const float4 &cb, const float2 &ncb,
+                                         const float4 &rt, uint32_t &ka, uint32_t &kb) {
+  float c0, c1, s0, s1, u0, u1, w0, w1;
+  mul2(u0, u1, ncb.x, ncb.y, rt.z, rt.w);          // -sin(p0) sin(t)
+  fma2(c0, c1, cb.x, cb.y, rt.x, rt.y, u0, u1);     // cos(p0 + t)
+  mul2(w0, w1, cb.x, cb.y, rt.z, rt.w);            // cos(p0) sin(t)
+  fma2(s0, s1, cb.z, cb.w, rt.x, rt.y, w0, w1);     // sin(p0 + t)
+  float p0, p1, q0, q1;
+  mul2(p0, p1, a0, a1, c0, c1);
+  mul2(q0, q1, b0, b1, s0, s1);
+  sub2(p0, p1, p0, p1, q0, q1);                    // x_i c - x_{i+64} s
+  mul2(u0, u1, b0, b1, c0, c1);
+  mul2(w0, w1, a0, a1, s0, s1);
+  add2(u0, u1, w0, w1);                            // x_{i+64} c + x_i s
+  ka = pack_bf16(p0, p1);
+  kb = pack_bf16(u0, u1);
 }
+
+// a window's RoPE row (cos, sin, cos, sin of channels 2l, 2l + 1) reordered to (cos, cos, sin, sin)
+__device__ __forceinline__ float4 cc_ss(const float4 &v) { return make_float4(v.x, v.z, v.y, v.w); }
 
 template <int W, int BITS, bool ROPE>
 __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDev C, const DecodeIO io) {
@@ -415,7 +430,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
     for (int k = threadIdx.x; k < DEC_REL_BYTES / 16; k += DEC_CONSUMERS * 32) {
       const int t = k >> 5, jj = (k >> 3) & 3, t4 = k & 3, hh = ((k >> 2) & 1) ^ (t & 1);
       *reinterpret_cast<float4 *>(rel + 16 * k) =
-          __ldg(reinterpret_cast<const float4 *>(tab + ((size_t)t * 64 + 16 * jj + 2 * t4 + 8 * hh) * 2));
+          cc_ss(__ldg(reinterpret_cast<const float4 *>(tab + ((size_t)t * 64 + 16 * jj + 2 * t4 + 8 * hh) * 2)));
     }
     asm volatile("bar.sync 1, %0;" ::"r"(DEC_CONSUMERS * 32) : "memory");   // consumer warps only
   }
@@ -593,7 +608,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
           tw[base + 2] = __byte_perm(p01, p23, 0x7531);
         }
       }
-      if constexpr (ROPE) *reinterpret_cast<float4 *>(tbl + DEC_TBL_BYTES + 16 * lane) = csr;
+      if constexpr (ROPE) *reinterpret_cast<float4 *>(tbl + DEC_TBL_BYTES + 16 * lane) = cc_ss(csr);
       __syncwarp();
       const uint4 kcw0 = lds128(ch + lane * 16), kcw1 = lds128(ch + 512 + lane * 16);
       if constexpr (ROPE) {
@@ -604,6 +619,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
           const uint4 TA1 = lds128(tbl + ((jj + 4) * 4 + tl) * 32), TB1 = lds128(tbl + ((jj + 4) * 4 + tl) * 32 + 16);
           const uint8_t *csw = tbl + DEC_TBL_BYTES + (16 * jj + 2 * tl) * 8;
           const float4 cb0 = *reinterpret_cast<const float4 *>(csw), cb1 = *reinterpret_cast<const float4 *>(csw + 64);
+          const float2 ncb0 = make_float2(-cb0.z, -cb0.w), ncb1 = make_float2(-cb1.z, -cb1.w);
 #pragma unroll
           for (int mt = 0; mt < NMT; ++mt) {
             // k-step j sits in code word j / 2, low half for even j
@@ -616,7 +632,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
               const int tt = 16 * mt + gl + 8 * (r & 1);
-              rope_rot(bf_lo(ka[r]), bf_hi(ka[r]), bf_lo(kb[r]), bf_hi(kb[r]), (r >> 1) ? cb1 : cb0,
+              rope_rot(bf_lo(ka[r]), bf_hi(ka[r]), bf_lo(kb[r]), bf_hi(kb[r]), (r >> 1) ? cb1 : cb0, (r >> 1) ? ncb1 : ncb0,
                        rel_cs(rel, tt, jj, r >> 1, tl), ka[r], kb[r]);
             }
             mma_bf16(s[mt], ka[0], ka[1], ka[2], ka[3], qb[jj][0], qb[jj][1]);
@@ -717,7 +733,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
       if constexpr (ROPE) {
 #pragma unroll
         for (int hv = 0; hv < HALVES; ++hv)
-          *reinterpret_cast<float4 *>(tbl + DEC_TBL_BYTES + hv * 512 + 16 * lane) = csr[hv];
+          *reinterpret_cast<float4 *>(tbl + DEC_TBL_BYTES + hv * 512 + 16 * lane) = cc_ss(csr[hv]);
       }
       __syncwarp();
       const __half *vsp = reinterpret_cast<const __half *>(pch + (Gm::OFF_VS - 2 * Gm::CODE_BYTES));
@@ -748,6 +764,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
               const float4 mb = *reinterpret_cast<const float4 *>(tbl + ((jj + 4) * 4 + tl) * 32 + 16);
               const uint8_t *csw = tbl + DEC_TBL_BYTES + hv * 512 + (16 * jj + 2 * tl) * 8;
               const float4 cb0 = *reinterpret_cast<const float4 *>(csw), cb1 = *reinterpret_cast<const float4 *>(csw + 64);
+              const float2 ncb0 = make_float2(-cb0.z, -cb0.w), ncb1 = make_float2(-cb1.z, -cb1.w);
               uint32_t ka[4], kb[4];
 #pragma unroll
               for (int r = 0; r < 4; ++r) {
@@ -756,7 +773,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
                 const float a1 = bf_round(__fmaf_rn(nib_f(Oa, r), h8 ? sa.w : sa.y, h8 ? ma.w : ma.y));
                 const float b0 = bf_round(__fmaf_rn(nib_f(Eb, r), h8 ? sb.z : sb.x, h8 ? mb.z : mb.x));
                 const float b1 = bf_round(__fmaf_rn(nib_f(Ob, r), h8 ? sb.w : sb.y, h8 ? mb.w : mb.y));
-                rope_rot(a0, a1, b0, b1, h8 ? cb1 : cb0, rel_cs(rel, 16 * mt + gl + 8 * (r & 1), jj, r >> 1, tl), ka[r], kb[r]);
+                rope_rot(a0, a1, b0, b1, h8 ? cb1 : cb0, h8 ? ncb1 : ncb0, rel_cs(rel, 16 * mt + gl + 8 * (r & 1), jj, r >> 1, tl),
+                         ka[r], kb[r]);
               }
               mma_bf16(s[mt], ka[0], ka[1], ka[2], ka[3], qb[jj][0], qb[jj][1]);
               mma_bf16(s[mt], kb[0], kb[1], kb[2], kb[3], qb[jj + 4][0], qb[jj + 4][1]);

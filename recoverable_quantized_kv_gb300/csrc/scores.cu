@@ -79,19 +79,7 @@ __device__ __forceinline__ float ex2(float x) {   // 2^x on the special-function
   return y;
 }
 
-// Packed fp32 pairs (two lanes of work per instruction) and the three-input maximum.
-__device__ __forceinline__ void fma2(float &dx, float &dy, float ax, float ay, float bx, float by, float cx, float cy) {
-  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
-      " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
-      : "=f"(dx), "=f"(dy)
-      : "f"(ax), "f"(ay), "f"(bx), "f"(by), "f"(cx), "f"(cy));
-}
-__device__ __forceinline__ void add2(float &ax, float &ay, float bx, float by) {
-  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%0, %1};\n mov.b64 rb, {%2, %3};\n add.rn.f32x2 rd, ra, rb;\n"
-      " mov.b64 {%0, %1}, rd;\n}"
-      : "+f"(ax), "+f"(ay)
-      : "f"(bx), "f"(by));
-}
+// The three-input maximum.
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
