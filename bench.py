@@ -583,7 +583,7 @@ def run_diag(wl, dev, stream, n_events):
     return {"events": rep["events"], "fmm_h32": rep["fmm"], "fmm_terms": rep["fmm_terms"], "churn": rep["churn"],
             "qsa": rep["qsa"], "r_q": rep["r_q"], "tier_mass_full_quant_evict_local": rep["tier_mass"].tolist(),
             "lir3_policy": [rep["lir_eligible"], rep["lir_rescued"]],
-            "lir3_fullkv_topk": [rep["lir_oracle_eligible"], rep["lir_oracle_rescued"]],
+            "lir3_fullkv_topk": [rep["lir_fullkv_eligible"], rep["lir_fullkv_rescued"]],
             "p01": [p(0, 1, 1), p(0, 1, 8)], "p10": [p(1, 0, 1), p(1, 0, 8)],
             "route_ms_per_event_with_diag": statistics.mean(diag_ms), "route_ms_plain_pair": plain_ms[0],
             "note": "policy and FullKV caches decode the same synthetic inputs; route_ms covers both caches' "

@@ -328,7 +328,7 @@ typedef struct {
   int64_t qsa_terms;
   double tier_mass[4];           /* Full, Quantized, Evicted, Local shares at the last event, mean over units */
   int64_t lir_eligible, lir_rescued;                 /* policy Full tier */
-  int64_t lir_oracle_eligible, lir_oracle_rescued;   /* FullKV top-k_f selection */
+  int64_t lir_fullkv_eligible, lir_fullkv_rescued;   /* FullKV top-k_f selection */
   int64_t lag[8][2][2];          /* lag[Delta-1][a][b] */
 } qevict_diag_report;
 qevict_status qevict_diag_bytes(const qevict_cache *policy, const qevict_diag_config *dc, size_t *bytes);

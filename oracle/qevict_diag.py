@@ -33,7 +33,7 @@ Readings (the pages define the diagnostics on token positions of model traces):
     prompt scores).
   * mu(z) is taken at each event over the windows that exist then (Local = not yet routed).
   * An inactive episode of Eq. (18) starts when a window leaves the selected set (X goes 1 -> 0): a
-    window that was never selected cannot re-enter.  The oracle selection is the top K_f of the
+    window that was never selected cannot re-enter.  The FullKV selection (the pages' "oracle") is the top K_f of the
     routed windows by FullKV score (descending, ties to the older window).
   * P_ab(Delta) counts every pair of events (r, r + Delta) at which the window was already routed.
 """
@@ -61,7 +61,7 @@ class EventRec:
     tiers: np.ndarray      # [n_windows] policy tier after routing (LOCAL for unrouted ids)
     s_policy: np.ndarray   # [n_windows] the policy's window scores after routing
     s_full: np.ndarray     # [n_windows] the FullKV run's window scores after routing
-    s_rank: np.ndarray     # [n_windows] scores the oracle selection ranks (normally s_full)
+    s_rank: np.ndarray     # [n_windows] scores the FullKV selection ranks (normally s_full)
 
 
 class Trace:
@@ -137,7 +137,7 @@ def tier_mass(tr: Trace, ev: EventRec) -> np.ndarray:
     return np.array([ev.s_full[ex & (ev.tiers == z)].sum() / tot for z in (FULL, QUANT, EVICTED, LOCAL)])
 
 
-def selections(tr: Trace, oracle: bool):
+def selections(tr: Trace, fullkv_topk: bool):
     """X[r][w] of App. I.4: 1 if window w is in the selected full-precision set at event r; and the
     first event at which each window was routed (-1 if never)."""
     n = len(tr.events[0].tiers)
@@ -146,7 +146,7 @@ def selections(tr: Trace, oracle: bool):
     for r, ev in enumerate(tr.events):
         routed = np.arange(n) < ev.n_route
         first[(first < 0) & routed] = r
-        if oracle:
+        if fullkv_topk:
             ids = sorted(np.flatnonzero(routed).tolist(), key=lambda w: (-ev.s_rank[w], w))
             X[r, ids[:tr.k_f]] = 1
         else:
@@ -205,10 +205,10 @@ def report(traces: List[Trace], H: int = 32, m: int = 3, max_lag: int = 8) -> di
         qsa += a
         rq += b
         mus.append(tier_mass(tr, tr.events[-1]))
-        X, first = selections(tr, oracle=False)
+        X, first = selections(tr, fullkv_topk=False)
         lir += global_lir(X, first, m)
         lag += lagged_counts(X, first, max_lag)
-        Xo, fo = selections(tr, oracle=True)
+        Xo, fo = selections(tr, fullkv_topk=True)
         lir_o += global_lir(Xo, fo, m)
 
     def mean(v):
@@ -216,4 +216,4 @@ def report(traces: List[Trace], H: int = 32, m: int = 3, max_lag: int = 8) -> di
     return {"events": len(traces[0].events), "fmm": mean(fmm), "fmm_terms": len(fmm), "churn": mean(churn),
             "churn_terms": len(churn), "qsa": mean(qsa), "r_q": mean(rq), "qsa_terms": len(qsa),
             "tier_mass": np.mean(mus, axis=0), "lir_eligible": int(lir[0]), "lir_rescued": int(lir[1]),
-            "lir_oracle_eligible": int(lir_o[0]), "lir_oracle_rescued": int(lir_o[1]), "lag": lag}
+            "lir_fullkv_eligible": int(lir_o[0]), "lir_fullkv_rescued": int(lir_o[1]), "lag": lag}

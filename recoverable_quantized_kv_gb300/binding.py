@@ -63,7 +63,7 @@ class DiagReport(ctypes.Structure):
                 ("churn", ctypes.c_double), ("churn_terms", ctypes.c_int64), ("qsa", ctypes.c_double),
                 ("r_q", ctypes.c_double), ("qsa_terms", ctypes.c_int64), ("tier_mass", ctypes.c_double * 4),
                 ("lir_eligible", ctypes.c_int64), ("lir_rescued", ctypes.c_int64),
-                ("lir_oracle_eligible", ctypes.c_int64), ("lir_oracle_rescued", ctypes.c_int64),
+                ("lir_fullkv_eligible", ctypes.c_int64), ("lir_fullkv_rescued", ctypes.c_int64),
                 ("lag", ctypes.c_int64 * 32)]
 
 
@@ -296,8 +296,8 @@ class Diagnostics:
         return {"events": r.events, "fmm": r.fmm, "fmm_terms": r.fmm_terms, "churn": r.churn,
                 "churn_terms": r.churn_terms, "qsa": r.qsa, "r_q": r.r_q, "qsa_terms": r.qsa_terms,
                 "tier_mass": np.array(list(r.tier_mass)), "lir_eligible": r.lir_eligible,
-                "lir_rescued": r.lir_rescued, "lir_oracle_eligible": r.lir_oracle_eligible,
-                "lir_oracle_rescued": r.lir_oracle_rescued, "lag": np.array(list(r.lag)).reshape(8, 2, 2)}
+                "lir_rescued": r.lir_rescued, "lir_fullkv_eligible": r.lir_fullkv_eligible,
+                "lir_fullkv_rescued": r.lir_fullkv_rescued, "lag": np.array(list(r.lag)).reshape(8, 2, 2)}
 
     def close(self):
         if self.handle:

@@ -633,8 +633,8 @@ qevict_status qevict_diag_read(qevict_diag *diag, qevict_diag_report *out, qevic
     for (int z = 0; z < 4; ++z) out->tier_mass[z] += a[qv::DA_MU + z] / d.U;
     out->lir_eligible += (int64_t)a[qv::DA_LIR + 0];
     out->lir_rescued += (int64_t)a[qv::DA_LIR + 1];
-    out->lir_oracle_eligible += (int64_t)a[qv::DA_LIR + 2];
-    out->lir_oracle_rescued += (int64_t)a[qv::DA_LIR + 3];
+    out->lir_fullkv_eligible += (int64_t)a[qv::DA_LIR + 2];
+    out->lir_fullkv_rescued += (int64_t)a[qv::DA_LIR + 3];
     for (int k = 0; k < qv::DG_MAX_LAG * 4; ++k) (&out->lag[0][0][0])[k] += (int64_t)a[qv::DA_LAG + k];
     if (u == 0) out->events = (int64_t)a[qv::DA_EVENTS];
   }

@@ -85,7 +85,7 @@ def _run(wl, steps, churn=None, horizon=32, lir_m=3):
 
 def _compare(got, want):
     for key in ("events", "fmm_terms", "churn_terms", "qsa_terms", "lir_eligible", "lir_rescued",
-                "lir_oracle_eligible", "lir_oracle_rescued"):
+                "lir_fullkv_eligible", "lir_fullkv_rescued"):
         assert got[key] == want[key], (key, got[key], want[key])
     assert np.array_equal(got["lag"], want["lag"]), (got["lag"], want["lag"])
     assert abs(got["fmm"] - want["fmm"]) <= 1e-3 * max(want["fmm"], 1e-3), (got["fmm"], want["fmm"])
