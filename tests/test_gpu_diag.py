@@ -95,7 +95,8 @@ def _compare(got, want):
 
 
 @pytest.mark.parametrize("variant", [dict(), dict(no_promotion=1), dict(batch=2, h_q=8, h_kv=2),
-                                     dict(window=64, bits=4, prompt_len=3000), dict(rope_base=10000.0)])
+                                     dict(window=64, bits=4, prompt_len=3000), dict(rope_base=10000.0),
+                                     dict(n_layers=2, batch=2)])
 def test_diagnostics_match_the_oracle(lib, variant):
     wl = synth.workload("tiny_4k", prompt_len=1500, steps=64, n_plant=4, kappa=6.0, budget_num=35, q_num=40)
     wl = wl.replace(**variant)
