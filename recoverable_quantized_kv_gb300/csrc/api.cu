@@ -306,7 +306,10 @@ qevict_status qevict_prefill_route(qevict_cache *cache, int32_t layer, const voi
     s0 = buf;
   }
   cudaError_t e = qv::launch_prefill_setup(cache->dev, kp, vp, layer, s0, s);
-  if (e == cudaSuccess) e = qv::launch_route(cache->dev, layer * cache->cfg.batch, cache->cfg.batch, kp, vp, layer, 64, s);
+  // the prompt's windows all migrate at once: about four migration CTAs per SM over the batch
+  const int mig_blocks = std::max(8, 4 * device_sm_count() / cache->cfg.batch);
+  if (e == cudaSuccess)
+    e = qv::launch_route(cache->dev, layer * cache->cfg.batch, cache->cfg.batch, kp, vp, layer, mig_blocks, s);
   if (e != cudaSuccess) return QEVICT_ECUDA;
   cache->prefilled[layer] = 1;
   cache->t_host[layer] = cache->cfg.prompt_len;
