@@ -336,7 +336,9 @@ qevict_status qevict_diag_bytes(const qevict_cache *policy, const qevict_diag_co
 qevict_status qevict_diag_init(qevict_cache *policy, qevict_cache *fullkv, const qevict_diag_config *dc, void *d_buf,
                                size_t bytes, qevict_stream_t stream, qevict_diag **out);
 /* A routing event of both caches in place of two qevict_route calls: reads the FullKV masses of the
- * steps since the previous event, routes the policy, routes the FullKV cache, records the event. */
+ * steps since the previous event, routes the policy, routes the FullKV cache, records the event.
+ * The schedule of both caches is checked before anything is enqueued (QEVICT_ESCHEDULE); a launch
+ * failure after that (QEVICT_ECUDA) leaves the caches and the diagnostics out of step. */
 qevict_status qevict_diag_route(qevict_diag *diag, qevict_stream_t stream);
 /* Synchronises `stream` and sums the per-unit records into `out` (host memory). */
 qevict_status qevict_diag_read(qevict_diag *diag, qevict_diag_report *out, qevict_stream_t stream);
