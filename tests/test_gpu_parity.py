@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 import torch
 
-from gpu_lockstep import Lockstep, OUT_TOL
+from gpu_lockstep import close_rel, Lockstep, OUT_TOL
 from oracle import qevict_oracle as O
 from recoverable_quantized_kv_gb300 import binding, synth
 
@@ -109,6 +109,20 @@ def test_rope_table_rules(lib):
         c.set_rope_table(table)
     assert e.value.status == binding.ESCHEDULE
     c.check()
+
+
+def test_prefill_scores_at_32k(lib):
+    """The tensor-core prefill passes over a full 32K prompt: one KV head with its group of four query
+    heads (the group shape of the Llama-3-8B layout, planted windows included) against the oracle's
+    fp64 causal attention, window by window."""
+    wl = synth.workload("llama8b_32k", n_layers=1, h_q=4, h_kv=1)
+    cache = binding.Cache(binding.make_config(wl))
+    ins = synth.prompt_inputs(wl, 0, 0)
+    npw = O.prompt_windows(O.Config.from_obj(wl))
+    s0 = torch.empty(1, npw, dtype=torch.float32, device="cuda")
+    cache.prefill_scores(ins["q"][None].cuda(), ins["k"][None].cuda(), s0)
+    ref = O.prefill_scores(ins["q"].float().numpy(), ins["k"].float().numpy(), O.Config.from_obj(wl))
+    close_rel(s0.cpu().numpy()[0], ref, "32K prefill window scores")
 
 
 def test_minimal_prompt_until_the_cache_is_full(lib):
