@@ -26,8 +26,8 @@ def lib():
     return binding.load()
 
 
-def _run(wl, steps, churn=None, horizon=32, lir_m=3):
-    ls = Lockstep(wl, churn=churn)
+def _run(wl, steps, churn=None, horizon=32, lir_m=3, oracle_prefill_scores=True):
+    ls = Lockstep(wl, churn=churn, oracle_prefill_scores=oracle_prefill_scores)
     ls.prefill()
     fwl = fullkv_config(wl)
     rc = binding.Cache(binding.make_config(fwl))
@@ -113,6 +113,15 @@ def test_diagnostics_without_forced_scores(lib):
     got, want = _run(wl, 64, horizon=16, lir_m=1)
     _compare(got, want)
     assert got["qsa_terms"] > 0 and 0 < got["qsa"] <= 1.0 + 1e-12
+
+
+def test_diagnostics_at_32k(lib):
+    """One layer of the Llama-3-8B-shaped 32K workload (about 1000 windows, 32 query heads), forced churn:
+    five routing events, two of them with a complete FMM horizon."""
+    wl = synth.workload("llama8b_32k", n_layers=1, steps=40)
+    got, want = _run(wl, 40, churn=3, oracle_prefill_scores=False)
+    _compare(got, want)
+    assert got["events"] == 6 and got["fmm_terms"] == 2 * wl.h_q and got["lir_eligible"] >= 0
 
 
 def test_diagnostics_argument_rules(lib):
