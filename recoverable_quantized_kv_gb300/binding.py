@@ -211,7 +211,8 @@ class Cache:
 
     def set_rope_table(self, table, stream=None):
         """table: fp32 CUDA tensor [rows][64][2] of (cos, sin) per position and channel pair."""
-        if table.dtype != __import__("torch").float32 or not table.is_cuda or not table.is_contiguous():
+        import torch
+        if table.dtype != torch.float32 or not table.is_cuda or not table.is_contiguous():
             raise QEvictError(EINVAL, "set_rope_table", "table must be a contiguous float32 CUDA tensor")
         _check(load().qevict_set_rope_table(self.handle, _ptr(table), int(table.shape[0]), _stream(stream)),
                "qevict_set_rope_table")
