@@ -80,6 +80,7 @@ def test_future_missed_mass_by_hand():
     # one head, windows 0..2 (starts 4, 36, 68); event at T = 68: window 2 did not exist yet
     tr = _trace([(68, 2, [E, F, L], [0, 0, 0], [0, 0, 0])])
     H = 2
+    tr.add_step(68, [[0.7, 0.1, 0.0]], [0.2])     # the step that ended at the event: in the past
     tr.add_step(69, [[0.2, 0.3, 0.1]], [0.4])     # tau = r + 1
     tr.add_step(70, [[0.1, 0.5, 0.2]], [0.2])     # tau = r + 2 = r + H
     tr.add_step(71, [[0.9, 0.0, 0.0]], [0.1])     # beyond the horizon
@@ -88,6 +89,18 @@ def test_future_missed_mass_by_hand():
     short = _trace([(68, 2, [E, F, L], [0, 0, 0], [0, 0, 0])])
     short.add_step(69, [[0.2, 0.3, 0.1]], [0.4])
     assert QD.fmm_terms(short, H) == []           # horizon not reached: not eligible
+
+
+def test_fullkv_selection_episodes():
+    """The FullKV selection takes the top K_f routed windows by FullKV score (descending, ties to the
+    older window): window 0 ranks first, drops below window 1 for three events, and returns."""
+    sc = [[5, 1, 0], [1, 5, 0], [1, 5, 0], [1, 5, 0], [5, 1, 0]]
+    tr = _trace([(100 + 8 * r, 3, [F, Q, Q], [0, 0, 0], row) for r, row in enumerate(sc)], k_f=1)
+    X, first = QD.selections(tr, fullkv_topk=True)
+    assert X[:, 0].tolist() == [1, 0, 0, 0, 1] and X[:, 1].tolist() == [0, 1, 1, 1, 0]
+    assert QD.global_lir(X, first, 3) == (1, 1)
+    tie = _trace([(100, 3, [F, Q, Q], [0, 0, 0], [2, 2, 2])], k_f=2)
+    assert QD.selections(tie, fullkv_topk=True)[0][0].tolist() == [1, 1, 0]
 
 
 def _inputs(wl):
