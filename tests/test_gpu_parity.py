@@ -243,10 +243,12 @@ def test_status_codes(lib):
     c.check()
 
 
-def test_tuple_views_and_checkpoint(lib):
+@pytest.mark.parametrize("rope_base", [0.0, 10000.0])
+def test_tuple_views_and_checkpoint(lib, rope_base):
     """qevict_get_tuple points at each unit's regions; an exported cache imported into a fresh arena
-    resumes the run: the same next steps and routing event as the original cache."""
-    wl = synth.workload("tiny_4k", prompt_len=1200, steps=32, n_plant=4, batch=2)
+    resumes the run: the same next steps and routing event as the original cache (with pre-RoPE keys,
+    the RoPE table travels inside the arena)."""
+    wl = synth.workload("tiny_4k", prompt_len=1200, steps=32, n_plant=4, batch=2, rope_base=rope_base)
     ls = Lockstep(wl)
     ls.prefill()
     ls.decode(10)                      # one routing event, then two steps with pending masses
