@@ -48,6 +48,9 @@ def parse_args():
     ap.add_argument("--diag", type=int, default=0,
                     help="also run N routing events with the routing diagnostics against a FullKV cache")
     ap.add_argument("--int4", action="store_true", help="the INT4 / 64-token-window format of the workload")
+    ap.add_argument("--ranker", type=int, default=0,
+                    help="window ranking: 0 cumulative, 1 decayed, 2 p-norm, 3 key norm (GPU arm only)")
+    ap.add_argument("--no-promotion", action="store_true", help="quantized windows never return to Full")
     ap.add_argument("--rope-base", type=float, default=0.0,
                     help="keys carry RoPE with this base and Quantized keys are kept before it (GPU arm only)")
     ap.add_argument("--layers", type=int, default=None,
@@ -279,6 +282,8 @@ def run_gpu(args, rank, world):
         wl = wl.replace(rope_base=args.rope_base)
     if args.int4:
         wl = wl.replace(window=64, bits=4)
+    if args.ranker or args.no_promotion:
+        wl = wl.replace(ranker=args.ranker, no_promotion=1 if args.no_promotion else 0)
     K, Wm = args.steps, args.warmup
     Om = wl.omega
     K_kern = 2 * Om
@@ -500,6 +505,7 @@ def run_gpu(args, rank, world):
                    "bits": wl.bits, "omega": Om, "budget": f"{wl.budget_num}/{wl.budget_den}",
                    "q": f"{wl.q_num}/{wl.q_den}", "k_f": bud.k_f, "k_q": bud.k_q,
                    "parallelism": f"replicas x{world}", "rope_base": wl.rope_base,
+                   "ranker": wl.ranker, "no_promotion": wl.no_promotion,
                    "l2": "inputs larger than L2: each step streams every layer's cache (%.0f MB)" %
                          (bytes_per_step / 1e6)},
         "hbm_gbs_step": bytes_per_step / (ms_step / 1e3) / 1e9,
