@@ -234,6 +234,15 @@ qevict_status qevict_read_counters(qevict_cache *cache, int64_t *host7, qevict_s
  * CUDA graphs of decode steps) and returns QEVICT_EDEVICE if the device status word is set. */
 qevict_status qevict_check(qevict_cache *cache, qevict_stream_t stream);
 
+/* Failure-reporting self-test.  Enqueues on `stream` a one-thread kernel that waits, through the
+ * same bounded wait every kernel of the library uses, on an mbarrier phase that nothing completes.
+ * After the wait's limit (about 200 ms) the kernel records a timeout in the cache's device status
+ * word and returns; no GPU fault is raised and the context stays usable.  Nothing else in the cache
+ * changes.  The next qevict_check / qevict_read_counters returns QEVICT_EDEVICE; the word stays set
+ * until an exported state taken before it is imported (the status word travels in the arena) or the
+ * cache is re-initialised.  Returns QEVICT_ECUDA if the launch fails. */
+qevict_status qevict_selftest_wait(qevict_cache *cache, qevict_stream_t stream);
+
 /* Scratch size, in floats, of qevict_prefill_scores_noalloc: 2 * batch * h_q * prompt_len must not
  * exceed it (2 Mi floats = 8 MiB, e.g. 32 query heads x 32768 prompt tokens for one sequence). */
 #define QEVICT_NOALLOC_SCRATCH_FLOATS (2LL * 1024 * 1024)

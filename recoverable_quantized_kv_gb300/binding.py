@@ -101,6 +101,7 @@ def load() -> ctypes.CDLL:
         "qevict_import_state": [P, P, ctypes.c_size_t, P],
         "qevict_read_counters": [P, ctypes.POINTER(I64), P],
         "qevict_check": [P, P],
+        "qevict_selftest_wait": [P, P],
         "qevict_destroy": [P],
         "qevict_prefill_scores_noalloc": [I32, I32, I32, I32, I32, I32, P, P, P, P],
     }
@@ -121,7 +122,8 @@ def exported_symbols():
             "qevict_read_counters", "qevict_check", "qevict_destroy", "qevict_status_string",
             "qevict_prefill_scores_noalloc", "qevict_flush_scores", "qevict_get_tuple", "qevict_export_bytes",
             "qevict_export_state", "qevict_import_state", "qevict_set_rope_table", "qevict_diag_bytes",
-            "qevict_diag_init", "qevict_diag_route", "qevict_diag_read", "qevict_diag_destroy"]
+            "qevict_diag_init", "qevict_diag_route", "qevict_diag_read", "qevict_diag_destroy",
+            "qevict_selftest_wait"]
 
 
 def _check(status: int, where: str):
@@ -260,6 +262,10 @@ class Cache:
 
     def check(self, stream=None):
         _check(load().qevict_check(self.handle, _stream(stream)), "qevict_check")
+
+    def selftest_wait(self, stream=None):
+        """Enqueue the bounded-wait self-test: a wait that runs out and records a timeout."""
+        _check(load().qevict_selftest_wait(self.handle, _stream(stream)), "qevict_selftest_wait")
 
     # ---- tensor views of the cache tuple inside the arena (read-only use in tests)
     def region(self, name: str, unit: int, nbytes: int):

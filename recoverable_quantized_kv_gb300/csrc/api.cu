@@ -15,6 +15,7 @@
 
 namespace qv {
 cudaError_t launch_init(const CacheDev &C, cudaStream_t s);
+cudaError_t launch_wait_selftest(const CacheDev &C, cudaStream_t s);
 cudaError_t launch_route(const CacheDev &C, int unit0, int n_units, const __nv_bfloat16 *kp,
                          const __nv_bfloat16 *vp, int layer, int mig_blocks, cudaStream_t s);
 cudaError_t launch_prefill_setup(const CacheDev &C, const __nv_bfloat16 *kp, const __nv_bfloat16 *vp, int layer,
@@ -414,6 +415,12 @@ qevict_status qevict_check(qevict_cache *cache, qevict_stream_t stream) {
       cache->routes_done = m[(size_t)l * qv::META_INTS + qv::M_NEVENT];
     }
   return st;
+}
+
+qevict_status qevict_selftest_wait(qevict_cache *cache, qevict_stream_t stream) {
+  if (!cache) return QEVICT_EINVAL;
+  return qv::launch_wait_selftest(cache->dev, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? QEVICT_OK
+                                                                                                       : QEVICT_ECUDA;
 }
 
 qevict_status qevict_get_tuple(const qevict_cache *cache, int32_t layer, int32_t seq, qevict_tuple *out) {

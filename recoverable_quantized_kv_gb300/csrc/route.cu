@@ -289,8 +289,15 @@ __global__ void __launch_bounds__(RT_THREADS, 1) route_kernel(const CacheDev C, 
   __syncthreads();
   const int nNeedF = block_exscan(rankF, n_new, wsum);
   const int nNeedL = block_exscan(rankL, n_new, wsum);
-  if (nNeedF > totF || nNeedL > totL) {   // impossible while the tables are consistent
-    if (tid == 0) atomicOr(C.status(), QV_ERR_SLOT);
+  // Unreachable with in-range slot ids: a busy F slot belongs to a window that keeps one of the K_f
+  // Full places and a newcomer takes another, so nNeedF <= totF; the ledger holds K_f + K_q places the
+  // same way.  Should it ever fire, this event changes no tier, table or slot and migrates nothing.
+  if (nNeedF > totF || nNeedL > totL) {
+    if (tid == 0) {
+      atomicOr(C.status(), QV_ERR_SLOT);
+      meta[M_NQUANT] = 0;
+      meta[M_NMOVE] = 0;
+    }
     return;
   }
 
@@ -650,6 +657,18 @@ __global__ void init_slots_kernel(const CacheDev C) {
   }
 }
 
+// Failure-reporting self-test: one thread waits, through the library's bounded wait, on an mbarrier
+// phase that nothing completes.  The wait gives up after its limit, records QV_ERR_TIMEOUT in the
+// status word and the kernel returns: the context stays usable.
+__global__ void wait_selftest_kernel(const CacheDev C) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_wait(&bar, 0, C.status());
+  }
+}
+
 // ----------------------------------------------------------------------------- launchers
 
 int route_smem_bytes() { return 8 * RT_MAXN + 4 * RT_MAXN * 2 + RT_MAXN; }
@@ -657,6 +676,11 @@ int route_max_windows() { return RT_MAXN; }
 
 cudaError_t launch_init(const CacheDev &C, cudaStream_t s) {
   init_slots_kernel<<<C.B * C.L, 256, 0, s>>>(C);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(const CacheDev &C, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(C);
   return cudaGetLastError();
 }
 

@@ -243,6 +243,32 @@ def test_status_codes(lib):
     c.check()
 
 
+def test_wait_timeout_is_reported_and_recoverable(lib):
+    """Failure detection without a GPU fault: a bounded wait that runs out (an mbarrier phase that
+    nothing completes) records a timeout in the device status word and returns.  qevict_check and
+    qevict_read_counters then report QEVICT_EDEVICE, the rest of the cache is untouched, and
+    importing a state exported before the timeout resumes the run in lockstep with the oracle."""
+    wl = synth.workload("tiny_4k", prompt_len=1200, steps=24, n_plant=4)
+    ls = Lockstep(wl)
+    ls.prefill()
+    ls.decode(8)
+    snap = ls.cache.export_state()
+    ls.cache.selftest_wait()
+    for call in (ls.cache.check, ls.cache.counters):
+        with pytest.raises(binding.QEvictError) as e:
+            call()
+        assert e.value.status == binding.EDEVICE
+    after = ls.cache.export_state()
+    diff = np.flatnonzero(snap != after)
+    # one byte changed: the low byte of the status word, 0 -> the timeout bit
+    assert diff.size == 1 and int(snap[diff[0]]) == 0 and int(after[diff[0]]) == 1, diff
+    ls.cache.import_state(snap)
+    ls.cache.check()
+    ls.decode(16)                                               # two more routing events
+    got, want = ls.counters()
+    assert got == want, (got, want)
+
+
 @pytest.mark.parametrize("rope_base", [0.0, 10000.0])
 def test_tuple_views_and_checkpoint(lib, rope_base):
     """qevict_get_tuple points at each unit's regions; an exported cache imported into a fresh arena
