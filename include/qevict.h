@@ -192,7 +192,8 @@ qevict_status qevict_prefill_scores(const qevict_cache *cache, const void *q_pro
  * from q_prompt when s0 is NULL), routes all historical prompt windows into F / Q / E and
  * materialises F (bf16 copy) and Q (quantised once).  k_prompt, v_prompt [batch][P][h_kv][d].
  * Must be called exactly once per layer, before any decode step of that layer.  A rope = 1 cache
- * needs its RoPE table first (QEVICT_ESCHEDULE otherwise). */
+ * needs its RoPE table first (QEVICT_ESCHEDULE otherwise).  k_prompt and v_prompt must be 2-byte,
+ * s0 4-byte and (when s0 is NULL) q_prompt and k_prompt 16-byte aligned, else QEVICT_EINVAL. */
 qevict_status qevict_prefill_route(qevict_cache *cache, int32_t layer, const void *k_prompt,
                                    const void *v_prompt, const float *s0, const void *q_prompt,
                                    qevict_stream_t stream);
@@ -204,7 +205,8 @@ qevict_status qevict_prefill_route(qevict_cache *cache, int32_t layer, const voi
  * and records the attention mass of every accessible non-sink window.  The window scores absorb
  * these masses, (1/h_q) * sum_h (mass of window w) per step and in step order, at the next
  * qevict_flush_scores or qevict_route.  q [batch][h_q][d].  Fails with QEVICT_ESCHEDULE if the
- * cache is full (T = max_len) or a routing event is due. */
+ * cache is full (T = max_len) or a routing event is due, with QEVICT_EINVAL if q or k_new is not
+ * 4-byte aligned or v_new or out is not 2-byte aligned. */
 qevict_status qevict_decode_step(qevict_cache *cache, int32_t layer, const void *q, const void *k_new,
                                  const void *v_new, void *out, qevict_stream_t stream);
 

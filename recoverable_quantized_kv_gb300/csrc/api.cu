@@ -4,6 +4,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <cstdint>
 #include <cstring>
 #include <new>
 #include <vector>
@@ -84,7 +85,12 @@ qevict_status compute_budget(const qevict_config *c, qevict_budget_info *b) {
   const int64_t c_tok = 4LL * c->h_kv * c->d_head;            // bf16 K + V of one token
   const int64_t tok_bytes = c_tok + 4;                          // + int32 position
   b->full_bytes = c_tok * c->prompt_len;                        // Eq. (7) per layer and sequence
-  b->b_total = c->b_total ? c->b_total : b->full_bytes * c->budget_num / c->budget_den;
+  if (c->b_total) {
+    b->b_total = c->b_total;
+  } else {   // the product may pass 2^63 for extreme fractions: clamp in 128 bits
+    const __int128 bt = (__int128)b->full_bytes * c->budget_num / c->budget_den;
+    b->b_total = bt > (__int128)INT64_MAX ? INT64_MAX : (int64_t)bt;
+  }
   b->b_sink = c->n_sink * tok_bytes;
   b->b_local = (int64_t)(c->n_recent + c->window) * tok_bytes;
   b->b_hist = b->b_total - b->b_sink - b->b_local;
@@ -295,6 +301,7 @@ qevict_status qevict_prefill_scores(const qevict_cache *cache, const void *q_pro
 qevict_status qevict_prefill_route(qevict_cache *cache, int32_t layer, const void *k_prompt, const void *v_prompt,
                                    const float *s0, const void *q_prompt, qevict_stream_t stream) {
   if (!cache || layer < 0 || layer >= cache->cfg.n_layers || !k_prompt || !v_prompt) return QEVICT_EINVAL;
+  if ((((uintptr_t)k_prompt | (uintptr_t)v_prompt) & 1) || ((uintptr_t)s0 & 3)) return QEVICT_EINVAL;
   if (!s0 && (!q_prompt || (((uintptr_t)q_prompt | (uintptr_t)k_prompt) & 15))) return QEVICT_EINVAL;
   if (cache->prefilled[layer] || (cache->cfg.rope && !cache->rope_set)) return QEVICT_ESCHEDULE;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -321,6 +328,8 @@ qevict_status qevict_prefill_route(qevict_cache *cache, int32_t layer, const voi
 qevict_status qevict_decode_step(qevict_cache *cache, int32_t layer, const void *q, const void *k_new,
                                  const void *v_new, void *out, qevict_stream_t stream) {
   if (!cache || layer < 0 || layer >= cache->cfg.n_layers || !q || !k_new || !v_new || !out) return QEVICT_EINVAL;
+  // q and k_new are read as bf16 pairs, v_new and out element by element
+  if ((((uintptr_t)q | (uintptr_t)k_new) & 3) || (((uintptr_t)v_new | (uintptr_t)out) & 1)) return QEVICT_EINVAL;
   if (!cache->prefilled[layer]) return QEVICT_ESCHEDULE;
   const int T = cache->t_host[layer];
   if (T >= cache->cfg.max_len) return QEVICT_ESCHEDULE;

@@ -88,3 +88,13 @@ def test_router_capacity(cpu_lib):
     with pytest.raises(binding.QEvictError) as e:
         binding.budget(binding.make_config(wl, max_len=cap + 1))
     assert e.value.status == binding.EINVAL
+
+
+def test_budget_fraction_does_not_overflow(cpu_lib):
+    """full_bytes * budget_num passes 2^63 for a wide, long unit and a huge fraction: the budget clamps
+    at the largest int64 instead of wrapping to a negative (EBUDGET) value."""
+    wl = synth.workload("tiny_4k", h_q=1024, h_kv=1024, prompt_len=1 << 18, budget_num=(1 << 31) - 1,
+                        budget_den=1)
+    b = binding.budget(binding.make_config(wl, max_len=1 << 18))
+    assert b.full_bytes == 4 * 1024 * 128 * (1 << 18)
+    assert b.b_total == (1 << 63) - 1 and b.k_f > 0 and b.k_q > 0

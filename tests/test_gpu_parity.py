@@ -224,6 +224,13 @@ def test_status_codes(lib):
     with pytest.raises(binding.QEvictError) as e:     # decode before prefill
         c.decode_step(0, q, kv, kv, out)
     assert e.value.status == binding.ESCHEDULE
+    # q one bf16 element off a 4-byte boundary: refused on the host, nothing is launched
+    qbuf = torch.zeros(1 + wl.h_q * 128, dtype=torch.bfloat16, device="cuda")
+    q_odd = qbuf[1:].view(1, wl.h_q, 128)
+    assert q_odd.data_ptr() % 4 == 2
+    with pytest.raises(binding.QEvictError) as e:
+        c.decode_step(0, q_odd, kv, kv, out)
+    assert e.value.status == binding.EINVAL
     p = synth.prompt_inputs(wl, 0, 0)
     s0 = torch.rand(1, O.prompt_windows(O.Config.from_obj(wl)), device="cuda")
     c.prefill_route(0, p["k"][None].cuda(), p["v"][None].cuda(), s0=s0)
