@@ -227,10 +227,6 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
-// Exact float of a small non-negative integer code (c < 2^23) without the conversion pipe.
-
-__device__ __forceinline__ float fast_exp2(float x) { return exp2f(x); }
-
 template <typename T>
 __device__ __forceinline__ T warp_max_xor_g(T v) {   // reduce over lanes sharing lane%4
   v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));

@@ -64,6 +64,14 @@ struct DecGeo {
 __device__ __forceinline__ uint32_t ldg32(const void *p) { return __ldg(reinterpret_cast<const uint32_t *>(p)); }
 __device__ __forceinline__ uint32_t ldg16(const void *p) { return __ldg(reinterpret_cast<const unsigned short *>(p)); }
 
+// 2^x on the special-function unit (relative error about 2^-22); results below 2^-126 flush to zero,
+// which drops nothing from a probability sum whose largest term is 1.
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // One online-softmax step over NMT 16-token groups of S^T fragments (rows tokens, cols heads).
 // s is in log2 units; rows flagged invalid are excluded.  On return s holds the probabilities
 // relative to the running max m_run, tsum the per-head sum over this item.  The running max only
@@ -71,8 +79,9 @@ __device__ __forceinline__ uint32_t ldg16(const void *p) { return __ldg(reinterp
 // probability is already <= 1 and nothing accumulated so far (o, macc, l_run) needs rescaling.
 template <int NMT>
 __device__ __forceinline__ void online_step(float (&s)[NMT][4], const bool (&valid)[NMT][2], float (&m_run)[2],
-                                            float (&l_run)[2], float (&o)[8][4], float (&macc)[2],
-                                            float (&tsum)[2]) {
+                                            float &l_run, float (&o)[8][4], float (&macc)[2],
+                                            float &tsum) {
+  const bool odd = (threadIdx.x >> 2) & 1;
   float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
   for (int mt = 0; mt < NMT; ++mt)
@@ -89,9 +98,9 @@ __device__ __forceinline__ void online_step(float (&s)[NMT][4], const bool (&val
       const float mnew = fmaxf(m_run[h], warp_max_xor_g(mx[h]));
       corr[h] = exp2f(m_run[h] - (mnew == -INFINITY ? 0.f : mnew));
       m_run[h] = mnew;
-      l_run[h] *= corr[h];
       macc[h] *= corr[h];
     }
+    l_run *= odd ? corr[1] : corr[0];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       o[i][0] *= corr[0];
@@ -109,15 +118,16 @@ __device__ __forceinline__ void online_step(float (&s)[NMT][4], const bool (&val
     for (int r = 0; r < 2; ++r)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const float p = valid[mt][r] ? exp2f(s[mt][2 * r + h] - base[h]) : 0.f;
+        const float p = valid[mt][r] ? ex2_ftz(s[mt][2 * r + h] - base[h]) : 0.f;
         s[mt][2 * r + h] = p;
         ps[h] += p;
       }
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    tsum[h] = warp_sum_xor_g(ps[h]);
-    l_run[h] += tsum[h];
-  }
+  float v = odd ? ps[1] : ps[0];
+  v += __shfl_xor_sync(0xffffffffu, odd ? ps[0] : ps[1], 4);
+  v += __shfl_xor_sync(0xffffffffu, v, 8);
+  v += __shfl_xor_sync(0xffffffffu, v, 16);
+  tsum = v;
+  l_run += v;
 }
 
 // B fragments of P^T for k-step kk from the S^T accumulator layout (8x8 transposes).
@@ -353,7 +363,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   if (threadIdx.x == 0) q_next = 0;
   __syncthreads();
 
-  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f}, macc[2] = {0.f, 0.f};
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run = 0.f, macc[2] = {0.f, 0.f};
   float o[8][4];
 #pragma unroll
   for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
@@ -441,7 +451,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
     if (pos >= cta_items) break;
     const int c0 = chunk_start(pos);
     const int it = item_of(pos);
-    float tsum[2];
+    float tsum;
     if (it == 0) {
       // ---------------- sink tokens (no mass): fragments straight from the compact sink rows
       float sacc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
@@ -476,14 +486,11 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
     }
 
     // log2-sum-exp of the window's logits per head, over its 32-token halves
-    float wmu[2] = {-INFINITY, -INFINITY};
+    float wmu = -INFINITY;   // this lane's head: 2tl + (gl & 1)
     auto add_half_mass = [&]() {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const float x = tsum[h] > 0.f ? m_run[h] + __log2f(tsum[h]) : -INFINITY;
-        const float hi = fmaxf(wmu[h], x), lo = fminf(wmu[h], x);
-        wmu[h] = lo == -INFINITY ? hi : hi + __log2f(1.f + exp2f(lo - hi));
-      }
+      const float x = tsum > 0.f ? (gl & 1 ? m_run[1] : m_run[0]) + __log2f(tsum) : -INFINITY;
+      const float hi = fmaxf(wmu, x), lo = fminf(wmu, x);
+      wmu = lo == -INFINITY ? hi : hi + __log2f(1.f + exp2f(lo - hi));
     };
 
     if (it <= nL + nF) {
@@ -686,8 +693,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
         pbh[kk][0] = movmatrix_trans(pack_half(s[kk][0] * s0v, s[kk][1] * s0v));
         pbh[kk][1] = movmatrix_trans(pack_half(s[kk][2] * s1v, s[kk][3] * s1v));
       }
-      macc[0] += warp_sum_xor_g(pm0);
-      macc[1] += warp_sum_xor_g(pm1);
+      macc[0] += pm0;
+      macc[1] += pm1;
       const uint4 vw0 = lds128(ch + Gm::OFF_VCODE + lane * 16), vw1 = lds128(ch + Gm::OFF_VCODE + 512 + lane * 16);
 #pragma unroll
       for (int kk = 0; kk < NMT; ++kk) {
@@ -813,8 +820,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
           pbh[kk][0] = movmatrix_trans(pack_half(s[kk][0] * s0v, s[kk][1] * s0v));
           pbh[kk][1] = movmatrix_trans(pack_half(s[kk][2] * s1v, s[kk][3] * s1v));
         }
-        macc[0] += warp_sum_xor_g(pm0);
-        macc[1] += warp_sum_xor_g(pm1);
+        macc[0] += pm0;
+        macc[1] += pm1;
         // values: tile (token group tg, dim tile i) is word ((tile/4)*32 + lane)*4 + tile%4 of the V
         // codes; its registers 0, 1 sit at nibbles 0, 1 of each half, registers 2, 3 at nibbles 2, 3
 #pragma unroll
@@ -838,13 +845,9 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
     }
     // the window's log2-sum-exp per head: its mass is 2^(mu - M) / L with the merged max M and sum
     // L; recorded under the window's stable index (recent, then Full, then Quantized)
-    if (gl == 0) {
+    if (gl < 2 && 2 * tl + gl < G) {
       const int sidx = it <= nL ? it : (it <= nL + nF ? it - nL + C.loc_items() : it - nL - nF + C.loc_items() + C.kf_cap());
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int head = 2 * tl + h;
-        if (head < G) mu[(size_t)sidx * 8 + head] = wmu[h];
-      }
+      mu[(size_t)sidx * 8 + 2 * tl + gl] = wmu;
     }
   }
   }   // consumer warps
@@ -858,12 +861,12 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   float *sM = cf + DEC_CONSUMERS * 8;            // [16] CTA max per head, then the merged max and 1/L
   float *cO = sM + 16;                           // [DEC_CONSUMERS][D][8] unnormalised outputs
   if (warp < DEC_CONSUMERS) {
-    if (gl == 0) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        cm[warp * 8 + 2 * tl + h] = m_run[h];
-        cl[warp * 8 + 2 * tl + h] = l_run[h];
-      }
+    // the Quantized values' offset term was summed per lane; its lanes of each head meet once, here
+    macc[0] = warp_sum_xor_g(macc[0]);
+    macc[1] = warp_sum_xor_g(macc[1]);
+    if (gl < 2) {
+      cm[warp * 8 + 2 * tl + gl] = gl ? m_run[1] : m_run[0];
+      cl[warp * 8 + 2 * tl + gl] = l_run;
     }
     if (2 * tl < G) {   // heads 2tl, 2tl+1 of dims 16i+gl and 16i+gl+8, as float2
 #pragma unroll
