@@ -98,3 +98,27 @@ def test_budget_fraction_does_not_overflow(cpu_lib):
     b = binding.budget(binding.make_config(wl, max_len=1 << 18))
     assert b.full_bytes == 4 * 1024 * 128 * (1 << 18)
     assert b.b_total == (1 << 63) - 1 and b.k_f > 0 and b.k_q > 0
+
+
+def _golden_budget_rows():
+    path = os.path.join(ROOT, "tests", "golden", "budget_capacities.txt")
+    rows = [ln.split() for ln in open(path) if ln.strip() and not ln.startswith("#")]
+    cols = ["name", "h_kv", "window", "bits", "n_sink", "n_recent", "prompt_len", "budget_num", "budget_den",
+            "c_tok", "full", "b_total", "b_sink", "b_local", "b_hist", "payload", "m_q", "m_f", "k_f", "k_q"]
+    return [dict(zip(cols, [r[0]] + [int(x) for x in r[1:]])) for r in rows]
+
+
+@pytest.mark.parametrize("row", _golden_budget_rows(), ids=lambda r: r["name"])
+def test_budget_against_hand_worked_capacities(cpu_lib, row):
+    """The oracle's and the library's budgets equal the capacities worked by hand from QEvict §4.3
+    Eq. (3) and App. B.4 Eq. (7)-(8) (tests/golden/budget_capacities.txt)."""
+    wl = synth.workload("tiny_4k", h_q=4 * row["h_kv"], h_kv=row["h_kv"], window=row["window"], bits=row["bits"],
+                        n_sink=row["n_sink"], n_recent=row["n_recent"], prompt_len=row["prompt_len"],
+                        budget_num=row["budget_num"], budget_den=row["budget_den"], q_num=70, q_den=100)
+    ob = O.budget(O.Config.from_obj(wl))
+    b = binding.budget(binding.make_config(wl))
+    want = (row["full"], row["b_total"], row["b_sink"], row["b_local"], row["b_hist"], row["payload"], row["m_q"],
+            row["m_f"], row["k_f"], row["k_q"])
+    for got in (ob, b):
+        assert (got.full_bytes, got.b_total, got.b_sink, got.b_local, got.b_hist, got.payload, got.m_q, got.m_f,
+                got.k_f, got.k_q) == want

@@ -113,3 +113,27 @@ def test_dequantize_is_bf16_of_one_rounded_sum():
     ref = torch.addcmul(torch.from_numpy(m.astype(np.float32))[:, None], torch.from_numpy(c.astype(np.float32)),
                         torch.from_numpy(s.astype(np.float32))[:, None]).to(torch.bfloat16).float().numpy()
     assert np.array_equal(ours, ref)
+
+
+def _golden_groups():
+    import os
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "quant_groups.txt")
+    out = []
+    for ln in open(path):
+        if ln.strip() and not ln.startswith("#"):
+            f = [p.split() for p in ln.split("|")]
+            out.append((int(f[0][0]), [float(v) for v in f[1]], float(f[2][0]), float(f[3][0]),
+                        [int(v) for v in f[4]], [float(v) for v in f[5]]))
+    return out
+
+
+@pytest.mark.parametrize("bits,x,s,m,codes,xhat", _golden_groups())
+def test_groups_worked_by_hand(bits, x, s, m, codes, xhat):
+    """Groups whose parameters, codes and reconstructions were worked by hand
+    (tests/golden/quant_groups.txt, QEvict §4.3 "Migration-Stable Quantization")."""
+    xa = np.array([x], np.float32)
+    assert np.array_equal(O.bf16_round(xa), xa)
+    c, s16, m16 = O.quantize_groups(xa, axis=1, bits=bits)
+    assert float(s16[0]) == s and float(m16[0]) == m
+    assert c[0].tolist() == codes
+    assert O.dequantize_groups(c, s16, m16, axis=1)[0].tolist() == xhat
