@@ -73,14 +73,17 @@ __device__ __forceinline__ float ex2_ftz(float x) {
 }
 
 // One online-softmax step over NMT 16-token groups of S^T fragments (rows tokens, cols heads).
-// s is in log2 units; rows flagged invalid are excluded.  On return s holds the probabilities
-// relative to the running max m_run, tsum the per-head sum over this item.  The running max only
+// s holds raw logits q.k; `scale` (log2(e) / sqrt(d)) takes them to log2 units inside the
+// exponent's FMA, and the item's max is taken on raw logits and scaled once (a positive factor keeps
+// the order).  Rows flagged invalid are excluded.  On return s holds the probabilities relative to
+// the running max m_run (log2 units), tsum the sum of this lane's head over the item (heads 2tl and
+// 2tl + 1 on even and odd gl).  The running max only
 // moves when some logit of the item exceeds it (one warp vote decides); otherwise every
 // probability is already <= 1 and nothing accumulated so far (o, macc, l_run) needs rescaling.
 template <int NMT>
 __device__ __forceinline__ void online_step(float (&s)[NMT][4], const bool (&valid)[NMT][2], float (&m_run)[2],
                                             float &l_run, float (&o)[8][4], float (&macc)[2],
-                                            float &tsum) {
+                                            float &tsum, const float scale) {
   const bool odd = (threadIdx.x >> 2) & 1;
   float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
@@ -91,6 +94,8 @@ __device__ __forceinline__ void online_step(float (&s)[NMT][4], const bool (&val
         mx[0] = fmaxf(mx[0], s[mt][2 * r]);
         mx[1] = fmaxf(mx[1], s[mt][2 * r + 1]);
       }
+  mx[0] *= scale;
+  mx[1] *= scale;
   if (!__all_sync(0xffffffffu, mx[0] <= m_run[0] && mx[1] <= m_run[1])) {
     float corr[2];
 #pragma unroll
@@ -118,7 +123,7 @@ __device__ __forceinline__ void online_step(float (&s)[NMT][4], const bool (&val
     for (int r = 0; r < 2; ++r)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const float p = valid[mt][r] ? ex2_ftz(s[mt][2 * r + h] - base[h]) : 0.f;
+        const float p = valid[mt][r] ? ex2_ftz(fmaf(s[mt][2 * r + h], scale, -base[h])) : 0.f;
         s[mt][2 * r + h] = p;
         ps[h] += p;
       }
@@ -465,10 +470,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
         const uint32_t a3 = r1 ? ldg32(sk + (gl + 8) * D + 16 * j + 2 * tl + 8) : 0u;
         mma_bf16(sacc[0], a0, a1, a2, a3, qb[j][0], qb[j][1]);
       }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) sacc[0][k] *= io.scale_log2;
       const bool valid[1][2] = {{r0, r1}};
-      online_step<1>(sacc, valid, m_run, l_run, o, macc, tsum);
+      online_step<1>(sacc, valid, m_run, l_run, o, macc, tsum, io.scale_log2);
       uint32_t pb[1][2];
       p_to_b<1>(sacc, pb);
       const int t0 = 2 * tl, t1 = 2 * tl + 8;
@@ -546,10 +549,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
           } else {
             valid[mt][0] = valid[mt][1] = true;
           }
-#pragma unroll
-          for (int k = 0; k < 4; ++k) s[mt][k] *= io.scale_log2;
         }
-        online_step<NMT>(s, valid, m_run, l_run, o, macc, tsum);
+        online_step<NMT>(s, valid, m_run, l_run, o, macc, tsum, io.scale_log2);
         uint32_t pb[NMT][2];
         p_to_b<NMT>(s, pb);
         const uint8_t *vc[NMT];
@@ -674,10 +675,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
 #pragma unroll
       for (int mt = 0; mt < NMT; ++mt) {
         valid[mt][0] = valid[mt][1] = true;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) s[mt][k] *= io.scale_log2;
       }
-      online_step<NMT>(s, valid, m_run, l_run, o, macc, tsum);
+      online_step<NMT>(s, valid, m_run, l_run, o, macc, tsum, io.scale_log2);
       // values: o += sum_tok (p * s_tok) * code + (sum_tok p * m_tok) in every dim
       uint32_t pbh[NMT][2];
       float pm0 = 0.f, pm1 = 0.f;
@@ -688,10 +687,13 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
         const int t0 = 16 * kk + gl, t1 = t0 + 8;
         const float s0v = __half2float(vsp[t0]), s1v = __half2float(vsp[t1]);
         const float m0v = __half2float(vmp[t0]), m1v = __half2float(vmp[t1]);
-        pm0 = fmaf(s[kk][0], m0v, fmaf(s[kk][2], m1v, pm0));
-        pm1 = fmaf(s[kk][1], m0v, fmaf(s[kk][3], m1v, pm1));
-        pbh[kk][0] = movmatrix_trans(pack_half(s[kk][0] * s0v, s[kk][1] * s0v));
-        pbh[kk][1] = movmatrix_trans(pack_half(s[kk][2] * s1v, s[kk][3] * s1v));
+        fma2(pm0, pm1, s[kk][2], s[kk][3], m1v, m1v, pm0, pm1);
+        fma2(pm0, pm1, s[kk][0], s[kk][1], m0v, m0v, pm0, pm1);
+        float x0, x1, x2, x3;
+        mul2(x0, x1, s[kk][0], s[kk][1], s0v, s0v);
+        mul2(x2, x3, s[kk][2], s[kk][3], s1v, s1v);
+        pbh[kk][0] = movmatrix_trans(pack_half(x0, x1));
+        pbh[kk][1] = movmatrix_trans(pack_half(x2, x3));
       }
       macc[0] += pm0;
       macc[1] += pm1;
@@ -804,10 +806,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
 #pragma unroll
         for (int mt = 0; mt < NMT; ++mt) {
           valid[mt][0] = valid[mt][1] = true;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) s[mt][k] *= io.scale_log2;
         }
-        online_step<NMT>(s, valid, m_run, l_run, o, macc, tsum);
+        online_step<NMT>(s, valid, m_run, l_run, o, macc, tsum, io.scale_log2);
         uint32_t pbh[NMT][2];
         float pm0 = 0.f, pm1 = 0.f;
 #pragma unroll
@@ -815,10 +815,13 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
           const int t0 = 32 * hv + 16 * kk + gl, t1 = t0 + 8;
           const float s0v = __half2float(vsp[t0]), s1v = __half2float(vsp[t1]);
           const float m0v = __half2float(vmp[t0]), m1v = __half2float(vmp[t1]);
-          pm0 = fmaf(s[kk][0], m0v, fmaf(s[kk][2], m1v, pm0));
-          pm1 = fmaf(s[kk][1], m0v, fmaf(s[kk][3], m1v, pm1));
-          pbh[kk][0] = movmatrix_trans(pack_half(s[kk][0] * s0v, s[kk][1] * s0v));
-          pbh[kk][1] = movmatrix_trans(pack_half(s[kk][2] * s1v, s[kk][3] * s1v));
+          fma2(pm0, pm1, s[kk][2], s[kk][3], m1v, m1v, pm0, pm1);
+          fma2(pm0, pm1, s[kk][0], s[kk][1], m0v, m0v, pm0, pm1);
+          float x0, x1, x2, x3;
+          mul2(x0, x1, s[kk][0], s[kk][1], s0v, s0v);
+          mul2(x2, x3, s[kk][2], s[kk][3], s1v, s1v);
+          pbh[kk][0] = movmatrix_trans(pack_half(x0, x1));
+          pbh[kk][1] = movmatrix_trans(pack_half(x2, x3));
         }
         macc[0] += pm0;
         macc[1] += pm1;
