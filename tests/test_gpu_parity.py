@@ -174,6 +174,16 @@ def test_budget_above_full_is_dense_attention(lib):
     assert not np.any(st == O.EVICTED) and not np.any(st == O.QUANT)
 
 
+def test_router_at_window_capacity(lib):
+    """The largest unit the router sorts in one CTA: 8192 windows (a 262K-token context at W = 32).
+    Prefill routing over every prompt window and one routing event, in lockstep with the oracle: the
+    tier states, slots, tables and ledgers of all 8192 windows, every output and every window mass."""
+    wl = synth.workload("tiny_4k", prompt_len=262148 - 8, steps=8, n_plant=8, kappa=6.0, budget_num=20)
+    assert binding.budget(binding.make_config(wl)).n_windows == 8192
+    ls = _run(wl, 8, oracle_prefill_scores=False)
+    assert ls.max_out_err <= OUT_TOL
+
+
 def test_full_size_llama_shape(lib):
     """The 32K Llama-3-8B-shaped workload in the bench's launch configuration (batch 1, 8 KV heads),
     two layers, 16 steps and 2 routing events, every output and window compared."""
