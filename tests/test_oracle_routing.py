@@ -227,3 +227,45 @@ def test_promoted_window_holds_the_dequantised_copy():
             Kh, Vh = led.dequantize()
             assert np.array_equal(K, Kh) and np.array_equal(V, Vh)
     del rng
+
+
+def _golden_events():
+    import os
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "routing_events.txt")
+    rows = []
+    for ln in open(path):
+        if ln.strip() and not ln.startswith("#"):
+            f = [p.split() for p in ln.split("|")]
+            rows.append(dict(event=int(f[0][0]), T=int(f[1][0]), scores=[float(x) for x in f[2]], tier=f[3],
+                             fslot=f[4], lslot=f[5], ledger=f[6], counters=[int(x) for x in f[7]]))
+    return rows
+
+
+def test_routing_events_worked_by_hand():
+    """Tiers, F slots, ledger slots and statuses, and transition counters of three routing events worked
+    by hand (tests/golden/routing_events.txt; QEvict §4.3 Eq. (4)-(6), App. A Algorithm 1)."""
+    rows = _golden_events()
+    u, k = _fresh_unit(6, 2, 2, seed=3)
+    P = u.cfg.prompt_len
+    assert P == 30 and O.prompt_windows(u.cfg) == 7
+    rng = np.random.default_rng(4)
+    tier_of = {O.FULL: "F", O.QUANT: "Q", O.EVICTED: "E", O.LOCAL: "L"}
+    for row in rows:
+        if row["event"] == 0:
+            before = u.counters.copy()
+            u.prefill_route(k, _bf16(rng, k.shape), np.array(row["scores"]))
+        else:
+            for _ in range(u.cfg.omega):
+                u.decode_step(_bf16(rng, (u.cfg.h_q, u.cfg.d_head)), _bf16(rng, (u.cfg.h_kv, u.cfg.d_head)),
+                              _bf16(rng, (u.cfg.h_kv, u.cfg.d_head)))
+            before = u.counters.copy()
+            scores = np.zeros(len(u.S))
+            scores[:7] = row["scores"]
+            u.route(scores)
+        assert u.T == row["T"]
+        assert [tier_of[int(z)] for z in u.z[:7]] == row["tier"]
+        assert [str(u.f_slot[w]) if w in u.f_slot else "-" for w in range(7)] == row["fslot"]
+        assert [str(u.ledger[w].slot) if w in u.ledger else "-" for w in range(7)] == row["lslot"]
+        st = {O.ACTIVE: "a", O.DORMANT: "d"}
+        assert [st[u.ledger[w].status] if w in u.ledger else "-" for w in range(7)] == row["ledger"]
+        assert (u.counters - before).tolist() == row["counters"]
