@@ -122,3 +122,13 @@ def test_budget_against_hand_worked_capacities(cpu_lib, row):
     for got in (ob, b):
         assert (got.full_bytes, got.b_total, got.b_sink, got.b_local, got.b_hist, got.payload, got.m_q, got.m_f,
                 got.k_f, got.k_q) == want
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch):
+    """No CPU fallback: without the built library every entry point's loader raises."""
+    monkeypatch.setattr(binding, "LIB_PATH", os.path.join(ROOT, "no_such_dir", "libqevict.so"))
+    monkeypatch.setattr(binding, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        binding.load()
+    with pytest.raises(RuntimeError, match="missing"):
+        binding.budget(binding.make_config(synth.workload("tiny_4k")))
