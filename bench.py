@@ -44,7 +44,6 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--cpu-sample-steps", type=int, default=8)
     ap.add_argument("--diag", type=int, default=0,
                     help="also run N routing events with the routing diagnostics against a FullKV cache")
     ap.add_argument("--int4", action="store_true", help="the INT4 / 64-token-window format of the workload")
@@ -152,59 +151,165 @@ class ClockSampler:
 
 # --------------------------------------------------------------------------------------- CPU oracle
 
-def oracle_sample(wl_name: str, steps: int, layers: int = 1) -> dict:
-    """Times the CPU oracle on a bounded sample of the workload: one (sequence, layer) unit, its
-    prefill routing (untimed), `steps` decode steps and one routing event; scaled to whole steps
-    (every layer and sequence, routing amortised over Omega)."""
+ORACLE_THREADS_ENV = {"OMP_NUM_THREADS": "1", "OPENBLAS_NUM_THREADS": "1", "MKL_NUM_THREADS": "1",
+                      "CUDA_VISIBLE_DEVICES": ""}
+
+
+def _oracle_worker(conn, wl_name, units, n_steps, seed):
+    """One oracle process: owns the (layer, sequence) units given, prefill-routes them on seeded random
+    prompt scores (the routing cost does not depend on their values; 32K-prompt attention on host
+    cores is out of reach), then runs one decode step of every unit per request, with the routing
+    event every Omega steps, and answers with its busy time."""
     import numpy as np
     from oracle import qevict_oracle as O
     from recoverable_quantized_kv_gb300 import synth
     wl = synth.workload(wl_name)
-    cfg = O.Config.from_obj(wl)
-    rng = np.random.default_rng(12345)
-    t_dec, t_route = [], []
-    for layer in range(layers):
+    cfg = O.Config.from_obj(wl, max_len=wl.prompt_len + n_steps + wl.omega)
+    rng = np.random.default_rng(seed)
+    state = []
+    for layer, b in units:
         u = O.Unit(cfg)
-        p = synth.prompt_inputs(wl, 0, layer, with_queries=False)
-        s0 = rng.random(O.prompt_windows(cfg))          # scores are inputs here: timing does not depend on them
-        u.prefill_route(p["k"].float().numpy(), p["v"].float().numpy(), s0)
-        dec = synth.decode_inputs(wl, 0, layer, steps=max(steps, wl.omega))
-        for s in range(steps):
-            t0 = time.perf_counter()
-            u.decode_step(dec["q"][s].float().numpy(), dec["k"][s].float().numpy(), dec["v"][s].float().numpy())
-            t_dec.append(time.perf_counter() - t0)
-        for s in range(steps, wl.omega):
-            u.decode_step(dec["q"][s].float().numpy(), dec["k"][s].float().numpy(), dec["v"][s].float().numpy())
+        p = synth.prompt_inputs(wl, b, layer, with_queries=False)
+        u.prefill_route(p["k"].float().numpy(), p["v"].float().numpy(), rng.random(O.prompt_windows(cfg)))
+        d = synth.decode_inputs(wl, b, layer, steps=n_steps)
+        state.append((u, d["q"].float().numpy(), d["k"].float().numpy(), d["v"].float().numpy()))
+    conn.send("ready")
+    while True:
+        s = conn.recv()
+        if s is None:
+            break
         t0 = time.perf_counter()
-        u.route()
-        t_route.append(time.perf_counter() - t0)
-    td, tr = statistics.mean(t_dec), statistics.mean(t_route)
-    per_step = wl.n_layers * wl.batch * (td + tr / wl.omega)
-    return {"value": 1.0 / per_step, "unit": "steps/s", "layer_step_s": td, "route_s": tr,
-            "sample": f"oracle on {layers} (sequence, layer) unit(s) of {wl_name}: {steps} decode steps + 1 routing "
-                      f"event timed, scaled x{wl.n_layers * wl.batch} units with routing amortised over Omega="
-                      f"{wl.omega}"}
+        for u, q, k, v in state:
+            u.decode_step(q[s], k[s], v[s])
+            if (s + 1) % wl.omega == 0:
+                u.route()
+        conn.send(time.perf_counter() - t0)
+    conn.close()
+
+
+class OraclePool:
+    """Oracle processes (spawned, one BLAS thread each) that decode the units of a workload in
+    lockstep: a step is one decode step of every unit, the routing event included every Omega
+    steps.  Units are dealt round-robin to the processes."""
+
+    def __init__(self, wl_name, units, n_proc, n_steps, seed=12345):
+        import multiprocessing as mp
+        saved = {k: os.environ.get(k) for k in ORACLE_THREADS_ENV}
+        os.environ.update(ORACLE_THREADS_ENV)
+        try:
+            ctx = mp.get_context("spawn")
+            self.conns, self.procs = [], []
+            for i in range(n_proc):
+                a, b = ctx.Pipe()
+                pr = ctx.Process(target=_oracle_worker, args=(b, wl_name, units[i::n_proc], n_steps, seed + i),
+                                 daemon=True)
+                pr.start()
+                self.conns.append(a)
+                self.procs.append(pr)
+        finally:
+            for k, v in saved.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        for c in self.conns:
+            assert c.recv() == "ready"
+
+    def step(self, s):
+        t0 = time.perf_counter()
+        for c in self.conns:
+            c.send(s)
+        busy = [c.recv() for c in self.conns]
+        return time.perf_counter() - t0, busy
+
+    def close(self):
+        for c in self.conns:
+            c.send(None)
+        for pr in self.procs:
+            pr.join(timeout=30)
+
+
+def oracle_config1_full():
+    """The tiny workload in full on one core: fp64 prompt attention for the scores, prefill routing,
+    64 decode steps with 8 routing events (the oracle as it stands, one BLAS thread)."""
+    import numpy as np
+    from oracle import qevict_oracle as O
+    from recoverable_quantized_kv_gb300 import synth
+    wl = synth.workload("tiny_4k")
+    cfg = O.Config.from_obj(wl)
+    u = O.Unit(cfg)
+    p = synth.prompt_inputs(wl, 0, 0)
+    dec = synth.decode_inputs(wl, 0, 0)
+    t0 = time.perf_counter()
+    s0 = O.prefill_scores(p["q"].float().numpy(), p["k"].float().numpy(), cfg)
+    u.prefill_route(p["k"].float().numpy(), p["v"].float().numpy(), s0)
+    t1 = time.perf_counter()
+    for s in range(wl.steps):
+        u.decode_step(dec["q"][s].float().numpy(), dec["k"][s].float().numpy(), dec["v"][s].float().numpy())
+        if (s + 1) % wl.omega == 0:
+            u.route()
+    t2 = time.perf_counter()
+    return {"workload": "tiny_4k", "steps": wl.steps, "routing_events": wl.steps // wl.omega,
+            "value": wl.steps / (t2 - t1), "unit": "steps/s", "prefill_s": round(t1 - t0, 3), "cores": 1}
 
 
 def run_oracle_child(args):
     """Runs in a subprocess with one BLAS/OpenMP thread so `cores` is exact."""
-    r = oracle_sample(args.workload, args.cpu_sample_steps)
-    print(json.dumps(r))
+    if args.oracle_child == "config1":
+        print(json.dumps(oracle_config1_full()))
 
 
-def cpu_baseline(args, steps):
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
+def oracle_steps(wl_name, n_units, n_proc, n_steps, warmup=0):
+    """Steps/s of the oracle over the first n_units (layer, sequence) units of the workload, on n_proc
+    processes: `warmup` untimed steps, then n_steps timed steps (wall clock of each lockstep step)."""
+    from recoverable_quantized_kv_gb300 import synth
+    wl = synth.workload(wl_name)
+    units = [(l, b) for l in range(wl.n_layers) for b in range(wl.batch)][:n_units]
+    pool = OraclePool(wl_name, units, n_proc, warmup + n_steps)
+    try:
+        walls = []
+        for s in range(warmup + n_steps):
+            wall, _ = pool.step(s)
+            if s >= warmup:
+                walls.append(wall)
+    finally:
+        pool.close()
+    return sum(walls), wl
+
+
+def cpu_baseline(args):
+    """The oracle, as it stands, on the host cores of this machine (QEvict config-2 workload and the tiny
+    workload): config 1 in full on one core; config 2 over every one of its 32 (layer, sequence)
+    units on all cores (one process per core, one BLAS thread each), and on one core over a 2-unit
+    sample scaled to the 32 units.  16 decode steps each, 2 routing events."""
+    cores = len(os.sched_getaffinity(0))
     t0 = time.time()
-    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--workload", args.workload,
-                        "--cpu-sample-steps", str(steps), "--oracle-child", "1"], capture_output=True, text=True,
-                       env=env, timeout=1800)
-    if r.returncode != 0:
-        return {"value": None, "unit": "steps/s", "cores": 1, "kind": "oracle", "error": r.stderr[-400:]}
-    d = json.loads(r.stdout.strip().splitlines()[-1])
-    d.update({"cores": 1, "kind": "oracle", "cpu": _cpu_model(), "host_cores": len(os.sched_getaffinity(0)),
-              "wall_s": round(time.time() - t0, 1)})
-    return d
+    out = {"kind": "oracle", "unit": "steps/s", "cpu": _cpu_model(), "host_cores": cores}
+    try:
+        env = dict(os.environ, **ORACLE_THREADS_ENV)
+        r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--oracle-child", "config1"],
+                           capture_output=True, text=True, env=env, timeout=600)
+        out["config1_full_1core"] = json.loads(r.stdout.strip().splitlines()[-1]) if r.returncode == 0 else \
+            {"error": r.stderr[-300:]}
+        from recoverable_quantized_kv_gb300 import synth
+        wl = synth.workload(args.workload)
+        U, steps = wl.n_layers * wl.batch, 16
+        t_all, _ = oracle_steps(args.workload, U, min(cores, U), steps)
+        t_one, _ = oracle_steps(args.workload, 2, 1, steps)
+        out.update({
+            "value": steps / t_all, "cores": min(cores, U),
+            "sample": f"oracle on all {U} (layer, sequence) units of {wl.name}, {steps} decode steps with "
+                      f"{steps // wl.omega} routing events, {min(cores, U)} processes x 1 BLAS thread; prompt "
+                      f"scores seeded random (prefill excluded)",
+            "config2_all_units_allcores": {"value": steps / t_all, "cores": min(cores, U), "units": U,
+                                           "steps": steps, "measured": True},
+            "config2_1core": {"value": steps / (t_one * U / 2), "cores": 1, "units_timed": 2, "steps": steps,
+                              "measured": False, "note": f"2 units timed on one core, scaled to {U} units"},
+        })
+    except Exception as e:   # the GPU figures stand on their own; report why the baseline is missing
+        out.update({"value": None, "cores": cores, "error": repr(e)[-300:]})
+    out["wall_s"] = round(time.time() - t0, 1)
+    return out
 
 
 def _cpu_model():
@@ -287,8 +392,10 @@ def run_gpu(args, rank, world):
     K, Wm = args.steps, args.warmup
     Om = wl.omega
     K_kern = 2 * Om
+    R_roof = 7                                       # replays of the steady-state graph
     K_e2e = 0 if args.no_e2e else K
-    total = Wm + (Om - 1) + K_kern + Om + K + K_e2e   # (Om - 1): steps that realign to a routing event
+    # (Om - 1) per phase: steps that realign the phase to a routing event
+    total = Wm + 4 * (Om - 1) + K_kern + R_roof * Om + K + 2 * K_e2e
     steps_cap = max(wl.steps, int(math.ceil(total / Om) * Om) + Om)
     cfg = binding.make_config(wl, max_len=wl.prompt_len + steps_cap)
     cache = binding.Cache(cfg, device=dev)
@@ -331,8 +438,10 @@ def run_gpu(args, rank, world):
     tpeak, tpeak_kind = measured_tensor_peak()
     prefill_scores = {"ms_per_layer": pre_ms, "tflops": pre_tf, "peak_tflops": tpeak, "frac": pre_tf / tpeak,
                       "flops_per_layer": pre_flops,
-                      "note": "causal FLOPs of both passes (row log-sum-exp, column sums), tcgen05.mma M=N=128 bf16 "
-                              "with TMA tensor-map loads; "
+                      "tflops_single_product": pre_tf / 2, "frac_single_product": pre_tf / 2 / tpeak,
+                      "note": "tflops/frac count the causal q.k products of both passes (row log-sum-exp, then "
+                              "column sums, which recomputes q.k); *_single_product count the one causal product "
+                              "the scores need.  tcgen05.mma M=N=128 bf16 with TMA tensor-map loads; "
                               f"peak = {tpeak_kind} dense bf16 burst"}
     del pq, pk, ps0
 
@@ -383,12 +492,22 @@ def run_gpu(args, rank, world):
     # ---- event-bracketed pass: decode kernel duration and the algorithmic bytes of each launch
     kern_ms, kern_bytes, step_bytes = [], [], []
     c0 = cache.counters()
+    per_event = []          # tier transitions of each routing event (counter deltas, all units)
+    last_ctr = [c0]
+
+    def record_event():
+        cur = cache.counters()
+        per_event.append({k: cur[k] - last_ctr[0][k] for k in cur})
+        last_ctr[0] = cur
+
     for _ in range(K_kern):
         metas = read_meta()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
         i = state["step"]
         one_step(i, events=ev)
         torch.cuda.synchronize()
+        if state["step"] % Om == 0:
+            record_event()
         sb = 0
         for layer in range(L):
             by = 0
@@ -409,7 +528,8 @@ def run_gpu(args, rank, world):
 
     # ---- steady-state decode launches: the Omega decode steps up to the next routing event (all
     # layers, no routing between them) captured in one CUDA graph and replayed between two events,
-    # so consecutive launches overlap as they do inside a step; the routing event then runs untimed
+    # so consecutive launches overlap as they do inside a step; after each replay the host mirror of
+    # the cache is resynchronised and the routing event runs untimed.  R_roof replays: median, spread
     assert state["step"] % Om == 0
     gd = torch.cuda.CUDAGraph()
     with torch.cuda.graph(gd, stream=stream):
@@ -418,17 +538,30 @@ def run_gpu(args, rank, world):
             for layer in range(L):
                 cache.decode_step(layer, qs[i][layer], ks[i][layer], vs[i][layer], outs[layer], stream)
     torch.cuda.synchronize()
-    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    d0.record(stream)
-    gd.replay()
-    d1.record(stream)
-    torch.cuda.synchronize()
-    steady_ms = d0.elapsed_time(d1) / (Om * L)
-    state["step"] += Om
-    cache.route(stream)
-    torch.cuda.synchronize()
+    replay_us = []
+    for _ in range(R_roof):
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        gd.replay()
+        d1.record(stream)
+        torch.cuda.synchronize()
+        replay_us.append(d0.elapsed_time(d1) * 1e3 / (Om * L))
+        cache.check(stream)          # the host mirror learns the Omega steps the replay took
+        cache.route(stream)
+        state["step"] += Om
+        torch.cuda.synchronize()
+        record_event()
+    steady_ms = statistics.median(replay_us) / 1e3
+
+    def align_end(n):
+        """Untimed steps until a run of n more steps ends on a routing event, so a timed run holds
+        ceil(n / Omega) events (never fewer than its share)."""
+        while (state["step"] + n) % Om:
+            one_step(state["step"])
+        torch.cuda.synchronize()
 
     # ---- timed region: exactly K steps, captured once in a CUDA graph and replayed once
+    align_end(K)
     launches_before = state["launches"]
     g = torch.cuda.CUDAGraph()
     first = state["step"]
@@ -436,6 +569,7 @@ def run_gpu(args, rank, world):
         for i in range(K):
             one_step(first + i)
     timed_launches = state["launches"] - launches_before
+    timed_events = sum(1 for i in range(first, first + K) if (i + 1) % Om == 0)
     torch.cuda.synchronize()
     sampler = ClockSampler(_bus_id(torch, dev))
     if world > 1:
@@ -456,6 +590,7 @@ def run_gpu(args, rank, world):
     # ---- e2e: inputs from pinned host memory, outputs back to pinned host memory, every step
     e2e = None
     if K_e2e:
+        align_end(K_e2e)
         hq = torch.empty(K_e2e, L, B, wl.h_q, D, dtype=torch.bfloat16, pin_memory=True)
         hk = torch.empty(K_e2e, L, B, wl.h_kv, D, dtype=torch.bfloat16, pin_memory=True)
         hv = torch.empty_like(hk, pin_memory=True)
@@ -483,9 +618,36 @@ def run_gpu(args, rank, world):
         torch.cuda.synchronize()
         ms_e2e = max_over_ranks(f0.elapsed_time(f1), world, dev)
         in_bytes = (hq[0].numel() + hk[0].numel() + hv[0].numel()) * 2
-        e2e = {"value": whole_job_rate(world, K_e2e, ms_e2e), "unit": "steps/s", "h2d_bytes_per_step": in_bytes,
-               "d2h_bytes_per_step": ho[0].numel() * 2, "ms_per_step": ms_e2e / K_e2e,
-               "timing": "CUDA graph of the C-ABI calls with pinned-host copies, CUDA events"}
+        state["step"] = s_e + K_e2e
+        cache.check(stream)
+        # the same K steps as eager calls: every C-ABI call made from Python as the step runs, so the
+        # host cost of the calls (ctypes, argument checks, launches) is inside the timed region too
+        align_end(K_e2e)
+        s_e = state["step"]
+        hq.copy_(qs[s_e:s_e + K_e2e].cpu())
+        hk.copy_(ks[s_e:s_e + K_e2e].cpu())
+        hv.copy_(vs[s_e:s_e + K_e2e].cpu())
+        torch.cuda.synchronize()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for i in range(K_e2e):
+            dq.copy_(hq[i], non_blocking=True)
+            dk.copy_(hk[i], non_blocking=True)
+            dv.copy_(hv[i], non_blocking=True)
+            one_step(s_e + i, dq, dk, dv, outs)
+            ho[i].copy_(outs, non_blocking=True)
+        f1.record(stream)
+        torch.cuda.synchronize()
+        ms_eager = max_over_ranks(f0.elapsed_time(f1), world, dev)
+        e2e = {"value": whole_job_rate(world, K_e2e, ms_eager), "unit": "steps/s", "h2d_bytes_per_step": in_bytes,
+               "d2h_bytes_per_step": ho[0].numel() * 2, "ms_per_step": ms_eager / K_e2e,
+               "routing_events": sum(1 for i in range(K_e2e) if (i + 1) % Om == 0),
+               "timing": "eager: every step's C-ABI calls made from Python as the GPU runs them, each step's "
+                         "inputs copied from pinned host memory and its outputs copied back, between CUDA "
+                         "events on the launching stream (the host cost of the calls is inside)",
+               "graph": {"value": whole_job_rate(world, K_e2e, ms_e2e), "ms_per_step": ms_e2e / K_e2e,
+                         "timing": "the same calls and copies captured in one CUDA graph and replayed between "
+                                   "CUDA events (the host cost of the calls is outside)"}}
         cache.check(stream)
     clocks = sampler.summary()
     sampler.close()
@@ -514,14 +676,24 @@ def run_gpu(args, rank, world):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic_from_profile(sha), "peak_kind": f"{peak_kind} copy bandwidth",
                      "kernel": "decode_kernel", "bytes_per_launch": bytes_per_launch, "avg_launch_us": steady_ms * 1e3,
-                     "launches_timed": Om * L,
-                     "timing": "CUDA graph of Omega decode-only steps (all layers) between two CUDA events on "
-                               "the launching stream; consecutive launches overlap as inside a step",
+                     "launches_timed": Om * L * R_roof,
+                     "avg_launch_us_replays": [round(x, 3) for x in replay_us],
+                     "avg_launch_us_spread": [round(min(replay_us), 3), round(max(replay_us), 3)],
+                     "timing": f"median over {R_roof} replays of a CUDA graph of Omega decode-only steps (all "
+                               "layers) between two CUDA events on the launching stream; consecutive launches "
+                               "overlap as inside a step",
                      "isolated_launch_us": isolated_ms * 1e3,
                      "isolated_timing": f"{len(kern_ms)} launches, each alone between two events",
                      "kernel_source_sha": sha,
                      "vs_8tbs": achieved / 8000.0},
         "gpu_launches": timed_launches,
+        "routing_events_timed": timed_events,
+        "transitions_per_event": {
+            "events": len(per_event), "units": L * B,
+            "mean": {k: statistics.mean(e[k] for e in per_event) for k in per_event[0]},
+            "max": {k: max(e[k] for e in per_event) for k in per_event[0]},
+            "note": "tier transitions per routing event over all (layer, sequence) units, from counter deltas "
+                    "of the untimed events (QEvict App. K Table 18's promotion counts)"},
         "clocks": clocks,
         "prefill_s": round(t_pre, 2), "prefill_scores": prefill_scores,
     }
@@ -602,46 +774,30 @@ def _bus_id(torch, dev):
 
 
 def run_reference(args, rank, world):
-    """The CPU oracle as the reference arm: K decode steps of one (sequence, layer) unit after W
-    warm-up steps, routing every Omega steps, each step scaled to every layer and sequence."""
+    """The CPU oracle as the reference arm: every (layer, sequence) unit of the workload decoded in
+    lockstep on the host cores (one process per core, one BLAS thread each), W warm-up steps then K
+    timed steps, each timed step one decode step of every unit with the routing event every Omega
+    steps.  Rank 0 only."""
     if rank != 0:
         return None
-    import numpy as np
-    from oracle import qevict_oracle as O
     from recoverable_quantized_kv_gb300 import synth
     wl = synth.workload(args.workload)
-    cfg = O.Config.from_obj(wl, max_len=wl.prompt_len + args.warmup + args.steps + wl.omega)
-    u = O.Unit(cfg)
-    p = synth.prompt_inputs(wl, 0, 0, with_queries=False)
-    u.prefill_route(p["k"].float().numpy(), p["v"].float().numpy(),
-                    np.random.default_rng(12345).random(O.prompt_windows(cfg)))
-    dec = synth.decode_inputs(wl, 0, 0, steps=args.warmup + args.steps)
-    t = 0.0
-    for s in range(args.warmup + args.steps):
-        t0 = time.perf_counter()
-        u.decode_step(dec["q"][s].float().numpy(), dec["k"][s].float().numpy(), dec["v"][s].float().numpy())
-        if (s + 1) % wl.omega == 0:
-            u.route()
-        if s >= args.warmup:
-            t += time.perf_counter() - t0
-    per_step = t / args.steps * wl.n_layers * wl.batch
-    value = 1.0 / per_step
+    cores = len(os.sched_getaffinity(0))
+    U = wl.n_layers * wl.batch
+    n_proc = min(cores, U)
+    t_start = time.time()
+    t, _ = oracle_steps(args.workload, U, n_proc, args.steps, warmup=args.warmup)
+    value = args.steps / t
+    sample = (f"oracle on all {U} (layer, sequence) units of {wl.name} per step, {n_proc} processes x 1 BLAS "
+              f"thread, routing every {wl.omega} steps; prompt scores seeded random (prefill excluded)")
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": t / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": wl.name, "batch": wl.batch, "layers": wl.n_layers, "prompt_len": wl.prompt_len},
-            "cpu_baseline": {"value": value, "unit": "steps/s", "kind": "oracle",
-                             "cores": _threads_hint(), "cpu": _cpu_model(),
-                             "sample": f"oracle, one (sequence, layer) unit per step of {wl.name}, routing every "
-                                       f"{wl.omega} steps, scaled x{wl.n_layers * wl.batch} units"},
-            "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-
-
-def _threads_hint():
-    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS"):
-        if os.environ.get(k):
-            return int(os.environ[k])
-    return len(os.sched_getaffinity(0))
+            "cpu_baseline": {"value": value, "unit": "steps/s", "kind": "oracle", "cores": n_proc, "cpu": _cpu_model(),
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": round(time.time() - t_start, 1)}
 
 
 def main():
@@ -664,7 +820,7 @@ def main():
     res = run_gpu(args, rank, world)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_baseline(args, args.cpu_sample_steps)
+            res["cpu_baseline"] = cpu_baseline(args)
         print(json.dumps(res))
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -23,7 +23,10 @@
  *     QEVICT_ESCHEDULE for a routing call off the Omega cadence, QEVICT_ECUDA
  *     when a launch fails, QEVICT_EDEVICE when a kernel recorded a fault in the
  *     device status word (read by qevict_read_counters / qevict_check).  On an
- *     error nothing is enqueued unless stated.
+ *     error nothing is enqueued unless stated.  Bits of the status word: 1 a
+ *     bounded wait ran out, 2 a routing event found too few free slots, 4 a
+ *     kernel found the cache state inconsistent; they stay set until an earlier
+ *     export is imported or the cache is re-initialised.
  *   - Tensors are dense, row-major, bf16 (uint16 storage) unless stated.
  *   - One cache serves `batch` sequences that decode in lockstep and all
  *     `n_layers` layers; every (sequence, layer) pair is one independent "unit".
@@ -245,6 +248,15 @@ qevict_status qevict_check(qevict_cache *cache, qevict_stream_t stream);
  * cache is re-initialised.  Returns QEVICT_ECUDA if the launch fails. */
 qevict_status qevict_selftest_wait(qevict_cache *cache, qevict_stream_t stream);
 
+/* Test hook for the router's slot-exhaustion guard (QEvict App. A Algorithm 1, slot allocation of
+ * newcomers to F and to the ledger).  With cap >= 0, every later routing event sees at most `cap`
+ * free F slots and at most `cap` free ledger slots; cap = -1 (the default) removes the limit.  Real
+ * pools cannot run out (a newcomer to F or Q always finds a slot released for it), so the guard is
+ * reachable only this way.  An event whose newcomers need more slots than it sees sets bit 2 of
+ * the device status word (qevict_check then returns QEVICT_EDEVICE) and changes no tier, slot,
+ * table or ledger; its pending window masses are still absorbed into the scores.  Host only: nothing is enqueued.  QEVICT_EINVAL if cap < -1. */
+qevict_status qevict_debug_cap_free_slots(qevict_cache *cache, int32_t cap);
+
 /* Scratch size, in floats, of qevict_prefill_scores_noalloc: 2 * batch * h_q * prompt_len must not
  * exceed it (2 Mi floats = 8 MiB, e.g. 32 query heads x 32768 prompt tokens for one sequence). */
 #define QEVICT_NOALLOC_SCRATCH_FLOATS (2LL * 1024 * 1024)
@@ -256,15 +268,26 @@ qevict_status qevict_selftest_wait(qevict_cache *cache, qevict_stream_t stream);
  * input and output buffers.  Its scratch is a fixed 8 MiB array inside the library image, held on
  * every GPU that loads the library until the process exits; nothing is allocated per call.
  *   q_prompt [batch][prompt_len][h_q][128], k_prompt [batch][prompt_len][h_kv][128] bf16 (device);
- *   s0_out [batch][ceil((prompt_len - n_sink) / window)] fp32 (device).  q_prompt, k_prompt 16-byte aligned.
- * Errors: QEVICT_EINVAL for bad sizes or NULL pointers; QEVICT_ENOMEM when
+ *   s0_out [batch][ceil((prompt_len - n_sink) / window)] fp32 (device).  q_prompt, k_prompt 16-byte
+ *   aligned, s0_out 4-byte aligned.
+ * Errors: QEVICT_EINVAL for bad sizes, NULL or misaligned pointers; QEVICT_ENOMEM when
  * 2 * batch * h_q * prompt_len > QEVICT_NOALLOC_SCRATCH_FLOATS (nothing is enqueued then).
+ * Device failures (a bounded wait of the scoring kernels that ran out) are not returned by this
+ * asynchronous call: they set a device status word of this entry point, which
+ * qevict_prefill_scores_noalloc_status reads and clears.
  * The first call on a device looks up the scratch address with that device current; make that first
  * call before capturing a stream.  All calls share the scratch: calls that can overlap on the GPU
  * (e.g. on two streams) race and must be ordered by the caller. */
 qevict_status qevict_prefill_scores_noalloc(int32_t batch, int32_t prompt_len, int32_t h_q, int32_t h_kv,
                                             int32_t n_sink, int32_t window, const void *q_prompt,
                                             const void *k_prompt, float *s0_out, qevict_stream_t stream);
+
+/* The device status word of qevict_prefill_scores_noalloc on the current device: synchronises
+ * `stream`, reads the word and clears it (a device-to-host copy and a memset of the word; nothing is
+ * allocated).  Returns QEVICT_EDEVICE if any call since the last read recorded a device failure,
+ * whose s0_out must then be discarded; QEVICT_OK otherwise; QEVICT_ECUDA if the copy fails.  The
+ * word is sticky until read: a failure of an earlier call is reported even after later calls. */
+qevict_status qevict_prefill_scores_noalloc_status(qevict_stream_t stream);
 
 /* Device views of one unit's cache tuple, QEvict §4.1 Eq. (2): C_t = (S, L_t, F_t, Q_t, E_t) of
  * (layer, seq).  Each pointer is the unit's region inside the arena, with the layout documented

@@ -104,6 +104,8 @@ def load() -> ctypes.CDLL:
         "qevict_selftest_wait": [P, P],
         "qevict_destroy": [P],
         "qevict_prefill_scores_noalloc": [I32, I32, I32, I32, I32, I32, P, P, P, P],
+        "qevict_prefill_scores_noalloc_status": [P],
+        "qevict_debug_cap_free_slots": [P, I32],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -123,7 +125,7 @@ def exported_symbols():
             "qevict_prefill_scores_noalloc", "qevict_flush_scores", "qevict_get_tuple", "qevict_export_bytes",
             "qevict_export_state", "qevict_import_state", "qevict_set_rope_table", "qevict_diag_bytes",
             "qevict_diag_init", "qevict_diag_route", "qevict_diag_read", "qevict_diag_destroy",
-            "qevict_selftest_wait"]
+            "qevict_selftest_wait", "qevict_prefill_scores_noalloc_status", "qevict_debug_cap_free_slots"]
 
 
 def _check(status: int, where: str):
@@ -173,6 +175,11 @@ def prefill_scores_noalloc(batch, prompt_len, h_q, h_kv, n_sink, window, q_promp
     _check(load().qevict_prefill_scores_noalloc(batch, prompt_len, h_q, h_kv, n_sink, window, _ptr(q_prompt),
                                                 _ptr(k_prompt), _ptr(s0_out), _stream(stream)),
            "qevict_prefill_scores_noalloc")
+
+
+def prefill_scores_noalloc_status(stream=None):
+    """Reads and clears the allocation-free entry point's device status word (raises EDEVICE if set)."""
+    _check(load().qevict_prefill_scores_noalloc_status(_stream(stream)), "qevict_prefill_scores_noalloc_status")
 
 
 class Cache:
@@ -266,6 +273,10 @@ class Cache:
     def selftest_wait(self, stream=None):
         """Enqueue the bounded-wait self-test: a wait that runs out and records a timeout."""
         _check(load().qevict_selftest_wait(self.handle, _stream(stream)), "qevict_selftest_wait")
+
+    def debug_cap_free_slots(self, cap: int):
+        """Routing events see at most `cap` free F / ledger slots (-1: no cap); a test hook."""
+        _check(load().qevict_debug_cap_free_slots(self.handle, cap), "qevict_debug_cap_free_slots")
 
     # ---- tensor views of the cache tuple inside the arena (read-only use in tests)
     def region(self, name: str, unit: int, nbytes: int):

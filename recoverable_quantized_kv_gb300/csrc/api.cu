@@ -215,6 +215,7 @@ void make_plan(const qevict_config *c, const qevict_budget_info *b, Plan *p) {
   C.decay = c->decay == 0.f ? 0.99f : c->decay;
   C.pnorm = c->pnorm == 0.f ? 3.0f : c->pnorm;
   C.rope = c->rope;
+  C.slot_cap = -1;
 }
 
 qevict_status cuda_status(cudaError_t e) { return e == cudaSuccess ? QEVICT_OK : QEVICT_ECUDA; }
@@ -255,6 +256,7 @@ qevict_status qevict_init_cache(const qevict_config *cfg, void *d_arena, size_t 
   c->lay = p.lay;
   c->dev = p.dev;
   c->dev.arena = static_cast<uint8_t *>(d_arena);
+  c->dev.status_word = reinterpret_cast<int *>(c->dev.arena + c->dev.off_status);
   c->off_s0buf = p.off_s0buf;
   c->t_host.assign(cfg->n_layers, 0);
   c->prefilled.assign(cfg->n_layers, 0);
@@ -424,6 +426,12 @@ qevict_status qevict_check(qevict_cache *cache, qevict_stream_t stream) {
       cache->routes_done = m[(size_t)l * qv::META_INTS + qv::M_NEVENT];
     }
   return st;
+}
+
+qevict_status qevict_debug_cap_free_slots(qevict_cache *cache, int32_t cap) {
+  if (!cache || cap < -1) return QEVICT_EINVAL;
+  cache->dev.slot_cap = cap;
+  return QEVICT_OK;
 }
 
 qevict_status qevict_selftest_wait(qevict_cache *cache, qevict_stream_t stream) {

@@ -26,7 +26,7 @@ struct CacheDev {
   int64_t off_mtask, st_mtask;     // int4 promote/copy tasks [n_windows]
   // global regions
   int64_t off_counters;            // int64 [U][N_COUNTERS]
-  int64_t off_status;              // int32
+  int64_t off_status;              // int32, inside the arena (status_word points at it for a cache)
   int64_t off_splitctr;            // uint32 [L][B][h_kv]
   int64_t off_thead;               // int32 [L][B][h_kv] tokens cached, one copy per KV head: the decode
                                    // CTAs of a head read theirs, its last CTA advances it
@@ -45,6 +45,9 @@ struct CacheDev {
   int ranker, no_promotion;
   float decay, pnorm;
   int rope;                        // 1: Quantized keys are kept before RoPE
+  int slot_cap;                    // >= 0: routing sees at most this many free F / ledger slots (a
+                                   // host-set test cap that makes the slot-exhaustion guard reachable)
+  int *status_word;                // device status word every bounded wait and guard reports to
 
   // Stable index of a window's mass record between two routing events: 1 + i for the i-th recent
   // window from the first unrouted one, then the Full table entries, then the Quantized ones.
@@ -56,7 +59,7 @@ struct CacheDev {
     return reinterpret_cast<T *>(arena + off + st * (int64_t)u);
   }
   __host__ __device__ const float *rope_tab() const { return reinterpret_cast<const float *>(arena + off_rope); }
-  __host__ __device__ int *status() const { return reinterpret_cast<int *>(arena + off_status); }
+  __host__ __device__ int *status() const { return status_word; }
 };
 
 constexpr int PART_FLOATS = 16 + 8 * 128;   // m[8], l[8], O[8][128] per split

@@ -17,6 +17,7 @@
 // dequantised keys to their positions in registers before the key MMAs.
 #include "cache_dev.cuh"
 #include "common.cuh"
+#include "smem_optin.h"
 
 namespace qv {
 
@@ -975,16 +976,9 @@ template <int W, int BITS, bool ROPE>
 static cudaError_t launch_decode_fmt(const CacheDev &C, const DecodeIO &io, cudaStream_t stream) {
   using Dg = DecGeo<W, BITS, ROPE>;
   auto kern = decode_kernel<W, BITS, ROPE>;
-  static bool attr_set[64] = {};   // per device: the dynamic shared memory opt-in of this kernel
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static SmemOptIn optin;   // per device: the dynamic shared memory opt-in of this kernel
+  const cudaError_t e = optin.ensure(kern, Dg::SMEM);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Dg::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C.n_split, C.h_kv, C.B);
   cfg.blockDim = dim3(DEC_WARPS * 32);

@@ -15,6 +15,7 @@
 // events whose whole horizon was decoded.
 #include "cache_dev.cuh"
 #include "common.cuh"
+#include "smem_optin.h"
 #include "diag_dev.cuh"
 
 namespace qv {
@@ -401,16 +402,9 @@ cudaError_t launch_diag_collect(const CacheDev &R, const DiagDev &Dg, cudaStream
 
 cudaError_t launch_diag_event(const CacheDev &P, const CacheDev &R, const DiagDev &Dg, int e, cudaStream_t s) {
   const size_t smem = (size_t)P.n_windows * 9;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
+  static SmemOptIn optin;
+  const cudaError_t err = optin.ensure(diag_event_kernel, 8192 * 9);
   if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    err = cudaFuncSetAttribute(diag_event_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 8192 * 9);
-    if (err != cudaSuccess) return err;
-    attr_set[dev] = true;
-  }
   diag_event_kernel<<<P.B * P.L, DG_EVENT_THREADS, smem, s>>>(P, R, Dg, e);
   return cudaGetLastError();
 }

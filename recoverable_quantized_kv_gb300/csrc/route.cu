@@ -19,6 +19,7 @@
 // keys back to the pre-RoPE domain at its positions, and move_kernel rotates rebuilt keys forward.
 #include "cache_dev.cuh"
 #include "common.cuh"
+#include "smem_optin.h"
 
 namespace qv {
 
@@ -291,8 +292,11 @@ __global__ void __launch_bounds__(RT_THREADS, 1) route_kernel(const CacheDev C, 
   const int nNeedL = block_exscan(rankL, n_new, wsum);
   // Unreachable with in-range slot ids: a busy F slot belongs to a window that keeps one of the K_f
   // Full places and a newcomer takes another, so nNeedF <= totF; the ledger holds K_f + K_q places the
-  // same way.  Should it ever fire, this event changes no tier, table or slot and migrates nothing.
-  if (nNeedF > totF || nNeedL > totL) {
+  // same way.  A test cap set on the host (slot_cap >= 0) hides free slots so that the guard can be
+  // exercised.  Should it fire, this event changes no tier, table or slot and migrates nothing.
+  const int capF = C.slot_cap >= 0 ? min(totF, C.slot_cap) : totF;
+  const int capL = C.slot_cap >= 0 ? min(totL, C.slot_cap) : totL;
+  if (nNeedF > capF || nNeedL > capL) {
     if (tid == 0) {
       atomicOr(C.status(), QV_ERR_SLOT);
       meta[M_NQUANT] = 0;
@@ -688,15 +692,10 @@ template <int W, int BITS>
 static cudaError_t launch_migrate(const CacheDev &C, const PromptIO &pio, int unit0, int n_units, int mig_blocks,
                                   cudaStream_t s) {
   constexpr int qsm = quant_smem_bytes<W, BITS>();
-  static bool attr_set[64] = {};   // per device: the dynamic shared memory opt-in
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (qsm > 48 * 1024 && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(quant_kernel<W, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, qsm);
+  static SmemOptIn optin;   // per device: the dynamic shared memory opt-in
+  if (qsm > 48 * 1024) {
+    const cudaError_t e = optin.ensure(quant_kernel<W, BITS>, qsm);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
   }
   dim3 grid(mig_blocks, n_units);
   quant_kernel<W, BITS><<<grid, MIG_THREADS, qsm, s>>>(C, pio, unit0);
@@ -706,16 +705,9 @@ static cudaError_t launch_migrate(const CacheDev &C, const PromptIO &pio, int un
 
 cudaError_t launch_route(const CacheDev &C, int unit0, int n_units, const __nv_bfloat16 *kp,
                          const __nv_bfloat16 *vp, int layer, int mig_blocks, cudaStream_t s) {
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static SmemOptIn optin;
+  const cudaError_t e = optin.ensure(route_kernel, route_smem_bytes());
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, route_smem_bytes());
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
   const int prefill = kp != nullptr;
   PromptIO pio{kp, vp, layer};
   route_kernel<<<n_units, RT_THREADS, route_smem_bytes(), s>>>(C, pio, unit0, prefill);

@@ -13,6 +13,7 @@
 
 #include "cache_dev.cuh"
 #include "common.cuh"
+#include "smem_optin.h"
 
 namespace qv {
 
@@ -377,18 +378,10 @@ cudaError_t launch_prefill_scores(const CacheDev &C, const __nv_bfloat16 *q, con
   if (((uintptr_t)q | (uintptr_t)k) & 15) return cudaErrorInvalidValue;   // tensor maps: 16-byte aligned bases
   CUtensorMap tq, tk;
   if (!prompt_map(&tq, q, C.B, P, C.h_q) || !prompt_map(&tk, k, C.B, P, C.h_kv)) return cudaErrorInvalidValue;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static SmemOptIn optin_rows, optin_cols;
+  cudaError_t e = optin_rows.ensure(tc_score_kernel<false>, TC_SMEM);
+  if (e == cudaSuccess) e = optin_cols.ensure(tc_score_kernel<true>, TC_SMEM);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_set[dev]) {
-    e = cudaFuncSetAttribute(tc_score_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(tc_score_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, TC_SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
   int *status = C.status();
   const int nrt = (P + TC_ROWS - 1) / TC_ROWS;
   dim3 grid((nrt + TC_RT - 1) / TC_RT, C.h_q, C.B);

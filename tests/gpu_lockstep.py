@@ -2,9 +2,12 @@
 inputs and compares them step by step.
 
 Tolerances (reading of the stated bar): attention outputs max-abs <= 2e-2 (bf16 outputs); window
-masses and scores relative <= 1e-3 where the value is >= 1e-6 of the largest in the same step
-(else absolute <= 1e-9); tier states, slots, tables, INT2 codes, fp16 parameters and bf16 window
-data bit-exact, with the router of the oracle fed the scores the GPU ranked ("identical scores").
+masses and scores relative <= 1e-3 wherever the value is at least 2^-100 of the largest in the same
+row, else absolute <= 2^-100 of that largest.  The floor only covers values that fp32 cannot carry:
+the kernels' exponentials flush results below 2^-126 of their running maximum to zero, so a window
+whose every probability lies that far below the maximum reads as 0.  Tier states, slots, tables,
+INT2 codes, fp16 parameters and bf16 window data bit-exact, with the router of the oracle fed the
+scores the GPU ranked ("identical scores").
 """
 import numpy as np
 import torch
@@ -15,17 +18,20 @@ from recoverable_quantized_kv_gb300 import binding, synth
 
 OUT_TOL = 2e-2
 REL_TOL = 1e-3
+FLOOR = 2.0 ** -100     # of the row's largest value: below it, values are compared in absolute terms
 
 
-def close_rel(gpu, ref, what, rel=REL_TOL, floor_frac=1e-6, abs_small=1e-9):
+def close_rel(gpu, ref, what, rel=REL_TOL, floor_frac=FLOOR):
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)
-    big = np.abs(ref) >= floor_frac * max(np.abs(ref).max(), 1e-300)
+    if ref.size == 0:
+        return
+    floor = max(floor_frac * np.abs(ref).max(), np.finfo(np.float64).tiny)
+    big = np.abs(ref) >= floor
     err_big = np.abs(gpu - ref)[big] / np.abs(ref)[big]
     err_small = np.abs(gpu - ref)[~big]
     assert err_big.size == 0 or err_big.max() <= rel, f"{what}: max rel err {err_big.max():.3e}"
-    assert err_small.size == 0 or err_small.max() <= abs_small + floor_frac * np.abs(ref).max(), \
-        f"{what}: small-value abs err {err_small.max():.3e}"
+    assert err_small.size == 0 or err_small.max() <= floor, f"{what}: small-value abs err {err_small.max():.3e}"
 
 
 class Lockstep:

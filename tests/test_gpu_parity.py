@@ -192,25 +192,46 @@ def test_full_size_llama_shape(lib):
     assert ls.max_out_err <= OUT_TOL
 
 
-@pytest.mark.parametrize("name,over,steps,check_state", [
+@pytest.mark.parametrize("name,over,steps,state_seqs", [
     # 16 sequences of the 32K shape: 128 (sequence, KV head) units, 2 splits each
-    ("batched_32k", dict(n_layers=1, steps=8), 8, True),
+    ("batched_32k", dict(n_layers=1, steps=8), 8, "ends"),
     # 131K prompt, lognormal per-window key scales (INT2, 20%, q = 0.7): outputs, masses and the
-    # transition counters of every unit every step; tier-state dumps are skipped at this size
-    ("long_131k", dict(n_layers=1, batch=2, steps=8), 8, False),
+    # transition counters of every unit every step; the full state (4091 windows: tiers, slots,
+    # tables, every ledger record and Full window) of the first sequence after prefill and routing
+    ("long_131k", dict(n_layers=1, batch=2, steps=8), 8, [0]),
     # random-walk queries, 12.5% budget, 256 recent tokens, batch 8: three routing events
-    ("drift_16k", dict(n_layers=1, steps=24), 24, True),
+    ("drift_16k", dict(n_layers=1, steps=24), 24, "ends"),
     # the 131K point in the INT4 / 64-token-window format
-    ("long_131k", dict(n_layers=1, batch=1, steps=8, window=64, bits=4), 8, False),
+    ("long_131k", dict(n_layers=1, batch=1, steps=8, window=64, bits=4), 8, None),
     # pre-RoPE Quantized keys at positions up to 131K (RoPE base 500000)
-    ("long_131k", dict(n_layers=1, batch=1, steps=8, rope_base=500000.0), 8, False),
+    ("long_131k", dict(n_layers=1, batch=1, steps=8, rope_base=500000.0), 8, None),
 ])
-def test_full_size_workloads(lib, name, over, steps, check_state):
+def test_full_size_workloads(lib, name, over, steps, state_seqs):
     """The other workloads at their full per-layer shapes (one layer each), in lockstep: outputs,
-    window masses, scores and counters of every sequence; full state of the first, middle and last."""
+    window masses, scores and counters of every sequence; the full state of the listed sequences
+    ("ends": the first, middle and last)."""
     wl = synth.workload(name, **over)
-    seqs = sorted({0, wl.batch // 2, wl.batch - 1})
-    ls = _run(wl, steps, oracle_prefill_scores=False, check_state=check_state, state_seqs=seqs)
+    if state_seqs == "ends":
+        state_seqs = sorted({0, wl.batch // 2, wl.batch - 1})
+    ls = _run(wl, steps, oracle_prefill_scores=False, check_state=state_seqs is not None,
+              state_seqs=state_seqs or [])
+    assert ls.max_out_err <= OUT_TOL
+
+
+@pytest.mark.parametrize("name,over,steps", [
+    # the bench's launch configuration: batch 1, 8 KV heads, 19 splits per head on 152 SMs
+    ("llama8b_32k", dict(n_layers=2, steps=16), 16),
+    # 16 sequences: 128 (sequence, KV head) units
+    ("batched_32k", dict(n_layers=1, steps=8), 8),
+])
+def test_full_size_deferred_score_flush(lib, name, over, steps):
+    """The production score path at full size (QEvict §4.2 Eq. (1), read as an update that the
+    router absorbs): every decode step records its window masses in its own step slot, and only the
+    routing event's flush adds them to the scores, step by step.  At every routing event the scores
+    of every window of every unit equal the oracle's per-step cumulative scores; outputs are compared
+    every step and the full state after each event."""
+    wl = synth.workload(name, **over)
+    ls = _run(wl, steps, oracle_prefill_scores=False, per_step=False, state_seqs=sorted({0, wl.batch - 1}))
     assert ls.max_out_err <= OUT_TOL
 
 
@@ -258,6 +279,44 @@ def test_status_codes(lib):
     c.route()
     c.decode_step(0, q, kv, kv, out)
     c.check()
+
+
+def test_slot_exhaustion_guard(lib):
+    """Failure detection of the router's slot allocation (QEvict App. A Algorithm 1): with a host-set
+    cap that hides free slots, a routing event whose newcomers need more F or ledger slots than it sees
+    records the failure (qevict_check returns QEVICT_EDEVICE) and leaves every tier, slot, table and
+    ledger record as it was; the pending masses are still absorbed.  No GPU fault is involved."""
+    wl = synth.workload("tiny_4k", prompt_len=1200, steps=24, n_plant=4)
+    ls = Lockstep(wl)
+    ls.prefill()
+    ls.decode(3 * wl.omega - 1)   # the event after step 24 is the first one with a newly aged window
+    one = ls.dec[(0, 0)]
+    s = ls.step
+    out = torch.empty(1, wl.h_q, 128, dtype=torch.bfloat16, device="cuda")
+    ls.cache.decode_step(0, one["q"][s][None].cuda(), one["k"][s][None].cuda(), one["v"][s][None].cuda(), out)
+    torch.cuda.synchronize()
+    u, N = 0, ls.N
+    regions = {"state": N, "fslot": 4 * N, "lslot": 4 * N, "ftab": 8 * max(1, min(ls.bud.k_f, N)),
+               "qtab": 8 * max(1, min(ls.bud.k_q, N)), "ledger": ls.lay.stride_ledger, "fpool": ls.lay.stride_fpool}
+    before = {k: ls.cache.region(k, u, n).clone() for k, n in regions.items()}
+    meta_before = ls.meta(0, 0).copy()
+    # a window ages out of the recent region at this event; ranked first, it enters F and needs an F
+    # slot, which the cap hides
+    aged = int(meta_before[1])
+    assert O.n_hist(int(meta_before[0]), ls.ocfg) > aged
+    ls.cache.region("score", u, 4 * wl.h_kv * N).view(torch.float32)[aged] = 1e6
+    ls.cache.debug_cap_free_slots(0)
+    ls.cache.route()
+    with pytest.raises(binding.QEvictError) as e:
+        ls.cache.check()
+    assert e.value.status == binding.EDEVICE
+    for k, t in before.items():
+        assert torch.equal(ls.cache.region(k, u, regions[k]), t), k
+    m = ls.meta(0, 0)
+    assert m[1] == meta_before[1] and m[2] == meta_before[2] and m[3] == meta_before[3]   # windows routed, |F|, |Q|
+    ls.cache.debug_cap_free_slots(-1)
+    with pytest.raises(binding.QEvictError):
+        ls.cache.debug_cap_free_slots(-2)
 
 
 def test_wait_timeout_is_reported_and_recoverable(lib):

@@ -75,10 +75,10 @@ def test_aging_rule_brute_force():
 
 # ----------------------------------------------------------------------------- TopK
 
-def _fresh_unit(n_windows, k_f, k_q, seed=0):
+def _fresh_unit(n_windows, k_f, k_q, seed=0, **policy):
     """A unit whose prompt holds exactly n_windows historical windows, with capacities forced."""
     P = TINY["n_sink"] + TINY["n_recent"] + n_windows * TINY["window"]
-    cfg = O.Config(**TINY, prompt_len=P, max_len=P + 64, b_total=10 ** 9)
+    cfg = O.Config(**TINY, prompt_len=P, max_len=P + 64, b_total=10 ** 9, **policy)
     u = O.Unit(cfg)
     u.bud = O.Budget(0, 10 ** 9, 0, 0, 10 ** 9, 0, 1, 1, k_f, k_q)
     rng = np.random.default_rng(seed)
@@ -229,9 +229,9 @@ def test_promoted_window_holds_the_dequantised_copy():
     del rng
 
 
-def _golden_events():
+def _golden_events(name="routing_events.txt"):
     import os
-    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "routing_events.txt")
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", name)
     rows = []
     for ln in open(path):
         if ln.strip() and not ln.startswith("#"):
@@ -241,11 +241,14 @@ def _golden_events():
     return rows
 
 
-def test_routing_events_worked_by_hand():
+@pytest.mark.parametrize("fixture,policy", [("routing_events.txt", {}),
+                                            ("routing_no_promotion.txt", {"no_promotion": 1})])
+def test_routing_events_worked_by_hand(fixture, policy):
     """Tiers, F slots, ledger slots and statuses, and transition counters of three routing events worked
-    by hand (tests/golden/routing_events.txt; QEvict §4.3 Eq. (4)-(6), App. A Algorithm 1)."""
-    rows = _golden_events()
-    u, k = _fresh_unit(6, 2, 2, seed=3)
+    by hand (tests/golden/; QEvict §4.3 Eq. (4)-(6), App. A Algorithm 1, and App. K's policy without
+    promotion, where a Quantized window that out-scores a Full one stays Quantized)."""
+    rows = _golden_events(fixture)
+    u, k = _fresh_unit(6, 2, 2, seed=3, **policy)
     P = u.cfg.prompt_len
     assert P == 30 and O.prompt_windows(u.cfg) == 7
     rng = np.random.default_rng(4)

@@ -28,7 +28,7 @@ def _rank_main(rank, world, port, out):
 
 def test_max_over_ranks_gloo():
     world = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_rank_main, args=(world, 29511, out), nprocs=world, join=True)
         got = dict(out)
