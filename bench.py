@@ -52,6 +52,11 @@ def parse_args():
     ap.add_argument("--no-promotion", action="store_true", help="quantized windows never return to Full")
     ap.add_argument("--rope-base", type=float, default=0.0,
                     help="keys carry RoPE with this base and Quantized keys are kept before it (GPU arm only)")
+    ap.add_argument("--budget", default=None, help="B_total as NUM/DEN of the full cache (overrides the workload)")
+    ap.add_argument("--q", default=None, help="quantised fraction q as NUM/DEN (overrides the workload)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="the long-context sweep: B_total in {10, 20, 40}%% x q in {0.5, 0.7, 0.9} of the workload "
+                         "(INT2/W=32, or INT4/W=64 with --int4), one reduced measurement each; one JSON line")
     ap.add_argument("--layers", type=int, default=None,
                     help="run the workload with fewer layers (a smaller case for profiler captures; "
                          "the JSON line then reports that layer count)")
@@ -389,6 +394,12 @@ def run_gpu(args, rank, world):
         wl = wl.replace(window=64, bits=4)
     if args.ranker or args.no_promotion:
         wl = wl.replace(ranker=args.ranker, no_promotion=1 if args.no_promotion else 0)
+    if args.budget:
+        num, den = (int(x) for x in args.budget.split("/"))
+        wl = wl.replace(budget_num=num, budget_den=den)
+    if args.q:
+        num, den = (int(x) for x in args.q.split("/"))
+        wl = wl.replace(q_num=num, q_den=den)
     K, Wm = args.steps, args.warmup
     Om = wl.omega
     K_kern = 2 * Om
@@ -571,6 +582,7 @@ def run_gpu(args, rank, world):
     timed_launches = state["launches"] - launches_before
     timed_events = sum(1 for i in range(first, first + K) if (i + 1) % Om == 0)
     torch.cuda.synchronize()
+    ctr_before_timed = cache.counters()
     sampler = ClockSampler(_bus_id(torch, dev))
     if world > 1:
         torch.distributed.barrier()
@@ -586,6 +598,7 @@ def run_gpu(args, rank, world):
         torch.distributed.barrier()
     ms_total = max_over_ranks(e0.elapsed_time(e1), world, dev)
     cache.check(stream)
+    ctr_after_timed = cache.counters()
 
     # ---- e2e: inputs from pinned host memory, outputs back to pinned host memory, every step
     e2e = None
@@ -692,8 +705,12 @@ def run_gpu(args, rank, world):
             "events": len(per_event), "units": L * B,
             "mean": {k: statistics.mean(e[k] for e in per_event) for k in per_event[0]},
             "max": {k: max(e[k] for e in per_event) for k in per_event[0]},
-            "note": "tier transitions per routing event over all (layer, sequence) units, from counter deltas "
-                    "of the untimed events (QEvict App. K Table 18's promotion counts)"},
+            "timed_events": timed_events,
+            "timed_mean": {k: (ctr_after_timed[k] - ctr_before_timed[k]) / max(1, timed_events)
+                           for k in ctr_after_timed},
+            "note": "tier transitions per routing event over all (layer, sequence) units: mean/max from counter "
+                    "deltas of each untimed event, timed_mean over the events of the timed region (QEvict "
+                    "App. K Table 18's promotion counts)"},
         "clocks": clocks,
         "prefill_s": round(t_pre, 2), "prefill_scores": prefill_scores,
     }
@@ -800,6 +817,30 @@ def run_reference(args, rank, world):
             "wall_s": round(time.time() - t_start, 1)}
 
 
+def run_sweep(args, rank, world):
+    """Config 4's grid (QEvict §5 "Ablations", App. G.2-G.3: budget and quantised fraction) on the
+    given workload: each point a full run_gpu measurement with a short timed region."""
+    import copy
+    import torch
+    pts = []
+    for b in (10, 20, 40):
+        for q in (50, 70, 90):
+            a = copy.copy(args)
+            a.budget, a.q, a.no_e2e = f"{b}/100", f"{q}/100", True
+            r = run_gpu(a, rank, world)
+            rf = r["roofline"]
+            pts.append({"budget": b / 100, "q": q / 100, "k_f": r["config"]["k_f"], "k_q": r["config"]["k_q"],
+                        "steps_per_s": r["value"], "ms_per_step": r["ms_per_step"],
+                        "avg_launch_us": rf["avg_launch_us"], "bytes_per_launch": rf["bytes_per_launch"],
+                        "achieved_gbs": rf["achieved"], "frac": rf["frac"], "hbm_frac_step": r["hbm_frac_step"],
+                        "clocks": r["clocks"]})
+            torch.cuda.empty_cache()
+    return {"metric": METRIC, "sweep": pts, "workload": args.workload, "layers": args.layers,
+            "format": "INT4/W=64" if args.int4 else "INT2/W=32", "steps": args.steps, "warmup": args.warmup,
+            "note": "each point: decode steps/s over the timed steps (routing included) and the decode "
+                    "kernel's roofline, as in the main bench line"}
+
+
 def main():
     args = parse_args()
     if args.oracle_child:
@@ -817,6 +858,11 @@ def main():
     torch.cuda.set_device(local)
     if world > 1:
         torch.distributed.init_process_group("nccl")
+    if args.sweep:
+        res = run_sweep(args, rank, world)
+        if rank == 0:
+            print(json.dumps(res))
+        return
     res = run_gpu(args, rank, world)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:

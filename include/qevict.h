@@ -25,8 +25,10 @@
  *     device status word (read by qevict_read_counters / qevict_check).  On an
  *     error nothing is enqueued unless stated.  Bits of the status word: 1 a
  *     bounded wait ran out, 2 a routing event found too few free slots, 4 a
- *     kernel found the cache state inconsistent; they stay set until an earlier
- *     export is imported or the cache is re-initialised.
+ *     kernel found the cache state inconsistent, 8 (checked build only,
+ *     libqevict_check.so) an index read from device data was outside its buffer
+ *     and its access was skipped; they stay set until an earlier export is
+ *     imported or the cache is re-initialised.
  *   - Tensors are dense, row-major, bf16 (uint16 storage) unless stated.
  *   - One cache serves `batch` sequences that decode in lockstep and all
  *     `n_layers` layers; every (sequence, layer) pair is one independent "unit".
@@ -126,9 +128,9 @@ typedef struct {
  *   K element (tok, dim): with r, c, lane, reg as above, group = (tok/16)*8 + dim/16,
  *     e = reg*2 + dim%2, bit = 4e (e < 4) or 4(e-4)+2 (e >= 4) inside the 16-bit field of
  *     (group, lane), which is lane bytes 2*group, 2*group+1 (little-endian).
- *   V element (tok, dim): with r = dim%16, c = tok%16, lane and reg as above, i = dim/16,
- *     rr = (i%2)*4 + reg, word w = (tok/16)*4 + i/2 (lane bytes 4w .. 4w+3, little-endian),
- *     bit = (rr < 5 ? 2*rr : 10 + 2*(rr-5)) + 16*(tok%2) inside that word.
+ *   V element (tok, dim): with r = dim%16, c = tok%16 and lane as above, word i = dim/16 (lane
+ *     bytes 4i .. 4i+3, little-endian), token pair tau = 2*(tok/16) + c/8,
+ *     bit = 8*(r/8) + 2*tau + 16*(tok%2) inside that word.
  * Fragment-native INT4 codes (W = 64; 4 KB per K or V block): one little-endian 32-bit word per
  * (16x16 tile, lane), tile = (tok/16)*8 + dim/16, stored at word ((tile/4)*32 + lane)*4 + tile%4.
  *   K element (tok, dim): r = tok%16, c = dim%16, lane and reg as above, bits 4*(reg*2 + dim%2).
@@ -238,6 +240,10 @@ qevict_status qevict_read_counters(qevict_cache *cache, int64_t *host7, qevict_s
 /* Synchronises `stream`, re-reads the per-layer token counts (needed after replaying captured
  * CUDA graphs of decode steps) and returns QEVICT_EDEVICE if the device status word is set. */
 qevict_status qevict_check(qevict_cache *cache, qevict_stream_t stream);
+
+/* The device status word itself (its bits are listed with the conventions above), copied to
+ * *host_word after `stream` synchronises; the word is not cleared.  QEVICT_ECUDA if the copy fails. */
+qevict_status qevict_read_status(const qevict_cache *cache, int32_t *host_word, qevict_stream_t stream);
 
 /* Failure-reporting self-test.  Enqueues on `stream` a one-thread kernel that waits, through the
  * same bounded wait every kernel of the library uses, on an mbarrier phase that nothing completes.

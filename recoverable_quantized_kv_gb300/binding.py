@@ -11,7 +11,8 @@ import os
 from typing import Optional
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libqevict.so")
+# QEVICT_LIB=check loads the checked build (device bounds checks that report to the status word)
+LIB_PATH = os.path.join(HERE, "libqevict_check.so" if os.environ.get("QEVICT_LIB") == "check" else "libqevict.so")
 
 OK, EINVAL, EBUDGET, ENOMEM, ESCHEDULE, ECUDA, EDEVICE = range(7)
 COUNTER_NAMES = ("promotions", "demotions", "first_quant", "reactivations", "evictions", "aged_full", "aged_quant")
@@ -106,6 +107,7 @@ def load() -> ctypes.CDLL:
         "qevict_prefill_scores_noalloc": [I32, I32, I32, I32, I32, I32, P, P, P, P],
         "qevict_prefill_scores_noalloc_status": [P],
         "qevict_debug_cap_free_slots": [P, I32],
+        "qevict_read_status": [P, ctypes.POINTER(I32), P],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -125,7 +127,8 @@ def exported_symbols():
             "qevict_prefill_scores_noalloc", "qevict_flush_scores", "qevict_get_tuple", "qevict_export_bytes",
             "qevict_export_state", "qevict_import_state", "qevict_set_rope_table", "qevict_diag_bytes",
             "qevict_diag_init", "qevict_diag_route", "qevict_diag_read", "qevict_diag_destroy",
-            "qevict_selftest_wait", "qevict_prefill_scores_noalloc_status", "qevict_debug_cap_free_slots"]
+            "qevict_selftest_wait", "qevict_prefill_scores_noalloc_status", "qevict_debug_cap_free_slots",
+            "qevict_read_status"]
 
 
 def _check(status: int, where: str):
@@ -273,6 +276,12 @@ class Cache:
     def selftest_wait(self, stream=None):
         """Enqueue the bounded-wait self-test: a wait that runs out and records a timeout."""
         _check(load().qevict_selftest_wait(self.handle, _stream(stream)), "qevict_selftest_wait")
+
+    def status_word(self, stream=None) -> int:
+        """The device status word (bit 1 timeout, 2 slot exhaustion, 4 inconsistent state, 8 bounds)."""
+        w = ctypes.c_int32()
+        _check(load().qevict_read_status(self.handle, ctypes.byref(w), _stream(stream)), "qevict_read_status")
+        return w.value
 
     def debug_cap_free_slots(self, cap: int):
         """Routing events see at most `cap` free F / ledger slots (-1: no cap); a test hook."""

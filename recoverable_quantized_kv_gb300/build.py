@@ -17,6 +17,9 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 SOURCES = ["api.cu", "decode.cu", "route.cu", "scores.cu", "noalloc.cu", "diag.cu"]
 LIB = os.path.join(HERE, "libqevict.so")
+# the checked build: every index read from device data is tested before use (-DQEVICT_CHECK); an index
+# outside its buffer sets a bit of the device status word instead of being used
+LIB_CHECK = os.path.join(HERE, "libqevict_check.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 
@@ -33,14 +36,16 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    """Compiles every CUDA source and links libqevict.so; returns its path."""
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime() and not extra_flags:
-        return LIB
+def build(force: bool = False, verbose: bool = False, extra_flags=None, checked: bool = False) -> str:
+    """Compiles every CUDA source and links libqevict.so (checked=True: libqevict_check.so, the build
+    with device bounds checks); returns its path."""
+    lib = LIB_CHECK if checked else LIB
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _deps_mtime() and not extra_flags:
+        return lib
     nvcc = _nvcc()
-    objdir = os.path.join(HERE, "_build")
+    objdir = os.path.join(HERE, "_build_check" if checked else "_build")
     os.makedirs(objdir, exist_ok=True)
-    flags = FLAGS + list(extra_flags or [])
+    flags = FLAGS + (["-DQEVICT_CHECK"] if checked else []) + list(extra_flags or [])
 
     def compile_one(src):
         obj = os.path.join(objdir, src.replace(".cu", ".o"))
@@ -54,12 +59,12 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
 
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -384,7 +384,7 @@ qevict_status qevict_flush_scores(qevict_cache *cache, qevict_stream_t stream) {
 
 static qevict_status read_status(qevict_cache *cache, cudaStream_t s) {
   int st = 0;
-  if (cudaMemcpyAsync(&st, cache->dev.arena + cache->dev.off_status, sizeof(int), cudaMemcpyDeviceToHost, s) !=
+  if (cudaMemcpyAsync(&st, cache->dev.status_word, sizeof(int), cudaMemcpyDeviceToHost, s) !=
           cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess)
     return QEVICT_ECUDA;
@@ -406,6 +406,15 @@ qevict_status qevict_read_counters(qevict_cache *cache, int64_t *host7, qevict_s
     host7[k] = t;
   }
   return st;
+}
+
+qevict_status qevict_read_status(const qevict_cache *cache, int32_t *host_word, qevict_stream_t stream) {
+  if (!cache || !host_word) return QEVICT_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(host_word, cache->dev.status_word, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return QEVICT_ECUDA;
+  return QEVICT_OK;
 }
 
 qevict_status qevict_check(qevict_cache *cache, qevict_stream_t stream) {

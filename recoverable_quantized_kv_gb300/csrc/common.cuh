@@ -20,7 +20,19 @@ enum : int { M_T = 0, M_NROUTE = 1, M_FCOUNT = 2, M_QCOUNT = 3, M_NQUANT = 4, M_
 
 enum : int { TIER_LOCAL = 0, TIER_FULL = 1, TIER_QUANT = 2, TIER_EVICT = 3 };
 enum : int { LED_NONE = 0, LED_ACTIVE = 1, LED_DORMANT = 2 };
-enum : int { QV_ERR_TIMEOUT = 1, QV_ERR_SLOT = 2, QV_ERR_STATE = 4 };
+enum : int { QV_ERR_TIMEOUT = 1, QV_ERR_SLOT = 2, QV_ERR_STATE = 4, QV_ERR_BOUNDS = 8 };
+
+// Checked builds (compiled with -DQEVICT_CHECK, libqevict_check.so) test every index read from
+// device data before the access it guards: an index outside its buffer records QV_ERR_BOUNDS in the
+// device status word and the access is skipped.  Other builds compile the test away.
+#ifdef QEVICT_CHECK
+__device__ __forceinline__ bool qv_inbounds(bool ok, int *status) {
+  if (!ok) atomicOr(status, QV_ERR_BOUNDS);
+  return ok;
+}
+#else
+__device__ __forceinline__ bool qv_inbounds(bool, int *) { return true; }
+#endif
 enum : int { N_COUNTERS = 8 };    // 7 used: promo, demo, firstq, react, evict, aged_f, aged_q
 
 // ----------------------------------------------------------------------------- layout maps
@@ -47,9 +59,11 @@ __host__ __device__ __forceinline__ int fnv_index(int tok, int dim) {
 //  K: the codes of one m16n8k16 A-register group (16 tokens x 16 channels) form a 16-bit field per
 //     lane; element e = reg*2 + half sits at bit 4e (e < 4) or 4(e-4)+2 (e >= 4), so masking with
 //     0x3333 yields byte-permute selectors directly.
-//  V: one 32-bit word per (16-token group kk, pair of 16-dim tiles); register r = (tile%2)*4 + reg
-//     keeps its two codes (even, odd token) at bits b and b+16 with b = 2r (r < 5) or 10 + 2(r-5),
-//     so one mask (after at most one shift by 10) lands them in fp16 mantissas.
+//  V: one 32-bit word per 16-dim tile i (word i of the lane's 32 bytes): the register of row half
+//     rh = (dim%16)/8 and token pair tau = 2*(tok/16) + (tok%16)/8 keeps its two codes (even, odd
+//     token) at bits b and b+16 with b = 8*rh + 2*tau.  One mask (after a shift by 8 for rh = 1)
+//     leaves them as the mantissas of two fp16 subnormals, c * 4^tau * 2^-24: the power of 4 depends
+//     on the token pair only, so the P operand of those tokens can carry its inverse.
 __host__ __device__ __forceinline__ void code_pos2(bool is_v, int tok, int dim, int &byte, int &shift) {
   int lb, bit;
   if (!is_v) {
@@ -62,10 +76,9 @@ __host__ __device__ __forceinline__ void code_pos2(bool is_v, int tok, int dim, 
   } else {
     const int rr = dim & 15, c = tok & 15, i = dim >> 4;
     const int lane = frag_lane(rr, c);
-    const int r = ((i & 1) << 2) | frag_reg(rr, c);
-    const int w = (tok >> 4) * 4 + (i >> 1);
-    bit = (r < 5 ? 2 * r : 10 + 2 * (r - 5)) + 16 * (c & 1);
-    lb = 4 * w + (bit >> 3);
+    const int tau = 2 * (tok >> 4) + (c >> 3);
+    bit = 8 * (rr >> 3) + 2 * tau + 16 * (c & 1);
+    lb = 4 * i + (bit >> 3);
     byte = (lb >> 4) * 512 + lane * 16 + (lb & 15);
   }
   shift = bit & 7;

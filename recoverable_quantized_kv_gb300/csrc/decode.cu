@@ -21,15 +21,23 @@
 
 namespace qv {
 
-constexpr int DEC_WARPS = 16;          // 15 consumer warps + 1 producer warp
+constexpr int DEC_WARPS = 12;          // 11 consumer warps + 1 producer warp (168 registers a thread)
 constexpr int DEC_CONSUMERS = DEC_WARPS - 1;
 constexpr int DEC_SLOTS = 36;          // CTA-wide ring of 4 KB slots filled by bulk copies
 constexpr int DEC_STAGE_BYTES = 4096;
-// per consumer warp: the key look-up table of the window in hand (INT2: bf16 bytes of the 4 values
-// of 128 channels; INT4: fp32 scale and offset of 128 channels), 8 k-steps x 4 lane classes x 32 B,
-// then (ROPE) the cos/sin rows of the window's first position of each 32-token half.  Both live in
-// the warp's own output region of the CTA merge, which the warp writes only after its last window.
+// per consumer warp: the key look-up tables of the windows in hand (INT2: bf16 bytes of the 4 values
+// of 128 channels; INT4: fp32 scale and offset of 128 channels), 8 k-steps x 4 lane classes x 32 B
+// each, then (ROPE) the cos/sin rows of the window's first position of each 32-token half.  They live
+// in the warp's own output region of the CTA merge, which the warp writes only after its last window.
 constexpr int DEC_TBL_BYTES = 1024;
+// Scale of the output accumulators of the INT2 kernels: P V of Quantized windows runs on value codes
+// held as fp16 subnormals (c * 4^tau * 2^-24) against P * s * 4^(3 - tau), so its products come out
+// at 2^-18; bf16 windows scale their P by the same 2^-18, and the CTA merge scales back.
+template <int BITS>
+struct OScale {
+  static constexpr float P = BITS == 2 ? 0x1p-18f : 1.f;
+  static constexpr float INV = BITS == 2 ? 0x1p18f : 1.f;
+};
 // CTA merge: running max / sum / rescale per (warp, head), CTA max, and every warp's outputs
 constexpr int DEC_CO_OFF = (3 * DEC_CONSUMERS * 8 + 16) * 4;   // bytes before the outputs
 constexpr int DEC_MRG_FLOATS = 3 * DEC_CONSUMERS * 8 + 16 + DEC_CONSUMERS * 128 * 8;
@@ -57,7 +65,7 @@ struct DecGeo {
   static constexpr int SMEM = MRG_OFF + DEC_MRG_FLOATS * 4;
   static_assert((PHASES - 1) * DEC_SLOTS >= DEC_CONSUMERS * MAX_CHUNKS, "too few full barriers per slot");
   static_assert(W == 32 || Geo<W, BITS>::CODE_BYTES == DEC_STAGE_BYTES, "INT4 code blocks fill one chunk each");
-  static_assert(DEC_TBL_BYTES + HALVES * 512 <= 128 * 8 * 4, "per-warp tables fit the warp's output region");
+  static_assert(2 * DEC_TBL_BYTES + HALVES * 512 <= 128 * 8 * 4, "per-warp tables fit the warp's output region");
   static_assert(SMEM <= 232448, "shared memory per CTA");
   static_assert(MRG_OFF % 16 == 0 && DEC_CO_OFF % 16 == 0, "16-byte aligned per-warp tables");
 };
@@ -136,13 +144,82 @@ __device__ __forceinline__ void online_step(float (&s)[NMT][4], const bool (&val
   l_run += v;
 }
 
-// B fragments of P^T for k-step kk from the S^T accumulator layout (8x8 transposes).
+// online_step for NW windows of 32 tokens at once (S^T fragments s[w][mt]): one max vote and at most
+// one rescale for all of them; tsum[w] is window w's sum of this lane's head, l_run gains them all.
+// Windows with valid[w] false contribute nothing (probabilities 0).
+template <int NW>
+__device__ __forceinline__ void online_step_w(float (&s)[NW][2][4], const bool (&valid)[NW], float (&m_run)[2],
+                                              float &l_run, float (&o)[8][4], float (&macc)[2], float (&tsum)[NW],
+                                              const float scale) {
+  const bool odd = (threadIdx.x >> 2) & 1;
+  float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int w = 0; w < NW; ++w)
+    if (valid[w]) {
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        mx[0] = fmaxf(mx[0], fmaxf(s[w][mt][0], s[w][mt][2]));
+        mx[1] = fmaxf(mx[1], fmaxf(s[w][mt][1], s[w][mt][3]));
+      }
+    }
+  mx[0] *= scale;
+  mx[1] *= scale;
+  if (!__all_sync(0xffffffffu, mx[0] <= m_run[0] && mx[1] <= m_run[1])) {
+    float corr[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float mnew = fmaxf(m_run[h], warp_max_xor_g(mx[h]));
+      corr[h] = exp2f(m_run[h] - (mnew == -INFINITY ? 0.f : mnew));
+      m_run[h] = mnew;
+      macc[h] *= corr[h];
+    }
+    l_run *= odd ? corr[1] : corr[0];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      o[i][0] *= corr[0];
+      o[i][2] *= corr[0];
+      o[i][1] *= corr[1];
+      o[i][3] *= corr[1];
+    }
+  }
+  float base[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) base[h] = m_run[h] == -INFINITY ? 0.f : m_run[h];
+  float v[NW];
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    float ps[2] = {0.f, 0.f};
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float p = valid[w] ? ex2_ftz(fmaf(s[w][mt][2 * r + h], scale, -base[h])) : 0.f;
+          s[w][mt][2 * r + h] = p;
+          ps[h] += p;
+        }
+    v[w] = odd ? ps[1] : ps[0];
+    v[w] += __shfl_xor_sync(0xffffffffu, odd ? ps[0] : ps[1], 4);
+  }
+#pragma unroll
+  for (int w = 0; w < NW; ++w) v[w] += __shfl_xor_sync(0xffffffffu, v[w], 8);
+#pragma unroll
+  for (int w = 0; w < NW; ++w) {
+    v[w] += __shfl_xor_sync(0xffffffffu, v[w], 16);
+    tsum[w] = v[w];
+    l_run += v[w];
+  }
+}
+
+// B fragments of P^T for k-step kk from the S^T accumulator layout (8x8 transposes), times `scale`
+// (a power of two: exact).
 template <int NMT>
-__device__ __forceinline__ void p_to_b(const float (&p)[NMT][4], uint32_t (&pb)[NMT][2]) {
+__device__ __forceinline__ void p_to_b(const float (&p)[NMT][4], uint32_t (&pb)[NMT][2], const float scale) {
 #pragma unroll
   for (int kk = 0; kk < NMT; ++kk) {
-    pb[kk][0] = movmatrix_trans(pack_bf16(p[kk][0], p[kk][1]));
-    pb[kk][1] = movmatrix_trans(pack_bf16(p[kk][2], p[kk][3]));
+    pb[kk][0] = movmatrix_trans(pack_bf16(p[kk][0] * scale, p[kk][1] * scale));
+    pb[kk][1] = movmatrix_trans(pack_bf16(p[kk][2] * scale, p[kk][3] * scale));
   }
 }
 
@@ -207,6 +284,133 @@ __device__ __forceinline__ uint32_t pack_half(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// Key look-up table of one INT2 window for this lane's four channels d = 4*lane + k: the bf16 values
+// bf16(fp32(c*s + m)) for c = 0..3, split into low and high bytes, stored where lut_k_regs reads them
+// (k-step j, lane class t, channel pair A or B, value half).
+__device__ __forceinline__ void ktab_int2(const uint8_t *ch, uint8_t *tbl, int lane) {
+  using Gm = Geo<32, 2>;
+  const uint2 sp = *reinterpret_cast<const uint2 *>(ch + Gm::OFF_KS + 8 * lane);
+  const uint2 mp = *reinterpret_cast<const uint2 *>(ch + Gm::OFF_KM + 8 * lane);
+  uint32_t *tw = reinterpret_cast<uint32_t *>(tbl);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t sw = k < 2 ? sp.x : sp.y, mw = k < 2 ? mp.x : mp.y;
+    const float sc = (k & 1) ? h2f_hi(sw) : h2f_lo(sw);
+    const float mn = (k & 1) ? h2f_hi(mw) : h2f_lo(mw);
+    const uint32_t p01 = pack_bf16(mn, __fadd_rn(sc, mn));
+    const uint32_t p23 = pack_bf16(__fmaf_rn(2.f, sc, mn), __fmaf_rn(3.f, sc, mn));
+    const int d = 4 * lane + k, j = d >> 4, c16 = d & 15;
+    const int t = (c16 & 7) >> 1, which = c16 >> 3, half = c16 & 1;
+    const int base = (j * 4 + t) * 8 + which * 4 + half;
+    tw[base] = __byte_perm(p01, p23, 0x6420);
+    tw[base + 2] = __byte_perm(p01, p23, 0x7531);
+  }
+}
+
+// S^T = K q^T over the 32 tokens of NW INT2 windows at once (their MMA chains interleave): exact
+// bf16 keys from the byte tables, the G query heads on the N side.  kc: each window's two 16-byte
+// pieces of this lane's K codes; tbl: the windows' tables, DEC_TBL_BYTES apart.
+template <int NW>
+__device__ __forceinline__ void keys_int2(const uint4 (&kc)[NW][2], const uint8_t *tbl, const uint32_t (&qb)[8][2],
+                                          float (&s)[NW][2][4], int tl) {
+#pragma unroll
+  for (int jp = 0; jp < 4; ++jp) {
+    // selectors of both fields of a code word at once: k-step 2jp in the low half, 2jp+1 high
+    uint32_t sa[NW][2], sb[NW][2];
+#pragma unroll
+    for (int w = 0; w < NW; ++w)
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const uint32_t wd = word_of(kc[w][mt], jp);
+        sa[w][mt] = (wd & 0x33333333u) | 0x40404040u;
+        sb[w][mt] = ((wd >> 2) & 0x33333333u) | 0x40404040u;
+      }
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int j = 2 * jp + hf;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const uint4 TA = lds128(tbl + w * DEC_TBL_BYTES + (j * 4 + tl) * 32);
+        const uint4 TB = lds128(tbl + w * DEC_TBL_BYTES + (j * 4 + tl) * 32 + 16);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          uint32_t a0, a1, a2, a3;
+          lut_k_regs(hf ? sa[w][mt] >> 16 : sa[w][mt], hf ? sb[w][mt] >> 16 : sb[w][mt], TA, TB, a0, a1, a2, a3);
+          mma_bf16(s[w][mt], a0, a1, a2, a3, qb[j][0], qb[j][1]);
+        }
+      }
+    }
+  }
+}
+
+// P V of one INT2 window (QEvict §4.3: values quantised per token, x = c*s + m), for this lane's
+// probabilities p (S^T layout, tokens 16kk + gl and + 8).  o += sum_t p_t s_t c_t at the 2^-18
+// scale of OScale<2>, macc += sum_t p_t m_t per lane head (its lanes are summed at the merge).
+// The codes enter the tensor core as fp16 subnormals c * 4^tau * 2^-24 (one mask each), and the P
+// operand of token pair tau carries p * s * 4^(3 - tau), so every product is c p s 2^-18.  That P
+// stays below the fp16 range while every token scale s <= 1023; a window with a larger scale takes
+// the products at 2^-24 into a zeroed tile and adds them 64-fold instead.
+__device__ __forceinline__ void pv_int2(const float (&p)[2][4], const uint8_t *ch, float (&o)[8][4], float (&macc)[2],
+                                        int lane) {
+  using Gm = Geo<32, 2>;
+  const int gl = lane >> 2;
+  const __half *vsp = reinterpret_cast<const __half *>(ch + Gm::OFF_VS);
+  const __half *vmp = reinterpret_cast<const __half *>(ch + Gm::OFF_VM);
+  float sv[2][2], pm0 = 0.f, pm1 = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < 2; ++kk) {
+    const int t0 = 16 * kk + gl, t1 = t0 + 8;
+    sv[kk][0] = __half2float(vsp[t0]);
+    sv[kk][1] = __half2float(vsp[t1]);
+    const float m0v = __half2float(vmp[t0]), m1v = __half2float(vmp[t1]);
+    fma2(pm0, pm1, p[kk][2], p[kk][3], m1v, m1v, pm0, pm1);
+    fma2(pm0, pm1, p[kk][0], p[kk][1], m0v, m0v, pm0, pm1);
+  }
+  macc[0] += pm0;
+  macc[1] += pm1;
+  const uint4 vw0 = lds128(ch + Gm::OFF_VCODE + lane * 16), vw1 = lds128(ch + Gm::OFF_VCODE + 512 + lane * 16);
+  const float smax = fmaxf(fmaxf(sv[0][0], sv[0][1]), fmaxf(sv[1][0], sv[1][1]));
+  const bool wide = __any_sync(0xffffffffu, !(smax <= 1023.f));
+  // P operand of k-step kk: b0 holds tokens 16kk + 2tl .. (pair tau = 2kk), b1 tokens 16kk + 8 + 2tl ..
+  // (tau = 2kk + 1), each scaled by 4^(3 - tau) (2^-6 more on the wide path)
+  const float wsc = wide ? 0.015625f : 1.f;
+  uint32_t pb[2][2];
+#pragma unroll
+  for (int kk = 0; kk < 2; ++kk) {
+    const float f0 = (kk ? 4.f : 64.f) * wsc, f1 = (kk ? 1.f : 16.f) * wsc;
+    const float s0 = sv[kk][0] * f0, s1 = sv[kk][1] * f1;
+    float x0, x1, x2, x3;
+    mul2(x0, x1, p[kk][0], p[kk][1], s0, s0);
+    mul2(x2, x3, p[kk][2], p[kk][3], s1, s1);
+    pb[kk][0] = movmatrix_trans(pack_half(x0, x1));
+    pb[kk][1] = movmatrix_trans(pack_half(x2, x3));
+  }
+  if (!wide) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t w = word_of(i < 4 ? vw0 : vw1, i & 3), w8 = w >> 8;
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        const uint32_t m0 = 0x00030003u << (4 * kk), m1 = m0 << 2;
+        mma_f16(o[i], w & m0, w8 & m0, w & m1, w8 & m1, pb[kk][0], pb[kk][1]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t w = word_of(i < 4 ? vw0 : vw1, i & 3), w8 = w >> 8;
+      float t[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        const uint32_t m0 = 0x00030003u << (4 * kk), m1 = m0 << 2;
+        mma_f16(t, w & m0, w8 & m0, w & m1, w8 & m1, pb[kk][0], pb[kk][1]);
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) o[i][r] = fmaf(64.f, t[r], o[i][r]);
+    }
+  }
+}
+
 __device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 __device__ __forceinline__ float bf_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
@@ -247,6 +451,7 @@ __device__ __forceinline__ void rope_rot(float a0, float a1, float b0, float b1,
 __device__ __forceinline__ float4 cc_ss(const float4 &v) { return make_float4(v.x, v.z, v.y, v.w); }
 
 template <int W, int BITS, bool ROPE>
+// 12 warps, three on each SM sub-partition, whose register file share (16K registers) allows 168 each
 __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDev C, const DecodeIO io) {
   static_assert((W == 32 && BITS == 2) || (W == 64 && BITS == 4), "formats: W=32 INT2, W=64 INT4");
   using Gm = Geo<W, BITS>;
@@ -271,7 +476,11 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   int *status = C.status();
   int *meta = C.at<int>(C.off_meta, C.st_meta, unit);
   int *thead = reinterpret_cast<int *>(C.arena + C.off_thead) + (size_t)unit * C.h_kv + g;
-  const int T = *thead, n_route = meta[M_NROUTE], nF = meta[M_FCOUNT], nQ = meta[M_QCOUNT];
+  int T = *thead, n_route = meta[M_NROUTE], nF = meta[M_FCOUNT], nQ = meta[M_QCOUNT];
+  if (!qv_inbounds(nF >= 0 && nF <= C.kf_cap() && nQ >= 0 && nQ <= min(C.k_q, C.n_windows) && n_route >= 0 &&
+                       T > C.n_sink && T < C.max_len && (T - C.n_sink) / C.W - n_route < C.ring_windows,
+                   status))
+    nF = nQ = 0, n_route = max(0, (T - C.n_sink) / C.W);
   // this step's slot in the per-step mass records: steps since the scores last absorbed them
   int mslot = T - meta[M_FLUSHT];
   if (mslot < 0 || mslot >= C.omega) {
@@ -299,8 +508,11 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   const int F0 = split * nF / ns, F1 = (split + 1) * nF / ns;
   const int Q0 = split * nQ / ns, Q1 = (split + 1) * nQ / ns;
   const int has_sink = split == 0 ? 1 : 0;
-  const int cta_items = has_sink + (L1 - L0) + (F1 - F0) + (Q1 - Q0);
-  auto item_of = [&](int k) -> int {
+  // Quantized windows per queue item: INT2 windows without RoPE go in pairs, whose MMA chains and
+  // softmax a warp runs together; the last item of an odd count holds one window
+  constexpr int QPER = (BITS == 2 && !ROPE) ? 2 : 1;
+  const int cta_items = has_sink + (L1 - L0) + (F1 - F0) + (Q1 - Q0 + QPER - 1) / QPER;
+  auto item_of = [&](int k) -> int {   // the item's (first) window
     if (has_sink) {
       if (k == 0) return 0;
       k -= 1;
@@ -309,7 +521,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
     k -= L1 - L0;
     if (k < F1 - F0) return 1 + nL + F0 + k;
     k -= F1 - F0;
-    return 1 + nL + nF + Q0 + k;
+    return 1 + nL + nF + Q0 + QPER * k;
   };
 
   uint8_t *slots = smem;
@@ -328,19 +540,20 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   auto chunk_start = [&](int pos) -> int {
     const int k = pos - has_sink;
     if (k <= 0) return 0;
-    return k <= nb ? BFC * k : BFC * nb + QCH * (k - nb);
+    return k <= nb ? BFC * k : BFC * nb + QCH * QPER * (k - nb);
   };
   // global source of chunk c
   auto chunk_src = [&](int c, const void *&src, uint32_t &bytes) {
-    int pos, sub;
+    // the window of chunk c: a bf16 window's item, or Quantized window (c - BFC nb) / QCH of the CTA
+    // (chunks count windows, not queue items, which pair Quantized windows)
+    int it, sub;
     if (c < BFC * nb) {
-      pos = has_sink + c / BFC;
+      it = item_of(has_sink + c / BFC);
       sub = c % BFC;
     } else {
-      pos = has_sink + nb + (c - BFC * nb) / QCH;
+      it = 1 + nL + nF + Q0 + (c - BFC * nb) / QCH;
       sub = (c - BFC * nb) % QCH;
     }
-    const int it = item_of(pos);
     if (it <= nL) {
       const int rs = (j0 + it - 1) % C.ring_windows;
       const __nv_bfloat16 *kb = ring + (size_t)rs * Gm::BLK;
@@ -348,11 +561,13 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
       src = sub < KCH ? (const void *)(kb + sub * 2048) : (const void *)(vb + (sub - KCH) * 2048);
       bytes = DEC_STAGE_BYTES;
     } else if (it <= nL + nF) {
-      const int slot = __ldg(&ftab[it - 1 - nL].y);
+      int slot = __ldg(&ftab[it - 1 - nL].y);
+      if (!qv_inbounds(slot >= 0 && slot < C.kf_cap(), status)) slot = 0;
       src = fpool + ((size_t)slot * C.h_kv + g) * 2 * Gm::BLK * 2 + (size_t)sub * DEC_STAGE_BYTES;
       bytes = DEC_STAGE_BYTES;
     } else {
-      const int slot = __ldg(&qtab[it - 1 - nL - nF].y);
+      int slot = __ldg(&qtab[it - 1 - nL - nF].y);
+      if (!qv_inbounds(slot >= 0 && slot < min(C.k_f + C.k_q, C.n_windows), status)) slot = 0;
       src = ledger + ((size_t)slot * C.h_kv + g) * Gm::QB + (size_t)sub * DEC_STAGE_BYTES;
       bytes = min(DEC_STAGE_BYTES, Gm::QB - sub * DEC_STAGE_BYTES);
     }
@@ -386,14 +601,22 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   if (producer) {
     // ---------------- producer warp: lane l issues chunk base + l of every batch of 32; a chunk
     // reuses its slot once the consumer of the chunk DEC_SLOTS earlier has released it
-    // The step's inputs come from the previous kernel in a model, and that kernel's last CTAs are
-    // still merging when this one starts: a burst of window copies now would slow their loads
-    // more than it would gain here.  So the copies start once the previous kernel has completed.
-    if (!io.wait_first) asm volatile("griddepcontrol.wait;" ::: "memory");
+    // The cache windows of this layer do not depend on the previous kernel, so the first batch of
+    // copies goes out before the wait, on an SM the previous kernel has already left.  (When the
+    // previous kernel may be this layer's own decode, everything waited above.)
+    int base0 = 0;
+    if (!io.wait_first) {
+      if (lane < n_total) {
+        mbar_arrive_expect_tx(&full[lane], bytes0);
+        bulk_g2s(slots + lane * DEC_STAGE_BYTES, src0, bytes0, &full[lane]);
+      }
+      base0 = 32;
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     int done = n_total;           // chunks before this one were all issued
     bool mine = false;            // this lane issued its chunk of the batch that stopped early
-    for (int base = 0; base < n_total; base += 32) {
+    for (int base = base0; base < n_total; base += 32) {
       const int c = base + lane;
       bool good = true;
       mine = false;
@@ -474,7 +697,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
       const bool valid[1][2] = {{r0, r1}};
       online_step<1>(sacc, valid, m_run, l_run, o, macc, tsum, io.scale_log2);
       uint32_t pb[1][2];
-      p_to_b<1>(sacc, pb);
+      p_to_b<1>(sacc, pb, OScale<BITS>::P);
       const int t0 = 2 * tl, t1 = 2 * tl + 8;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -553,7 +776,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
         }
         online_step<NMT>(s, valid, m_run, l_run, o, macc, tsum, io.scale_log2);
         uint32_t pb[NMT][2];
-        p_to_b<NMT>(s, pb);
+        p_to_b<NMT>(s, pb, OScale<BITS>::P);
         const uint8_t *vc[NMT];
 #pragma unroll
         for (int kk = 0; kk < NMT; ++kk) vc[kk] = wait_chunk(c0 + KCH + 2 * hv + kk);
@@ -586,129 +809,94 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
         for (int kk = 0; kk < NMT; ++kk) release_chunk(c0 + KCH + 2 * hv + kk);
         add_half_mass();
       }
+    } else if constexpr (BITS == 2 && !ROPE) {
+      // ---------------- Quantized windows, W = 32, two per item: INT2 codes + fp16 scale/offset in one
+      // chunk each.  The two windows' key products run as interleaved MMA chains and share one online
+      // softmax step over their 64 tokens; their masses stay separate.
+      const int qi = it - 1 - nL - nF;          // Q-table index of the first window
+      const bool hasB = qi + 1 < Q1;            // the item's second window
+      const uint8_t *ch[2];
+      ch[0] = wait_chunk(c0);
+      ch[1] = hasB ? wait_chunk(c0 + 1) : ch[0];
+      ktab_int2(ch[0], tbl, lane);
+      ktab_int2(ch[1], tbl + DEC_TBL_BYTES, lane);
+      __syncwarp();
+      uint4 kc[2][2];
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {
+        kc[w][0] = lds128(ch[w] + lane * 16);
+        kc[w][1] = lds128(ch[w] + 512 + lane * 16);
+      }
+      float s2[2][2][4];
+#pragma unroll
+      for (int w = 0; w < 2; ++w)
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) s2[w][mt][0] = s2[w][mt][1] = s2[w][mt][2] = s2[w][mt][3] = 0.f;
+      keys_int2<2>(kc, tbl, qb, s2, tl);
+      const bool vw[2] = {true, hasB};
+      float ts[2];
+      online_step_w<2>(s2, vw, m_run, l_run, o, macc, ts, io.scale_log2);
+      pv_int2(s2[0], ch[0], o, macc, lane);
+      if (hasB) pv_int2(s2[1], ch[1], o, macc, lane);
+      __syncwarp();
+      release_chunk(c0);
+      if (hasB) release_chunk(c0 + 1);
+      // the windows' log2-sum-exp per head (see below), under their stable indices
+      if (gl < 2 && 2 * tl + gl < G) {
+        const float mr = gl & 1 ? m_run[1] : m_run[0];
+        const int sidx = 1 + qi + C.loc_items() + C.kf_cap();   // as for single windows below
+        mu[(size_t)sidx * 8 + 2 * tl + gl] = ts[0] > 0.f ? mr + __log2f(ts[0]) : -INFINITY;
+        if (hasB) mu[(size_t)(sidx + 1) * 8 + 2 * tl + gl] = ts[1] > 0.f ? mr + __log2f(ts[1]) : -INFINITY;
+      }
+      continue;
     } else if constexpr (BITS == 2) {
-      // ---------------- Quantized window, W = 32: INT2 codes + fp16 scale/offset in one chunk
+      // ---------------- Quantized window with pre-RoPE keys, W = 32: INT2 codes + fp16 scale/offset
+      // in one chunk
       bool valid[NMT][2];
       float s[NMT][4];
 #pragma unroll
       for (int mt = 0; mt < NMT; ++mt) s[mt][0] = s[mt][1] = s[mt][2] = s[mt][3] = 0.f;
-      float4 csr;   // ROPE: this lane's 16 B of the RoPE row of the window's first position
-      if constexpr (ROPE) {
-        const int wq = __ldg(&qtab[it - 1 - nL - nF].x);
-        csr = __ldg(reinterpret_cast<const float4 *>(C.rope_tab() + (size_t)(C.n_sink + wq * W) * D) + lane);
-      }
+      // this lane's 16 B of the RoPE row of the window's first position
+      const int wq = __ldg(&qtab[it - 1 - nL - nF].x);
+      const float4 csr = __ldg(reinterpret_cast<const float4 *>(C.rope_tab() + (size_t)(C.n_sink + wq * W) * D) + lane);
       const uint8_t *ch = wait_chunk(c0);
-      // key tables: channel d = 4*lane + k, values bf16(fp32(c*s + m)), c = 0..3, split in lo / hi bytes
-      {
-        const uint2 sp = *reinterpret_cast<const uint2 *>(ch + Gm::OFF_KS + 8 * lane);
-        const uint2 mp = *reinterpret_cast<const uint2 *>(ch + Gm::OFF_KM + 8 * lane);
-        uint32_t *tw = reinterpret_cast<uint32_t *>(tbl);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t sw = k < 2 ? sp.x : sp.y, mw = k < 2 ? mp.x : mp.y;
-          const float sc = (k & 1) ? h2f_hi(sw) : h2f_lo(sw);
-          const float mn = (k & 1) ? h2f_hi(mw) : h2f_lo(mw);
-          const uint32_t p01 = pack_bf16(mn, __fadd_rn(sc, mn));
-          const uint32_t p23 = pack_bf16(__fmaf_rn(2.f, sc, mn), __fmaf_rn(3.f, sc, mn));
-          const int d = 4 * lane + k, j = d >> 4, c16 = d & 15;
-          const int t = (c16 & 7) >> 1, which = c16 >> 3, half = c16 & 1;
-          const int base = (j * 4 + t) * 8 + which * 4 + half;
-          tw[base] = __byte_perm(p01, p23, 0x6420);
-          tw[base + 2] = __byte_perm(p01, p23, 0x7531);
-        }
-      }
-      if constexpr (ROPE) *reinterpret_cast<float4 *>(tbl + DEC_TBL_BYTES + 16 * lane) = cc_ss(csr);
+      ktab_int2(ch, tbl, lane);
+      *reinterpret_cast<float4 *>(tbl + 2 * DEC_TBL_BYTES + 16 * lane) = cc_ss(csr);
       __syncwarp();
       const uint4 kcw0 = lds128(ch + lane * 16), kcw1 = lds128(ch + 512 + lane * 16);
-      if constexpr (ROPE) {
-        // k-steps jj and jj + 4 hold the RoPE partners (channels c and c + 64) in the same registers
+      // k-steps jj and jj + 4 hold the RoPE partners (channels c and c + 64) in the same registers
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const uint4 TA0 = lds128(tbl + (jj * 4 + tl) * 32), TB0 = lds128(tbl + (jj * 4 + tl) * 32 + 16);
-          const uint4 TA1 = lds128(tbl + ((jj + 4) * 4 + tl) * 32), TB1 = lds128(tbl + ((jj + 4) * 4 + tl) * 32 + 16);
-          const uint8_t *csw = tbl + DEC_TBL_BYTES + (16 * jj + 2 * tl) * 8;
-          const float4 cb0 = *reinterpret_cast<const float4 *>(csw), cb1 = *reinterpret_cast<const float4 *>(csw + 64);
-          const float2 ncb0 = make_float2(-cb0.z, -cb0.w), ncb1 = make_float2(-cb1.z, -cb1.w);
-#pragma unroll
-          for (int mt = 0; mt < NMT; ++mt) {
-            // k-step j sits in code word j / 2, low half for even j
-            const uint4 &kc = mt == 0 ? kcw0 : kcw1;
-            const uint32_t wa = word_of(kc, jj >> 1) >> (16 * (jj & 1));
-            const uint32_t wb = word_of(kc, 2 + (jj >> 1)) >> (16 * (jj & 1));
-            uint32_t ka[4], kb[4];
-            lut_k_regs((wa & 0x3333u) | 0x4040u, ((wa >> 2) & 0x3333u) | 0x4040u, TA0, TB0, ka[0], ka[1], ka[2], ka[3]);
-            lut_k_regs((wb & 0x3333u) | 0x4040u, ((wb >> 2) & 0x3333u) | 0x4040u, TA1, TB1, kb[0], kb[1], kb[2], kb[3]);
-#pragma unroll
-            for (int r = 0; r < 4; ++r) {
-              const int tt = 16 * mt + gl + 8 * (r & 1);
-              rope_rot(bf_lo(ka[r]), bf_hi(ka[r]), bf_lo(kb[r]), bf_hi(kb[r]), (r >> 1) ? cb1 : cb0, (r >> 1) ? ncb1 : ncb0,
-                       rel_cs(rel, tt, jj, r >> 1, tl), ka[r], kb[r]);
-            }
-            mma_bf16(s[mt], ka[0], ka[1], ka[2], ka[3], qb[jj][0], qb[jj][1]);
-            mma_bf16(s[mt], kb[0], kb[1], kb[2], kb[3], qb[jj + 4][0], qb[jj + 4][1]);
-          }
-        }
-      } else {
-#pragma unroll
-      for (int jp = 0; jp < 4; ++jp) {
-        // selectors of both fields of a code word at once: k-step 2jp in the low half, 2jp+1 high
-        uint32_t sa[NMT], sb[NMT];
+      for (int jj = 0; jj < 4; ++jj) {
+        const uint4 TA0 = lds128(tbl + (jj * 4 + tl) * 32), TB0 = lds128(tbl + (jj * 4 + tl) * 32 + 16);
+        const uint4 TA1 = lds128(tbl + ((jj + 4) * 4 + tl) * 32), TB1 = lds128(tbl + ((jj + 4) * 4 + tl) * 32 + 16);
+        const uint8_t *csw = tbl + 2 * DEC_TBL_BYTES + (16 * jj + 2 * tl) * 8;
+        const float4 cb0 = *reinterpret_cast<const float4 *>(csw), cb1 = *reinterpret_cast<const float4 *>(csw + 64);
+        const float2 ncb0 = make_float2(-cb0.z, -cb0.w), ncb1 = make_float2(-cb1.z, -cb1.w);
 #pragma unroll
         for (int mt = 0; mt < NMT; ++mt) {
-          const uint32_t wd = word_of(mt == 0 ? kcw0 : kcw1, jp);
-          sa[mt] = (wd & 0x33333333u) | 0x40404040u;
-          sb[mt] = ((wd >> 2) & 0x33333333u) | 0x40404040u;
-        }
+          // k-step j sits in code word j / 2, low half for even j
+          const uint4 &kc = mt == 0 ? kcw0 : kcw1;
+          const uint32_t wa = word_of(kc, jj >> 1) >> (16 * (jj & 1));
+          const uint32_t wb = word_of(kc, 2 + (jj >> 1)) >> (16 * (jj & 1));
+          uint32_t ka[4], kb[4];
+          lut_k_regs((wa & 0x3333u) | 0x4040u, ((wa >> 2) & 0x3333u) | 0x4040u, TA0, TB0, ka[0], ka[1], ka[2], ka[3]);
+          lut_k_regs((wb & 0x3333u) | 0x4040u, ((wb >> 2) & 0x3333u) | 0x4040u, TA1, TB1, kb[0], kb[1], kb[2], kb[3]);
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const int j = 2 * jp + hf;
-          const uint4 TA = lds128(tbl + (j * 4 + tl) * 32);
-          const uint4 TB = lds128(tbl + (j * 4 + tl) * 32 + 16);
-#pragma unroll
-          for (int mt = 0; mt < NMT; ++mt) {
-            uint32_t a0, a1, a2, a3;
-            lut_k_regs(hf ? sa[mt] >> 16 : sa[mt], hf ? sb[mt] >> 16 : sb[mt], TA, TB, a0, a1, a2, a3);
-            mma_bf16(s[mt], a0, a1, a2, a3, qb[j][0], qb[j][1]);
+          for (int r = 0; r < 4; ++r) {
+            const int tt = 16 * mt + gl + 8 * (r & 1);
+            rope_rot(bf_lo(ka[r]), bf_hi(ka[r]), bf_lo(kb[r]), bf_hi(kb[r]), (r >> 1) ? cb1 : cb0, (r >> 1) ? ncb1 : ncb0,
+                     rel_cs(rel, tt, jj, r >> 1, tl), ka[r], kb[r]);
           }
+          mma_bf16(s[mt], ka[0], ka[1], ka[2], ka[3], qb[jj][0], qb[jj][1]);
+          mma_bf16(s[mt], kb[0], kb[1], kb[2], kb[3], qb[jj + 4][0], qb[jj + 4][1]);
         }
-      }
       }
 #pragma unroll
       for (int mt = 0; mt < NMT; ++mt) {
         valid[mt][0] = valid[mt][1] = true;
       }
       online_step<NMT>(s, valid, m_run, l_run, o, macc, tsum, io.scale_log2);
-      // values: o += sum_tok (p * s_tok) * code + (sum_tok p * m_tok) in every dim
-      uint32_t pbh[NMT][2];
-      float pm0 = 0.f, pm1 = 0.f;
-      const __half *vsp = reinterpret_cast<const __half *>(ch + Gm::OFF_VS);
-      const __half *vmp = reinterpret_cast<const __half *>(ch + Gm::OFF_VM);
-#pragma unroll
-      for (int kk = 0; kk < NMT; ++kk) {
-        const int t0 = 16 * kk + gl, t1 = t0 + 8;
-        const float s0v = __half2float(vsp[t0]), s1v = __half2float(vsp[t1]);
-        const float m0v = __half2float(vmp[t0]), m1v = __half2float(vmp[t1]);
-        fma2(pm0, pm1, s[kk][2], s[kk][3], m1v, m1v, pm0, pm1);
-        fma2(pm0, pm1, s[kk][0], s[kk][1], m0v, m0v, pm0, pm1);
-        float x0, x1, x2, x3;
-        mul2(x0, x1, s[kk][0], s[kk][1], s0v, s0v);
-        mul2(x2, x3, s[kk][2], s[kk][3], s1v, s1v);
-        pbh[kk][0] = movmatrix_trans(pack_half(x0, x1));
-        pbh[kk][1] = movmatrix_trans(pack_half(x2, x3));
-      }
-      macc[0] += pm0;
-      macc[1] += pm1;
-      const uint4 vw0 = lds128(ch + Gm::OFF_VCODE + lane * 16), vw1 = lds128(ch + Gm::OFF_VCODE + 512 + lane * 16);
-#pragma unroll
-      for (int kk = 0; kk < NMT; ++kk) {
-#pragma unroll
-        for (int ip = 0; ip < 4; ++ip) {
-          const uint32_t w = word_of(kk == 0 ? vw0 : vw1, ip);
-          const uint32_t w10 = w >> 10;
-          mma_f16(o[2 * ip], dq_v(w, 0), dq_v(w, 1), dq_v(w, 2), dq_v(w, 3), pbh[kk][0], pbh[kk][1]);
-          mma_f16(o[2 * ip + 1], dq_v(w, 4), dq_v(w10, 0), dq_v(w10, 1), dq_v(w10, 2), pbh[kk][0], pbh[kk][1]);
-        }
-      }
+      pv_int2(s, ch, o, macc, lane);
       __syncwarp();
       release_chunk(c0);
       add_half_mass();
@@ -876,8 +1064,9 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         float *r = cO + ((size_t)warp * D + 16 * i + gl) * 8 + 2 * tl;
-        *reinterpret_cast<float2 *>(r) = make_float2(o[i][0] + macc[0], o[i][1] + macc[1]);
-        *reinterpret_cast<float2 *>(r + 64) = make_float2(o[i][2] + macc[0], o[i][3] + macc[1]);
+        constexpr float U = OScale<BITS>::INV;   // the accumulators' scale, undone here
+        *reinterpret_cast<float2 *>(r) = make_float2(fmaf(o[i][0], U, macc[0]), fmaf(o[i][1], U, macc[1]));
+        *reinterpret_cast<float2 *>(r + 64) = make_float2(fmaf(o[i][2], U, macc[0]), fmaf(o[i][3], U, macc[1]));
       }
     }
   }

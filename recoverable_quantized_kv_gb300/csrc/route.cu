@@ -368,8 +368,9 @@ __global__ void __launch_bounds__(RT_THREADS, 1) route_kernel(const CacheDev C, 
   const int nQ = block_exscan(rankL, n_new, wsum);
   for (int w = tid; w < n_new; w += nt) {
     const int t = state[w] & 3;
-    if (t == TIER_FULL) ftab[rankF[w]] = make_int2(w, fslot[w]);
-    if (t == TIER_QUANT) qtab[rankL[w]] = make_int2(w, lslot[w]);
+    if (t == TIER_FULL && qv_inbounds(rankF[w] < kf_cap, C.status())) ftab[rankF[w]] = make_int2(w, fslot[w]);
+    if (t == TIER_QUANT && qv_inbounds(rankL[w] < min(C.k_q, N), C.status()))
+      qtab[rankL[w]] = make_int2(w, lslot[w]);
   }
   const int tp = block_sum(c_promo, wsum), td = block_sum(c_demo, wsum), tf = block_sum(c_firstq, wsum);
   const int tr = block_sum(c_react, wsum), te = block_sum(c_evict, wsum), ta = block_sum(c_agedf, wsum);
@@ -456,9 +457,17 @@ __global__ void __launch_bounds__(MIG_THREADS) quant_kernel(const CacheDev C, co
   const int4 *qtask = C.at<const int4>(C.off_qtask, C.st_qtask, unit);
   uint8_t *ledger = C.at<uint8_t>(C.off_ledger, C.st_ledger, unit);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int kf_cap = min(C.k_f, C.n_windows), lp_cap = min(C.k_f + C.k_q, C.n_windows);
+  if (!qv_inbounds(ntask >= 0 && ntask <= C.n_windows, C.status())) return;
   for (int job = blockIdx.x; job < ntask * C.h_kv; job += gridDim.x) {
     const int4 tk = qtask[job / C.h_kv];
     const int g = job % C.h_kv;
+    // task: window, source kind, source (F slot / window id / prompt window), ledger slot
+    const bool src_ok = tk.y == SRC_FSLOT ? (tk.z >= 0 && tk.z < kf_cap)
+                      : tk.y == SRC_RING  ? (tk.z >= 0 && tk.z < C.n_windows)
+                      : tk.y == SRC_PROMPT && tk.z >= 0 && C.n_sink + (tk.z + 1) * W <= C.prompt_len;
+    if (!qv_inbounds(src_ok && tk.x >= 0 && tk.x < C.n_windows && tk.w >= 0 && tk.w < lp_cap, C.status()))
+      continue;   // the same for every thread of the CTA
     __syncthreads();
     load_window<W>(C, pio, unit, b, g, tk.y, tk.z, xk, xv);
     for (int i = threadIdx.x; i < 2 * Gm::CODE_BYTES / 4; i += blockDim.x) cw[i] = 0u;
@@ -540,9 +549,18 @@ __global__ void __launch_bounds__(MIG_THREADS) move_kernel(const CacheDev C, con
   const __nv_bfloat16 *ring = C.at<const __nv_bfloat16>(C.off_ring, C.st_ring, unit);
   __nv_bfloat16 *fpool = C.at<__nv_bfloat16>(C.off_fpool, C.st_fpool, unit);
   const int tid = threadIdx.x;
+  const int kf_cap = min(C.k_f, C.n_windows), lp_cap = min(C.k_f + C.k_q, C.n_windows);
+  if (!qv_inbounds(ntask >= 0 && ntask <= C.n_windows, C.status())) return;
   for (int job = blockIdx.x; job < ntask * C.h_kv; job += gridDim.x) {
     const int4 tk = mtask[job / C.h_kv];
     const int g = job % C.h_kv;
+    // task: window, kind | source kind << 4, source (ledger slot / window id / prompt window), F slot
+    const int k0 = tk.y & 15, s0k = tk.y >> 4;
+    const bool src_ok = k0 == MOVE_PROMOTE ? (tk.z >= 0 && tk.z < lp_cap)
+                      : s0k == SRC_RING    ? (tk.z >= 0 && tk.z < C.n_windows)
+                      : s0k == SRC_PROMPT && tk.z >= 0 && C.n_sink + (tk.z + 1) * W <= C.prompt_len;
+    if (!qv_inbounds(src_ok && tk.x >= 0 && tk.x < C.n_windows && tk.w >= 0 && tk.w < kf_cap, C.status()))
+      continue;   // the same for every thread of the CTA
     __nv_bfloat16 *dk = fpool + ((size_t)tk.w * C.h_kv + g) * 2 * Gm::BLK;
     __nv_bfloat16 *dv = dk + Gm::BLK;
     const int kind = tk.y & 15, src_kind = tk.y >> 4;

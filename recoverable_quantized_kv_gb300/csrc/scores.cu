@@ -410,7 +410,9 @@ __global__ void __launch_bounds__(256) flush_kernel(const CacheDev C, float inv_
   if (threadIdx.x < 8) s_meta[threadIdx.x] = meta[threadIdx.x];
   __syncthreads();
   const int T = s_meta[M_T], F = s_meta[M_FLUSHT], j0 = s_meta[M_NROUTE];
-  const int nF = s_meta[M_FCOUNT], nQ = s_meta[M_QCOUNT];
+  int nF = s_meta[M_FCOUNT], nQ = s_meta[M_QCOUNT];
+  if (!qv_inbounds(nF >= 0 && nF <= C.kf_cap() && nQ >= 0 && nQ <= min(C.k_q, C.n_windows), C.status()))
+    nF = nQ = 0;
   const int nk = T - F;
   if (nk < 0 || nk > C.omega) {
     if (threadIdx.x == 0) atomicOr(C.status(), QV_ERR_STATE);
@@ -442,6 +444,7 @@ __global__ void __launch_bounds__(256) flush_kernel(const CacheDev C, float inv_
         if (q >= nQ) continue;
         w = qtab[q].x;
       }
+      if (!qv_inbounds(w >= 0 && w < C.n_windows, C.status())) continue;
       float s = score[w];
       for (int k = k0; k < nk; ++k) {
         const float *m = mu + ((size_t)k * C.max_items + idx) * 8;

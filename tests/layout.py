@@ -49,12 +49,11 @@ def code_position(W, bits, is_v):
         lb = grp * 2 + bit // 8
     else:
         r, c = dim % 16, tok % 16
-        lane, reg = _frag(r, c)
-        i = dim // 16
-        rr = (i % 2) * 4 + reg
-        w = (tok // 16) * 4 + i // 2
-        bit = np.where(rr < 5, 2 * rr, 10 + 2 * (rr - 5)) + 16 * (c % 2)
-        lb = 4 * w + bit // 8
+        lane, _ = _frag(r, c)
+        i = dim // 16                        # word i of the lane's 32 bytes
+        tau = 2 * (tok // 16) + c // 8       # token pair of the A register
+        bit = 8 * (r // 8) + 2 * tau + 16 * (c % 2)
+        lb = 4 * i + bit // 8
     byte = (lb // 16) * 512 + lane * 16 + lb % 16
     return byte.reshape(W, D), (bit % 8).reshape(W, D)
 

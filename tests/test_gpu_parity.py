@@ -205,6 +205,10 @@ def test_full_size_llama_shape(lib):
     ("long_131k", dict(n_layers=1, batch=1, steps=8, window=64, bits=4), 8, None),
     # pre-RoPE Quantized keys at positions up to 131K (RoPE base 500000)
     ("long_131k", dict(n_layers=1, batch=1, steps=8, rope_base=500000.0), 8, None),
+    # the corners of the budget x q sweep at 131K: 10% with q = 0.9 (the most Quantized-heavy point,
+    # full state checked) and 40% with q = 0.5 (the most Full-heavy)
+    ("long_131k", dict(n_layers=1, batch=1, steps=8, budget_num=10, q_num=90), 8, [0]),
+    ("long_131k", dict(n_layers=1, batch=1, steps=8, budget_num=40, q_num=50), 8, None),
 ])
 def test_full_size_workloads(lib, name, over, steps, state_seqs):
     """The other workloads at their full per-layer shapes (one layer each), in lockstep: outputs,
@@ -310,6 +314,7 @@ def test_slot_exhaustion_guard(lib):
     with pytest.raises(binding.QEvictError) as e:
         ls.cache.check()
     assert e.value.status == binding.EDEVICE
+    assert ls.cache.status_word() == 2                           # the slot bit alone
     for k, t in before.items():
         assert torch.equal(ls.cache.region(k, u, regions[k]), t), k
     m = ls.meta(0, 0)
@@ -334,6 +339,7 @@ def test_wait_timeout_is_reported_and_recoverable(lib):
         with pytest.raises(binding.QEvictError) as e:
             call()
         assert e.value.status == binding.EDEVICE
+    assert ls.cache.status_word() == 1                           # the timeout bit alone
     after = ls.cache.export_state()
     diff = np.flatnonzero(snap != after)
     # one byte changed: the low byte of the status word, 0 -> the timeout bit
