@@ -166,7 +166,8 @@ void make_plan(const qevict_config *c, const qevict_budget_info *b, Plan *p) {
   C.off_thead = global(4LL * c->n_layers * c->batch * c->h_kv);
   C.st_part_layer = align256(4LL * c->batch * c->h_kv * n_split * qv::PART_FLOATS);
   C.off_part = global(C.st_part_layer * c->n_layers);
-  C.st_mu_layer = align256(4LL * c->batch * c->h_kv * c->omega * max_items * 8);
+  // per-step window log-masses: one record of G floats (the KV head's query heads) per item
+  C.st_mu_layer = align256(4LL * c->batch * c->h_kv * c->omega * max_items * (c->h_q / c->h_kv));
   C.off_mu = global(C.st_mu_layer * c->n_layers);
   C.st_mstat_layer = align256(4LL * c->batch * c->h_kv * c->omega * 16);
   C.off_mstat = global(C.st_mstat_layer * c->n_layers);

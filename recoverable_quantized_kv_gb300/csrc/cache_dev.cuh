@@ -33,7 +33,7 @@ struct CacheDev {
   int64_t off_part, st_part_layer; // float [L][B][h_kv][n_split][PART_FLOATS]
   // per-window log2-sum-exp of the decode steps since the last score flush, by step slot
   // (tokens cached at the step minus those at the flush) and stable item index
-  int64_t off_mu, st_mu_layer;     // float [L][B][h_kv][omega][max_items][8]
+  int64_t off_mu, st_mu_layer;     // float [L][B][h_kv][omega][max_items][G]
   int64_t off_mstat, st_mstat_layer;   // float [L][B][h_kv][omega][16]: merged max M[8], 1/L[8] per step
   int64_t off_flushctr;            // uint32 [L][B] score-flush arrivals
   int64_t off_rowstat;             // float [B][h_q][P] prefill row log2-sum-exp

@@ -495,7 +495,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   const uint8_t *ledger = C.at<const uint8_t>(C.off_ledger, C.st_ledger, unit);
   const int bg = b * C.h_kv + g;
   float *mu = reinterpret_cast<float *>(C.arena + C.off_mu + C.st_mu_layer * io.layer) +
-              ((size_t)bg * C.omega + mslot) * C.max_items * 8;
+              ((size_t)bg * C.omega + mslot) * C.max_items * G;
   float *part = reinterpret_cast<float *>(C.arena + C.off_part + C.st_part_layer * io.layer) +
                 (size_t)bg * C.n_split * PART_FLOATS;
 
@@ -601,17 +601,24 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   if (producer) {
     // ---------------- producer warp: lane l issues chunk base + l of every batch of 32; a chunk
     // reuses its slot once the consumer of the chunk DEC_SLOTS earlier has released it
-    // The cache windows of this layer do not depend on the previous kernel, so the first batch of
-    // copies goes out before the wait, on an SM the previous kernel has already left.  (When the
+    // The cache windows of this layer do not depend on the previous kernel, so the first copies go
+    // out before the wait, on an SM the previous kernel has already left.  (When the
     // previous kernel may be this layer's own decode, everything waited above.)
+    // How many: the previous layer's last CTAs are merging their splits from L2 meanwhile, and a deep
+    // burst of copies delays those loads; 16 chunks measured best for INT2, the whole batch for INT4.
+    constexpr int PRE = BITS == 2 ? 16 : 32;
     int base0 = 0;
     if (!io.wait_first) {
-      if (lane < n_total) {
+      if (lane < PRE && lane < n_total) {
         mbar_arrive_expect_tx(&full[lane], bytes0);
         bulk_g2s(slots + lane * DEC_STAGE_BYTES, src0, bytes0, &full[lane]);
       }
       base0 = 32;
       asm volatile("griddepcontrol.wait;" ::: "memory");
+      if (lane >= PRE && lane < n_total) {   // the rest of the first batch
+        mbar_arrive_expect_tx(&full[lane], bytes0);
+        bulk_g2s(slots + lane * DEC_STAGE_BYTES, src0, bytes0, &full[lane]);
+      }
     }
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     int done = n_total;           // chunks before this one were all issued
@@ -845,8 +852,8 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
       if (gl < 2 && 2 * tl + gl < G) {
         const float mr = gl & 1 ? m_run[1] : m_run[0];
         const int sidx = 1 + qi + C.loc_items() + C.kf_cap();   // as for single windows below
-        mu[(size_t)sidx * 8 + 2 * tl + gl] = ts[0] > 0.f ? mr + __log2f(ts[0]) : -INFINITY;
-        if (hasB) mu[(size_t)(sidx + 1) * 8 + 2 * tl + gl] = ts[1] > 0.f ? mr + __log2f(ts[1]) : -INFINITY;
+        mu[(size_t)sidx * G + 2 * tl + gl] = ts[0] > 0.f ? mr + __log2f(ts[0]) : -INFINITY;
+        if (hasB) mu[(size_t)(sidx + 1) * G + 2 * tl + gl] = ts[1] > 0.f ? mr + __log2f(ts[1]) : -INFINITY;
       }
       continue;
     } else if constexpr (BITS == 2) {
@@ -1039,7 +1046,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
     // L; recorded under the window's stable index (recent, then Full, then Quantized)
     if (gl < 2 && 2 * tl + gl < G) {
       const int sidx = it <= nL ? it : (it <= nL + nF ? it - nL + C.loc_items() : it - nL - nF + C.loc_items() + C.kf_cap());
-      mu[(size_t)sidx * 8 + 2 * tl + gl] = wmu;
+      mu[(size_t)sidx * G + 2 * tl + gl] = wmu;
     }
   }
   }   // consumer warps
@@ -1108,45 +1115,65 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   __syncthreads();
   if (!s_last) return;
 
-  // outputs: one warp covers 32 dims of one head; lane sp holds split sp's (m, l), the merged max
-  // M and sum L come from warp reductions, and each lane folds every split's output for its dim
+  // outputs: one warp covers 32 dims of one head; lane sp holds split sp's (m, l), the merged max M
+  // and sum L come from warp reductions, and each lane folds every split's output for its dim.  A
+  // thread may own several (head, dim) items: the loads of all of them are issued before any is
+  // used, so the partials cross the L2 once (per 32 splits).
   const int nsp = C.n_split;
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-    const int h = idx / D, d = idx % D;
-    const float *ph = part + h, *po = part + 16 + h * D + d;
-    float M = -INFINITY, L = 0.f, O = 0.f;
-    for (int s0 = 0; s0 < nsp; s0 += 32) {
-      const int n = min(32, nsp - s0);
-      float ov[32];
+  constexpr int IPT = (8 * D + DEC_WARPS * 32 - 1) / (DEC_WARPS * 32);   // (head, dim) items per thread
+  float M[IPT], L[IPT], O[IPT];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) ov[k] = k < n ? __ldcg(po + (size_t)(s0 + k) * PART_FLOATS) : 0.f;
-      const float l = lane < n ? __ldcg(ph + (size_t)(s0 + lane) * PART_FLOATS + 8) : 0.f;
-      const float m = lane < n ? __ldcg(ph + (size_t)(s0 + lane) * PART_FLOATS) : -INFINITY;
+  for (int k = 0; k < IPT; ++k) M[k] = -INFINITY, L[k] = 0.f, O[k] = 0.f;
+  for (int s0 = 0; s0 < nsp; s0 += 32) {
+    const int n = min(32, nsp - s0);
+    float ov[IPT][32], lk[IPT], mk[IPT];
+#pragma unroll
+    for (int k = 0; k < IPT; ++k) {
+      const int idx = threadIdx.x + k * DEC_WARPS * 32;   // the same head across a warp (D % 32 == 0)
+      const bool valid = idx < G * D;
+      const int h = valid ? idx / D : 0;
+      const float *po = part + 16 + (valid ? idx : 0) + (size_t)s0 * PART_FLOATS;
+#pragma unroll
+      for (int x = 0; x < 32; ++x) ov[k][x] = (valid && x < n) ? __ldcg(po + (size_t)x * PART_FLOATS) : 0.f;
+      const float *ph = part + h + (size_t)(s0 + lane) * PART_FLOATS;
+      lk[k] = (valid && lane < n) ? __ldcg(ph + 8) : 0.f;
+      mk[k] = (valid && lane < n) ? __ldcg(ph) : -INFINITY;
+    }
+#pragma unroll
+    for (int k = 0; k < IPT; ++k) {
+      if (threadIdx.x + k * DEC_WARPS * 32 >= G * D) continue;   // uniform over the warp
+      const float l = lk[k], m = mk[k];
       float Mc = l > 0.f ? m : -INFINITY;
 #pragma unroll
       for (int x = 16; x >= 1; x >>= 1) Mc = fmaxf(Mc, __shfl_xor_sync(0xffffffffu, Mc, x));
-      const float Mn = fmaxf(M, Mc);   // finite: the newest token's window always holds mass
-      const float cold = M == -INFINITY ? 0.f : exp2f(M - Mn);
+      const float Mn = fmaxf(M[k], Mc);   // finite: the newest token's window always holds mass
+      const float cold = M[k] == -INFINITY ? 0.f : exp2f(M[k] - Mn);
       const float e = l > 0.f ? exp2f(m - Mn) : 0.f;
       float Lc = l * e;
 #pragma unroll
       for (int x = 16; x >= 1; x >>= 1) Lc += __shfl_xor_sync(0xffffffffu, Lc, x);
       float Oc0 = 0.f, Oc1 = 0.f;
 #pragma unroll
-      for (int k = 0; k < 32; k += 2) {
-        Oc0 = fmaf(ov[k], __shfl_sync(0xffffffffu, e, k), Oc0);
-        Oc1 = fmaf(ov[k + 1], __shfl_sync(0xffffffffu, e, k + 1), Oc1);
+      for (int x = 0; x < 32; x += 2) {
+        Oc0 = fmaf(ov[k][x], __shfl_sync(0xffffffffu, e, x), Oc0);
+        Oc1 = fmaf(ov[k][x + 1], __shfl_sync(0xffffffffu, e, x + 1), Oc1);
       }
-      L = fmaf(L, cold, Lc);
-      O = fmaf(O, cold, Oc0 + Oc1);
-      M = Mn;
+      L[k] = fmaf(L[k], cold, Lc);
+      O[k] = fmaf(O[k], cold, Oc0 + Oc1);
+      M[k] = Mn;
     }
-    const float inv = 1.f / L;
-    io.out[((size_t)b * C.h_q + (size_t)g * G + h) * D + d] = __float2bfloat16_rn(O * inv);
+  }
+#pragma unroll
+  for (int k = 0; k < IPT; ++k) {
+    const int idx = threadIdx.x + k * DEC_WARPS * 32;
+    if (idx >= G * D) continue;
+    const int h = idx / D, d = idx % D;
+    const float inv = 1.f / L[k];
+    io.out[((size_t)b * C.h_q + (size_t)g * G + h) * D + d] = __float2bfloat16_rn(O[k] * inv);
     if (d == 0) {   // this step's merged max and 1/L: the window masses are applied when scores are flushed
       float *ms = reinterpret_cast<float *>(C.arena + C.off_mstat + C.st_mstat_layer * io.layer) +
                   ((size_t)bg * C.omega + mslot) * 16;
-      ms[h] = M;
+      ms[h] = M[k];
       ms[8 + h] = inv;
     }
   }

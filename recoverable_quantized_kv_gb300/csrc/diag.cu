@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(DG_COLLECT_THREADS) diag_collect_kernel(const 
   }
   __syncthreads();
   const float *mu = reinterpret_cast<const float *>(R.arena + R.off_mu + R.st_mu_layer * layer) +
-                    (size_t)bg * R.omega * R.max_items * 8;
+                    (size_t)bg * R.omega * R.max_items * R.G;
   const int2 *ftab = R.at<const int2>(R.off_ftab, R.st_ftab, unit);
   const int2 *qtab = R.at<const int2>(R.off_qtab, R.st_qtab, unit);
   const int *evict = Dg.evict(unit);
@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(DG_COLLECT_THREADS) diag_collect_kernel(const 
     for (int k = k0; k < nk; ++k) {
       const unsigned me = evb & s_inh[k], mn = nxb & s_inh[k];
       if (!(me | mn)) continue;
-      const float *m = mu + ((size_t)k * R.max_items + idx) * 8;
+      const float *m = mu + ((size_t)k * R.max_items + idx) * R.G;
       const float *Mk = st + k * 16;
 #pragma unroll
       for (int h = 0; h < 8; ++h) {

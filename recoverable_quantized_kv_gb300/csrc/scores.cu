@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(256) flush_kernel(const CacheDev C, float inv_
     for (int i = threadIdx.x; i < nk * 16; i += blockDim.x) st[i] = ms[i];
     __syncthreads();
     const float *mu = reinterpret_cast<const float *>(C.arena + C.off_mu + C.st_mu_layer * layer) +
-                      (size_t)bg * C.omega * C.max_items * 8;
+                      (size_t)bg * C.omega * C.max_items * C.G;
     float *score = C.at<float>(C.off_score, C.st_score, unit) + (size_t)g * C.n_windows;
     const int2 *ftab = C.at<const int2>(C.off_ftab, C.st_ftab, unit);
     const int2 *qtab = C.at<const int2>(C.off_qtab, C.st_qtab, unit);
@@ -447,7 +447,7 @@ __global__ void __launch_bounds__(256) flush_kernel(const CacheDev C, float inv_
       if (!qv_inbounds(w >= 0 && w < C.n_windows, C.status())) continue;
       float s = score[w];
       for (int k = k0; k < nk; ++k) {
-        const float *m = mu + ((size_t)k * C.max_items + idx) * 8;
+        const float *m = mu + ((size_t)k * C.max_items + idx) * C.G;
         const float *Mk = st + k * 16;
         float a = 0.f;
         for (int h = 0; h < G; ++h) a = fmaf(exp2f(m[h] - Mk[h]), Mk[8 + h], a);
