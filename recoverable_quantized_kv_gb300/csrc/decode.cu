@@ -7,12 +7,13 @@
 // Grid (n_split, h_kv, batch).  Each CTA owns a proportional slice of the recent, Full and
 // Quantized windows of one (sequence, KV head).  One producer warp streams the slice's windows
 // through a CTA-wide ring of 4 KB shared-memory slots with 1-D bulk copies (TMA), each completing on
-// an mbarrier; fifteen consumer warps take windows from a shared queue, wait for their chunks,
-// compute, and release the slots.  The G query heads of the KV head ride on the N side of
-// mma.m16n8k16 (tokens on M for Q K^T, dims on M for P V), so both products run on tensor cores.
-// Softmax is online per warp; per-window masses are kept as log2-sum-exp values, which the last CTA
-// of the (sequence, KV head) to finish (counted with one atomic, no waiting) normalises into the
-// window scores while it merges the splits.
+// an mbarrier; eleven consumer warps take items (a window, or two Quantized INT2 windows) from a
+// shared queue, wait for their chunks, compute, and release the slots.  The G query heads of the KV
+// head ride on the N side of mma.m16n8k16 (tokens on M for Q K^T, dims on M for P V), so both
+// products run on tensor cores.  Softmax is online per warp; per-window masses are kept as
+// log2-sum-exp values, normalised into the window scores when the scores are flushed.  The last CTA
+// of the (sequence, KV head) to finish (counted with one atomic, no waiting) merges the splits and
+// stores the step's merged max and 1/L for that flush.
 // With pre-RoPE Quantized keys (QEvict §4.3 "Cache Execution") the kernel variant ROPE rotates the
 // dequantised keys to their positions in registers before the key MMAs.
 #include "cache_dev.cuh"
@@ -242,17 +243,6 @@ __device__ __forceinline__ void lut_k_regs(uint32_t sel01, uint32_t sel23, const
   hi = __byte_perm(TB.z, TB.w, sel23);
   a2 = __byte_perm(lo, hi, 0x5140);
   a3 = __byte_perm(lo, hi, 0x7362);
-}
-
-// Value codes as exact fp16 integers: mask two codes into fp16 mantissas under exponent 2^10
-// (value 1024 + 4^p c), then one packed fma (x - 1024) * 4^-p recovers c exactly.
-__device__ __forceinline__ uint32_t dq_v(uint32_t w, int p) {
-  static constexpr uint32_t SCL[5] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u, 0x1C001C00u};
-  static constexpr uint32_t OFF[5] = {0xE400E400u, 0xDC00DC00u, 0xD400D400u, 0xCC00CC00u, 0xC400C400u};
-  const uint32_t x = (w & (0x00030003u << (2 * p))) | 0x64006400u;
-  uint32_t r;
-  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(x), "r"(SCL[p]), "r"(OFF[p]));
-  return r;
 }
 
 // INT4 value codes as exact fp16 integers: the codes at nibble p (0 or 1) of both fp16 halves land
