@@ -4,11 +4,12 @@
 // QEvict (arXiv 2608.05326) §4.1: o = softmax(q K_acc^T / sqrt(d)) V_acc over the accessible set;
 // §4.2 Eq. (1): the window score accumulates (1/H_q) sum_h sum_{i in w} a^h(i).
 //
-// Grid (n_split, h_kv, batch).  Each CTA owns a proportional slice of the recent, Full and
-// Quantized windows of one (sequence, KV head).  One producer warp streams the slice's windows
-// through a CTA-wide ring of 4 KB shared-memory slots with 1-D bulk copies (TMA), each completing on
-// an mbarrier; eleven consumer warps take items (a window, or two Quantized INT2 windows) from a
-// shared queue, wait for their chunks, compute, and release the slots.  The G query heads of the KV
+// Grid (n_split, h_kv, batch); at batch 1 (h_kv, 1, n_split), so that the CTAs dispatched last are
+// one split of every KV head.  Each CTA owns a slice of the recent, Full and Quantized windows of
+// one (sequence, KV head), proportional to its split's weight.  One producer warp streams the
+// slice's windows through a CTA-wide ring of 4 KB shared-memory slots with 1-D bulk copies (TMA),
+// each completing on an mbarrier; eleven consumer warps take items (a window, or two Quantized INT2
+// windows) from a shared queue, wait for their chunks, compute, and release the slots.  The G query heads of the KV
 // head ride on the N side of mma.m16n8k16 (tokens on M for Q K^T, dims on M for P V), so both
 // products run on tensor cores.  Softmax is online per warp; per-window masses are kept as
 // log2-sum-exp values, normalised into the window scores when the scores are flushed.  The last CTA
@@ -453,7 +454,9 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gl = lane >> 2, tl = lane & 3;
-  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const bool one_seq = C.B == 1;
+  const int split = one_seq ? blockIdx.z : blockIdx.x, g = one_seq ? blockIdx.x : blockIdx.y,
+            b = one_seq ? 0 : blockIdx.z;
   const int unit = io.layer * C.B + b;
   const int G = C.G;
   // Programmatic dependent launch.  This kernel may start while the previous kernel in the stream
@@ -492,26 +495,34 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   const int jn = (T - C.n_sink) / W;   // window of the new token at position T
   const int j0 = n_route;
   const int nL = jn - n_route + 1;
-  // this CTA's proportional slice of every class; item ids: 0 sink, 1..nL recent, then F, then Q
+  // this CTA's slice of every class; item ids: 0 sink, 1..nL recent, then F, then Q.  Slice
+  // weights, in sixteenths of a share.  At batch 1 the last split takes 11: its CTAs are
+  // dispatched last, onto the SMs that the previous layer's split merges free, so they start about a
+  // microsecond after the others and without copies issued before the programmatic-launch wait.
+  // (At larger batches the previous kernel merges on B * h_kv SMs and every loop is long: equal
+  // shares.)  n is at most the router's window capacity, so the products fit 32 bits.
   const int ns = C.n_split;
-  const int L0 = split * nL / ns, L1 = (split + 1) * nL / ns;
-  const int F0 = split * nF / ns, F1 = (split + 1) * nF / ns;
-  const int Q0 = split * nQ / ns, Q1 = (split + 1) * nQ / ns;
+  const int last_w = one_seq ? 11 : 16, wtot = 16 * (ns - 1) + last_w;
+  auto cut = [&](int s, int n) { return s >= ns ? n : (int)((unsigned)n * (16u * s) / (unsigned)wtot); };
+  const int L0 = cut(split, nL), L1 = cut(split + 1, nL);
+  const int F0 = cut(split, nF), F1 = cut(split + 1, nF);
+  const int Q0 = cut(split, nQ), Q1 = cut(split + 1, nQ);
   const int has_sink = split == 0 ? 1 : 0;
   // Quantized windows per queue item: INT2 windows without RoPE go in pairs, whose MMA chains and
   // softmax a warp runs together; the last item of an odd count holds one window
   constexpr int QPER = (BITS == 2 && !ROPE) ? 2 : 1;
-  const int cta_items = has_sink + (L1 - L0) + (F1 - F0) + (Q1 - Q0 + QPER - 1) / QPER;
+  const int nq = Q1 - Q0, nqi = (nq + QPER - 1) / QPER;   // Quantized windows and items of this CTA
+  const int cta_items = has_sink + nqi + (L1 - L0) + (F1 - F0);
+  // queue order [sink][Quantized][recent][Full]: the short bf16 items come last and fill the tail
   auto item_of = [&](int k) -> int {   // the item's (first) window
     if (has_sink) {
       if (k == 0) return 0;
       k -= 1;
     }
+    if (k < nqi) return 1 + nL + nF + Q0 + QPER * k;
+    k -= nqi;
     if (k < L1 - L0) return 1 + L0 + k;
-    k -= L1 - L0;
-    if (k < F1 - F0) return 1 + nL + F0 + k;
-    k -= F1 - F0;
-    return 1 + nL + nF + Q0 + QPER * k;
+    return 1 + nL + F0 + (k - (L1 - L0));
   };
 
   uint8_t *slots = smem;
@@ -521,7 +532,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   uint64_t *empty = full + Dg::FULL;                                    // [DEC_SLOTS]
   __shared__ int q_next;    // next queue position to hand to a consumer warp
 
-  // ---- chunk stream.  The CTA's windows in queue order [sink][recent][Full][Quantized]; a bf16
+  // ---- chunk stream.  The CTA's windows in queue order [sink][Quantized][recent][Full]; a bf16
   // window is KCH K chunks then KCH V chunks (4 KB each), a Quantized window QCH chunks of its
   // ledger record, the sink none.  Chunk c lives in slot c % DEC_SLOTS and completes on
   // full[c % Dg::FULL].
@@ -530,19 +541,20 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
   auto chunk_start = [&](int pos) -> int {
     const int k = pos - has_sink;
     if (k <= 0) return 0;
-    return k <= nb ? BFC * k : BFC * nb + QCH * QPER * (k - nb);
+    return k <= nqi ? QCH * min(QPER * k, nq) : QCH * nq + BFC * (k - nqi);
   };
   // global source of chunk c
   auto chunk_src = [&](int c, const void *&src, uint32_t &bytes) {
-    // the window of chunk c: a bf16 window's item, or Quantized window (c - BFC nb) / QCH of the CTA
-    // (chunks count windows, not queue items, which pair Quantized windows)
+    // the window of chunk c: Quantized window c / QCH of the CTA (chunks count windows, not queue
+    // items, which pair Quantized windows), then the bf16 windows
     int it, sub;
-    if (c < BFC * nb) {
-      it = item_of(has_sink + c / BFC);
-      sub = c % BFC;
+    if (c < QCH * nq) {
+      it = 1 + nL + nF + Q0 + c / QCH;
+      sub = c % QCH;
     } else {
-      it = 1 + nL + nF + Q0 + (c - BFC * nb) / QCH;
-      sub = (c - BFC * nb) % QCH;
+      const int bi = (c - QCH * nq) / BFC;   // bf16 window of the CTA: recent, then Full
+      it = bi < L1 - L0 ? 1 + L0 + bi : 1 + nL + F0 + (bi - (L1 - L0));
+      sub = (c - QCH * nq) % BFC;
     }
     if (it <= nL) {
       const int rs = (j0 + it - 1) % C.ring_windows;
@@ -1186,7 +1198,7 @@ static cudaError_t launch_decode_fmt(const CacheDev &C, const DecodeIO &io, cuda
   const cudaError_t e = optin.ensure(kern, Dg::SMEM);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(C.n_split, C.h_kv, C.B);
+  cfg.gridDim = C.B == 1 ? dim3(C.h_kv, 1, C.n_split) : dim3(C.n_split, C.h_kv, C.B);
   cfg.blockDim = dim3(DEC_WARPS * 32);
   cfg.dynamicSmemBytes = Dg::SMEM;
   cfg.stream = stream;
