@@ -257,9 +257,18 @@ __device__ __forceinline__ uint32_t dq_v4(uint32_t w, int p) {
   return r;
 }
 
-// Byte r of a word holding one 4-bit code per byte, as an exact float (mantissa of 2^23 + c).
-__device__ __forceinline__ float nib_f(uint32_t bytes4, int r) {
-  return __uint_as_float(__byte_perm(bytes4, 0x4B000000u, 0x7540u | r)) - 8388608.0f;
+// Byte r of two words holding one 4-bit code per byte, as exact floats: the mantissa of 2^23 + c, less
+// 2^23 in one packed subtraction.
+__device__ __forceinline__ void nib_f2(uint32_t e, uint32_t o, int r, float &ce, float &co) {
+  ce = __uint_as_float(__byte_perm(e, 0x4B000000u, 0x7540u | r));
+  co = __uint_as_float(__byte_perm(o, 0x4B000000u, 0x7540u | r));
+  sub2(ce, co, ce, co, 8388608.0f, 8388608.0f);
+}
+// bf16(fp32(c * s + m)) of two channels (c exact floats), packed low / high, each FMA rounded on its own
+__device__ __forceinline__ uint32_t dq_k4(float c0, float c1, float s0, float s1, float m0, float m1) {
+  float d0, d1;
+  fma2(d0, d1, c0, c1, s0, s1, m0, m1);
+  return pack_bf16(d0, d1);
 }
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
@@ -282,20 +291,29 @@ __device__ __forceinline__ void ktab_int2(const uint8_t *ch, uint8_t *tbl, int l
   using Gm = Geo<32, 2>;
   const uint2 sp = *reinterpret_cast<const uint2 *>(ch + Gm::OFF_KS + 8 * lane);
   const uint2 mp = *reinterpret_cast<const uint2 *>(ch + Gm::OFF_KM + 8 * lane);
-  uint32_t *tw = reinterpret_cast<uint32_t *>(tbl);
+  float sc[4] = {h2f_lo(sp.x), h2f_hi(sp.x), h2f_lo(sp.y), h2f_hi(sp.y)};
+  float mn[4] = {h2f_lo(mp.x), h2f_hi(mp.x), h2f_lo(mp.y), h2f_hi(mp.y)};
+  float v1[4], v2[4], v3[4];   // c*s + m for c = 1, 2, 3, each product and sum rounded on its own
+#pragma unroll
+  for (int k = 0; k < 4; k += 2) {
+    v1[k] = sc[k], v1[k + 1] = sc[k + 1];
+    add2(v1[k], v1[k + 1], mn[k], mn[k + 1]);
+    fma2(v2[k], v2[k + 1], 2.f, 2.f, sc[k], sc[k + 1], mn[k], mn[k + 1]);
+    fma2(v3[k], v3[k + 1], 3.f, 3.f, sc[k], sc[k + 1], mn[k], mn[k + 1]);
+  }
+  uint32_t lo[4], hi[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const uint32_t sw = k < 2 ? sp.x : sp.y, mw = k < 2 ? mp.x : mp.y;
-    const float sc = (k & 1) ? h2f_hi(sw) : h2f_lo(sw);
-    const float mn = (k & 1) ? h2f_hi(mw) : h2f_lo(mw);
-    const uint32_t p01 = pack_bf16(mn, __fadd_rn(sc, mn));
-    const uint32_t p23 = pack_bf16(__fmaf_rn(2.f, sc, mn), __fmaf_rn(3.f, sc, mn));
-    const int d = 4 * lane + k, j = d >> 4, c16 = d & 15;
-    const int t = (c16 & 7) >> 1, which = c16 >> 3, half = c16 & 1;
-    const int base = (j * 4 + t) * 8 + which * 4 + half;
-    tw[base] = __byte_perm(p01, p23, 0x6420);
-    tw[base + 2] = __byte_perm(p01, p23, 0x7531);
+    const uint32_t p01 = pack_bf16(mn[k], v1[k]), p23 = pack_bf16(v2[k], v3[k]);
+    lo[k] = __byte_perm(p01, p23, 0x6420);
+    hi[k] = __byte_perm(p01, p23, 0x7531);
   }
+  // channel d = 4 lane + k sits at k-step j = lane / 4, lane class t = 2 (lane & 1) + k / 2, channel pair
+  // (lane / 2) & 1, value half k & 1: channels k = 0, 1 fill one 16-byte run (low bytes, then high
+  // bytes), k = 2, 3 the run 32 bytes on
+  uint4 *tw = reinterpret_cast<uint4 *>(tbl) + ((lane >> 2) * 4 + 2 * (lane & 1)) * 2 + ((lane >> 1) & 1);
+  tw[0] = make_uint4(lo[0], lo[1], hi[0], hi[1]);
+  tw[2] = make_uint4(lo[2], lo[3], hi[2], hi[3]);
 }
 
 // S^T = K q^T over the 32 tokens of NW INT2 windows at once (their MMA chains interleave): exact
@@ -976,10 +994,12 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
 #pragma unroll
               for (int r = 0; r < 4; ++r) {
                 const bool h8 = r >= 2;   // channels 2t + 8, 2t + 9
-                const float a0 = bf_round(__fmaf_rn(nib_f(Ea, r), h8 ? sa.z : sa.x, h8 ? ma.z : ma.x));
-                const float a1 = bf_round(__fmaf_rn(nib_f(Oa, r), h8 ? sa.w : sa.y, h8 ? ma.w : ma.y));
-                const float b0 = bf_round(__fmaf_rn(nib_f(Eb, r), h8 ? sb.z : sb.x, h8 ? mb.z : mb.x));
-                const float b1 = bf_round(__fmaf_rn(nib_f(Ob, r), h8 ? sb.w : sb.y, h8 ? mb.w : mb.y));
+                float ca0, ca1, cb0f, cb1f;
+                nib_f2(Ea, Oa, r, ca0, ca1);
+                nib_f2(Eb, Ob, r, cb0f, cb1f);
+                const uint32_t pa = dq_k4(ca0, ca1, h8 ? sa.z : sa.x, h8 ? sa.w : sa.y, h8 ? ma.z : ma.x, h8 ? ma.w : ma.y);
+                const uint32_t pbk = dq_k4(cb0f, cb1f, h8 ? sb.z : sb.x, h8 ? sb.w : sb.y, h8 ? mb.z : mb.x, h8 ? mb.w : mb.y);
+                const float a0 = bf16_lo(pa), a1 = bf16_hi(pa), b0 = bf16_lo(pbk), b1 = bf16_hi(pbk);
                 rope_rot(a0, a1, b0, b1, h8 ? cb1 : cb0, h8 ? ncb1 : ncb0, rel_cs(rel, 16 * mt + gl + 8 * (r & 1), jj, r >> 1, tl),
                          ka[r], kb[r]);
               }
@@ -993,10 +1013,13 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
             const uint32_t E = w & 0x0F0F0F0Fu, Od = (w >> 4) & 0x0F0F0F0Fu;
             const float4 sc = *reinterpret_cast<const float4 *>(tbl + (j * 4 + tl) * 32);
             const float4 mn = *reinterpret_cast<const float4 *>(tbl + (j * 4 + tl) * 32 + 16);
-            const uint32_t a0 = pack_bf16(__fmaf_rn(nib_f(E, 0), sc.x, mn.x), __fmaf_rn(nib_f(Od, 0), sc.y, mn.y));
-            const uint32_t a1 = pack_bf16(__fmaf_rn(nib_f(E, 1), sc.x, mn.x), __fmaf_rn(nib_f(Od, 1), sc.y, mn.y));
-            const uint32_t a2 = pack_bf16(__fmaf_rn(nib_f(E, 2), sc.z, mn.z), __fmaf_rn(nib_f(Od, 2), sc.w, mn.w));
-            const uint32_t a3 = pack_bf16(__fmaf_rn(nib_f(E, 3), sc.z, mn.z), __fmaf_rn(nib_f(Od, 3), sc.w, mn.w));
+            float c[4][2];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) nib_f2(E, Od, r, c[r][0], c[r][1]);
+            const uint32_t a0 = dq_k4(c[0][0], c[0][1], sc.x, sc.y, mn.x, mn.y);
+            const uint32_t a1 = dq_k4(c[1][0], c[1][1], sc.x, sc.y, mn.x, mn.y);
+            const uint32_t a2 = dq_k4(c[2][0], c[2][1], sc.z, sc.w, mn.z, mn.w);
+            const uint32_t a3 = dq_k4(c[3][0], c[3][1], sc.z, sc.w, mn.z, mn.w);
             mma_bf16(s[mt], a0, a1, a2, a3, qb[j][0], qb[j][1]);
           }
           }
