@@ -356,11 +356,36 @@ def traffic_from_profile(kernel_sha):
     return d.get("dram_bytes_per_launch") if d.get("kernel_source_sha") == kernel_sha else None
 
 
+def _strip_comments(src: str) -> str:
+    """C++ source without comments, trailing blanks or blank lines (string literals kept)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"' or c == "'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            while i < n and src[i] != "\n":
+                i += 1
+        elif src.startswith("/*", i):
+            k = src.find("*/", i + 2)
+            i = n if k < 0 else k + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(ln.rstrip() for ln in "".join(out).split("\n") if ln.strip())
+
+
 def kernel_sha():
+    """Hash of the decode kernel's code (decode.cu, common.cuh, cache_dev.cuh), comments and blank lines
+    left out, so that a DRAM capture stays tied to the code it measured."""
     h = hashlib.sha256()
     for f in ("decode.cu", "common.cuh", "cache_dev.cuh"):
-        with open(os.path.join(ROOT, "recoverable_quantized_kv_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "recoverable_quantized_kv_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(_strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

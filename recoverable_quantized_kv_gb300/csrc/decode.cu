@@ -9,12 +9,13 @@
 // one (sequence, KV head), proportional to its split's weight.  One producer warp streams the
 // slice's windows through a CTA-wide ring of 4 KB shared-memory slots with 1-D bulk copies (TMA),
 // each completing on an mbarrier; eleven consumer warps take items (a window, or two Quantized INT2
-// windows) from a shared queue, wait for their chunks, compute, and release the slots.  The G query heads of the KV
-// head ride on the N side of mma.m16n8k16 (tokens on M for Q K^T, dims on M for P V), so both
-// products run on tensor cores.  Softmax is online per warp; per-window masses are kept as
-// log2-sum-exp values, normalised into the window scores when the scores are flushed.  The last CTA
-// of the (sequence, KV head) to finish (counted with one atomic, no waiting) merges the splits and
-// stores the step's merged max and 1/L for that flush.
+// windows; the Quantized items first, the bf16 windows last) from a shared queue, wait for their
+// chunks, compute, and release the slots.  The G query heads of the KV head ride on the N side of
+// mma.m16n8k16 (tokens on M for Q K^T, dims on M for P V), so both products run on tensor cores.
+// Softmax is online per warp; per-window masses are kept as log2-sum-exp values, normalised into the
+// window scores when the scores are flushed.  The last CTA of the (sequence, KV head) to finish
+// (counted with one atomic, no waiting) merges the splits and stores the step's merged max and 1/L
+// for that flush.
 // With pre-RoPE Quantized keys (QEvict §4.3 "Cache Execution") the kernel variant ROPE rotates the
 // dequantised keys to their positions in registers before the key MMAs.
 #include "cache_dev.cuh"
