@@ -26,7 +26,6 @@ cudaError_t launch_prefill_scores(const CacheDev &C, const __nv_bfloat16 *q, con
 cudaError_t launch_decode(const CacheDev &C, const DecodeIO &io, cudaStream_t s);
 cudaError_t launch_flush(const CacheDev &C, cudaStream_t s);
 int route_max_windows();
-int decode_warps();
 cudaError_t launch_diag_collect(const CacheDev &R, const DiagDev &Dg, cudaStream_t s);
 cudaError_t launch_diag_event(const CacheDev &P, const CacheDev &R, const DiagDev &Dg, int e, cudaStream_t s);
 }  // namespace qv

@@ -421,10 +421,6 @@ __device__ __forceinline__ void pv_int2(const float (&p)[2][4], const uint8_t *c
   }
 }
 
-__device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
-__device__ __forceinline__ float bf_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
-
 // cos/sin of the in-window offset tt for channels 16jj + 2tl + 8hh and + 1, as (cos, cos, sin, sin) of the
 // two channels, from the offset table:
 // 16 B per (offset, k-step jj, channel half, lane class), the two halves swapped on odd offsets so
@@ -912,7 +908,7 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             const int tt = 16 * mt + gl + 8 * (r & 1);
-            rope_rot(bf_lo(ka[r]), bf_hi(ka[r]), bf_lo(kb[r]), bf_hi(kb[r]), (r >> 1) ? cb1 : cb0, (r >> 1) ? ncb1 : ncb0,
+            rope_rot(bf16_lo(ka[r]), bf16_hi(ka[r]), bf16_lo(kb[r]), bf16_hi(kb[r]), (r >> 1) ? cb1 : cb0, (r >> 1) ? ncb1 : ncb0,
                      rel_cs(rel, tt, jj, r >> 1, tl), ka[r], kb[r]);
           }
           mma_bf16(s[mt], ka[0], ka[1], ka[2], ka[3], qb[jj][0], qb[jj][1]);
@@ -1211,8 +1207,6 @@ __global__ void __launch_bounds__(DEC_WARPS * 32, 1) decode_kernel(const CacheDe
     if (g == 0) meta[M_T] = T + 1;
   }
 }
-
-int decode_warps() { return DEC_WARPS; }
 
 template <int W, int BITS, bool ROPE>
 static cudaError_t launch_decode_fmt(const CacheDev &C, const DecodeIO &io, cudaStream_t stream) {
